@@ -1,0 +1,412 @@
+"""Benchmark of the CP state-correction pass on GB300.
+
+Workload: 32 heads, K = V = 128, S = 8 segments (32K tokens at 4K per segment),
+fp32 states.  One step is the whole hot path over one batch: four calls of the
+C ABI -- forward kv and forward vk on Householder-type M (g (I - beta u u^T)),
+reverse kv and reverse vk on M = 0.99 Q (Q Haar-orthogonal) -- each on its own
+input set.  The metric is microseconds per call (lower is better), with the
+achieved HBM bandwidth of the kernel against the measured copy bandwidth.
+
+Timing: inputs resident in HBM; each step replays a CUDA graph of its four
+calls; steps rotate through enough input/output replicas that every call's
+buffers were last touched far more than an L2's worth of traffic earlier (the
+rotation spans at least 3x the L2 size), so every call reads from DRAM.  Time
+is taken with CUDA events on the launching stream, warm-up excluded.
+
+``--impl reference`` times the fp64 CPU oracle instead (the only reference
+this computation has), on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+HEADS, K, V, S = 32, 128, 128, 8
+CALLS = (("c1", "kv", "fwd"), ("c1", "vk", "fwd"), ("c2", "kv", "rev"), ("c2", "vk", "rev"))
+METRIC = "µs per call and achieved HBM GB/s (fraction of roofline) at 32 heads, K=V=128"
+WORKLOAD = ("CP state correction, B=1, 32 heads, K=V=128, S=8 (32K tokens / 4K per segment), fp32; "
+            "step = fwd kv + fwd vk (Householder M) + rev kv + rev vk (0.99*orthogonal M)")
+
+
+def algorithmic_bytes(chains, S_, K_, V_, with_init=True):
+    """Bytes one call must move: H and M of the S-1 segments it visits, every
+    output state, and h_init."""
+    return 4 * chains * ((S_ - 1) * K_ * V_ + (S_ - 1) * K_ * K_ + S_ * K_ * V_ + (K_ * V_ if with_init else 0))
+
+
+def algorithmic_flops(chains, S_, K_, V_):
+    return 2 * chains * (S_ - 1) * K_ * K_ * V_
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append((time.time(), ln.strip()))
+
+    def mark(self, name):
+        self.marks.append((name, time.time()))
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        t0 = dict(self.marks).get("start", 0)
+        t1 = dict(self.marks).get("end", time.time())
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ts, ln in self.lines:
+            if not (t0 <= ts <= t1 + 0.06):
+                continue
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def make_problem_set():
+    """The four calls' seeded inputs (numpy, host)."""
+    import qla_inputs as qi
+    probs = []
+    for name, layout, direction in CALLS:
+        H, M, h0 = qi.make_inputs(qi.WORKLOADS[name], layout)
+        probs.append(dict(name=name, layout=layout, direction=direction, H=H, M=M, h0=h0))
+    return probs
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import linear_attention_context_gb300 as qla
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    probs = make_problem_set()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_call = sum(p["H"].nbytes * 2 + p["M"].nbytes + p["h0"].nbytes for p in probs) / len(probs)
+    reps = max(2, math.ceil(3 * l2 / (per_call * len(probs))))
+    bufs = []
+    for r in range(reps):
+        row = []
+        for p in probs:
+            row.append(dict(H=torch.from_numpy(p["H"]).to(dev), M=torch.from_numpy(p["M"]).to(dev),
+                            h0=torch.from_numpy(p["h0"]).to(dev), out=torch.empty(p["H"].shape, device=dev),
+                            layout=p["layout"], direction=p["direction"]))
+        bufs.append(row)
+    stream = torch.cuda.Stream(dev)
+    kw = dict(engine=args.engine, variant=args.variant, release=args.release)
+
+    def call(b, s=None):
+        qla.cp_correct(b["H"], b["M"], b["h0"], b["out"], layout=b["layout"], direction=b["direction"],
+                       stream=s, **kw)
+
+    # correctness first (untimed): every replica's outputs against the oracle
+    # on the first head (full check happens in the tests)
+    with torch.cuda.stream(stream):
+        for row in bufs:
+            for b in row:
+                call(b, stream)
+    stream.synchronize()
+    if rank == 0 and not args.skip_check:
+        import oracle
+        from_qla = bufs[0]
+        for p, b in zip(probs, from_qla):
+            sl = (slice(0, 1), slice(0, 2))
+            ref, _ = oracle.cp_correct(p["H"][sl], p["M"][sl], p["h0"][sl], p["layout"], p["direction"])
+            got = b["out"][sl].cpu().numpy().astype(np.float64)
+            err = np.sqrt(((got - ref) ** 2).sum()) / np.sqrt((ref ** 2).sum())
+            if not err <= 1e-5:
+                raise SystemExit(f"bench pre-check failed for {p['name']} {p['layout']} {p['direction']}: {err}")
+
+    # one CUDA graph per replica: the step's four calls
+    graphs = []
+    with torch.cuda.stream(stream):
+        for row in bufs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for b in row:
+                    call(b, stream)
+            graphs.append(g)
+    stream.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    with torch.cuda.stream(stream):
+        for w in range(args.warmup):
+            graphs[w % reps].replay()
+    stream.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.mark("start")
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for s in range(args.steps):
+            graphs[s % reps].replay()
+        e1.record(stream)
+    stream.synchronize()
+    if sampler:
+        sampler.mark("end")
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    ms = max_over_ranks(ms, world)
+    clocks = sampler.stop() if sampler else None
+
+    n_calls = args.steps * len(CALLS)
+    us_per_call_rank = ms * 1e3 / n_calls
+    value = ms * 1e3 / (n_calls * world)  # whole job: all ranks' calls over the slowest rank's time
+    var, eng = qla.resolve(1, HEADS, S, K, V, "kv")
+    if args.engine != "auto":
+        eng = args.engine
+    if args.variant != "auto":
+        var = args.variant
+    launches_per_call = 1 if var == "seq" else 4
+    bytes_call = algorithmic_bytes(HEADS, S, K, V)
+    achieved = bytes_call / (us_per_call_rank * 1e-6) / 1e9
+    peak, peak_kind = load_peaks()
+
+    # end-to-end through the public API with host buffers: pinned host inputs
+    # copied in and outputs copied out inside the timed region
+    e2e = None
+    if not args.skip_e2e:
+        hin = [dict(H=torch.from_numpy(p["H"]).pin_memory(), M=torch.from_numpy(p["M"]).pin_memory(),
+                    h0=torch.from_numpy(p["h0"]).pin_memory(), out=torch.empty(p["H"].shape).pin_memory())
+               for p in probs]
+        row = bufs[0]
+        e2e_steps = max(3, min(args.steps, 50))
+
+        def e2e_step():
+            for h, b in zip(hin, row):
+                b["H"].copy_(h["H"], non_blocking=True)
+                b["M"].copy_(h["M"], non_blocking=True)
+                b["h0"].copy_(h["h0"], non_blocking=True)
+                call(b, stream)
+                h["out"].copy_(b["out"], non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                e2e_step()
+        stream.synchronize()
+        barrier(world)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a0.record(stream)
+            for _ in range(e2e_steps):
+                e2e_step()
+            a1.record(stream)
+        stream.synchronize()
+        ems = max_over_ranks(a0.elapsed_time(a1), world)
+        h2d = sum(h["H"].nbytes + h["M"].nbytes + h["h0"].nbytes for h in hin)
+        d2h = sum(h["out"].nbytes for h in hin)
+        e2e = {"value": round(ems * 1e3 / (e2e_steps * len(CALLS) * world), 3), "unit": "us",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and not args.skip_cpu:
+        cpu = cpu_baseline(probs, budget_s=args.cpu_budget)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "us", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 6),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; Householder and 0.99*orthogonal M, N(0,1)*0.1 states)",
+            "config": {"workload": WORKLOAD, "B": 1, "heads": HEADS, "K": K, "V": V, "S": S,
+                       "calls_per_step": len(CALLS), "variant": var, "engine": eng, "release": args.release,
+                       "l2_defeat": f"inputs larger than L2: {reps} rotating replicas x {len(CALLS)} calls "
+                                    f"({reps * len(CALLS) * per_call / 1e6:.0f} MB) vs L2 {l2 / 1e6:.0f} MB",
+                       "graph": "one CUDA graph per step (its 4 calls)",
+                       "parallelism": f"replicas x{world} (no collective)"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": args.traffic,
+                         "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                                        if peak_kind == "measured" else "fallback 6.8 TB/s",
+                         "algorithmic_bytes_per_launch": bytes_call, "launches_per_call": launches_per_call,
+                         "avg_launch_us": round(us_per_call_rank / launches_per_call, 3),
+                         "flops_per_call": algorithmic_flops(HEADS, S, K, V)},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_calls * launches_per_call, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def cpu_baseline(probs, budget_s=20.0):
+    """The oracle as it stands, on this host's cores, on the same four calls.
+    Runs whole calls (all 32 heads) when they fit the budget, else a head
+    sample; returns microseconds per full call."""
+    import oracle
+    t0 = time.perf_counter()
+    p = probs[0]
+    _, _, threads = oracle.cp_correct(p["H"][:, :1], p["M"][:, :1], p["h0"][:, :1], p["layout"], p["direction"],
+                                      return_threads=True)
+    per_head = time.perf_counter() - t0  # single head, one thread busy
+    heads = HEADS
+    est = per_head * HEADS * len(probs) / max(1, min(threads, HEADS))
+    if est > budget_s:
+        heads = max(threads, int(HEADS * budget_s / est))
+        heads = min(HEADS, heads)
+    t = time.perf_counter()
+    for q in probs:
+        oracle.cp_correct(q["H"][:, :heads], q["M"][:, :heads], q["h0"][:, :heads], q["layout"], q["direction"])
+    el = time.perf_counter() - t
+    us_per_call = el / len(probs) * (HEADS / heads) * 1e6
+    return {"value": round(us_per_call, 1), "unit": "us", "cores": threads, "kind": "oracle",
+            "sample": f"{len(probs)} calls x {heads} of {HEADS} heads (fp64 oracle, {threads} threads), "
+                      f"scaled to a full call"}
+
+
+def run_reference(args):
+    """The oracle timed as the reference arm: K steps after W warm-up steps,
+    each step one bounded sample (a block of heads of one of the four calls,
+    rotating), reported per full call."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    probs = make_problem_set()
+    # calibrate: one head of one call
+    p = probs[0]
+    t0 = time.perf_counter()
+    _, _, threads = oracle.cp_correct(p["H"][:, :1], p["M"][:, :1], p["h0"][:, :1], p["layout"], p["direction"],
+                                      return_threads=True)
+    one = time.perf_counter() - t0
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    heads = max(1, min(HEADS, threads, int(budget / max(one, 1e-9))))
+    times = []
+    for s in range(args.warmup + args.steps):
+        q = probs[s % len(probs)]
+        t = time.perf_counter()
+        oracle.cp_correct(q["H"][:, :heads], q["M"][:, :heads], q["h0"][:, :heads], q["layout"], q["direction"])
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t)
+    total = sum(times)
+    us_per_call = total / len(times) * (HEADS / heads) * 1e6
+    line = {"impl": "reference", "metric": METRIC, "value": round(us_per_call, 1), "unit": "us", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / len(times) * 1e3, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; same inputs as the GPU arm)",
+            "config": {"workload": WORKLOAD, "B": 1, "heads": HEADS, "K": K, "V": V, "S": S,
+                       "calls_per_step": 1, "parallelism": "host threads"},
+            "cpu_baseline": {"value": round(us_per_call, 1), "unit": "us", "cores": threads, "kind": "oracle",
+                             "sample": f"each step: {heads} of {HEADS} heads of one call (rotating over the "
+                                       f"4 calls), scaled to a full call"},
+            "e2e": {"value": round(us_per_call, 1), "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--engine", default="auto")
+    ap.add_argument("--variant", default="auto")
+    ap.add_argument("--release", default="membar")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per launch of the current kernel build (read+write)")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-check", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,170 @@
+/*
+ * qla.h -- C ABI of the GB300 (sm_103a) context-parallel state-correction pass.
+ *
+ * The operation.  Antarx Memos, "一次 TileLang Warp Specialization 数值错误的定位
+ * 与修复：从双缓冲竞争到 membar", section "从版本升级后的数值偏差开始": a long
+ * sequence is split into S segments; each segment yields a local state H_i
+ * ("ht") and a K x K propagation matrix M_i ("mt"); one kernel corrects the
+ * segment-initial states on the forward pass and the segment-terminal states
+ * on the reverse pass, with the state stored K x V ("kv") or V x K ("vk").
+ * Section "理解三个缓冲区，才能判断哪里需要同步" gives the recurrence (its
+ * formula was lost in text extraction; the reading below follows the buffer
+ * roles the same section lists):
+ *
+ *     X_0 = h_init,   X_{i+1} = propagate(M_i, X_i) + H_i
+ *
+ *                    forward          reverse
+ *     kv (K x V)     M_i X            M_i^T X
+ *     vk (V x K)     X M_i^T          X M_i
+ *
+ * Outputs are exclusive, one state per segment, in H's shape:
+ *     forward  out[i] = X_i                                   i = 0..S-1
+ *     reverse  out[S-1] = h_init,
+ *              out[i] = propagate_rev(M_{i+1}, out[i+1]) + H_{i+1}
+ * so the forward pass never reads H_{S-1}, M_{S-1} and the reverse pass never
+ * reads H_0, M_0 -- unless the final state is requested (qla_cp_correct_ex),
+ * which is the state after the last segment: X_S going forward,
+ * propagate_rev(M_0, out[0]) + H_0 in reverse.
+ *
+ * Memory (all fp32, contiguous, row-major, DEVICE pointers owned by the caller):
+ *     H      [B][heads][S][K][V]  (kv)   or  [B][heads][S][V][K]  (vk)
+ *     M      [B][heads][S][K][K]         (independent of the layout)
+ *     h_init [B][heads][K][V]     (kv)   or  [B][heads][V][K]     (vk);  NULL = zeros
+ *     out    same shape as H
+ *
+ * Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t; NULL
+ * is the legacy default stream).  A status other than QLA_OK means nothing was
+ * launched.  Device-side faults surface at the caller's next synchronisation,
+ * as with any CUDA launch.
+ *
+ * Aliasing: out == H (exactly the same pointer) is supported and computes the
+ * same result as separate buffers: each tile's H_i is read before out[i] is
+ * written over it.  Any other overlap among H, M, h_init, out and final_state
+ * returns QLA_ERR_ALIAS.  H, M and h_init are never written.
+ *
+ * Limits: B, heads, S >= 1; K and V multiples of 32 in [32, 256]; every pointer
+ * 16-byte aligned; B*heads*S*K*max(K,V) < 2^62.  The device must be sm_103
+ * (GB300): checked once per device, QLA_ERR_ARCH otherwise.
+ */
+#ifndef QLA_H_
+#define QLA_H_
+
+#include <stddef.h>
+
+/* Exported symbols; everything else in the library has hidden visibility. */
+#if defined(__GNUC__)
+#define QLA_API __attribute__((visibility("default")))
+#else
+#define QLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { QLA_LAYOUT_KV = 0, QLA_LAYOUT_VK = 1 };
+enum { QLA_FORWARD = 0, QLA_REVERSE = 1 };
+
+enum {
+  QLA_OK = 0,
+  QLA_ERR_INVALID_ARG = -1, /* null pointer, non-positive size, unknown enum */
+  QLA_ERR_UNSUPPORTED = -2, /* K or V outside the supported set, engine not built for the shape */
+  QLA_ERR_ALIGNMENT = -3,   /* a pointer not 16-byte aligned */
+  QLA_ERR_ALIAS = -4,       /* overlapping buffers other than out == H */
+  QLA_ERR_CUDA = -5,        /* a CUDA runtime call failed; qla_last_error() has its text */
+  QLA_ERR_ARCH = -6,        /* the current device is not sm_103 */
+  QLA_ERR_TIMEOUT = -7      /* a bounded device-side wait gave up (see qla_device_status) */
+};
+
+/* Which algorithm computes the recurrence. */
+enum {
+  QLA_VARIANT_AUTO = 0, /* the library chooses from the shape */
+  QLA_VARIANT_SEQ = 1,  /* one sequential pass per (chain, column tile) */
+  QLA_VARIANT_SCAN = 2  /* group aggregates -> carry pass -> per-group re-run (small B*heads) */
+};
+
+/* Which kernel engine runs the sequential pass. */
+enum {
+  QLA_ENGINE_AUTO = 0,    /* tensor-core engine where the shape allows, else SIMT */
+  QLA_ENGINE_SIMT = 1,    /* plain FFMA kernel, no TMA: any supported K, V */
+  QLA_ENGINE_WS_SIMT = 2, /* warp-specialised TMA/mbarrier pipeline, FFMA propagate */
+  QLA_ENGINE_TC = 3       /* warp-specialised TMA/mbarrier pipeline, tcgen05 3xTF32 propagate */
+};
+
+/* How a consumer releases a double-buffer slot it has read with ordinary
+ * shared-memory loads, before the TMA producer may overwrite it (section
+ * "三个可用源码方案的具体差别" of the page above). */
+enum {
+  QLA_RELEASE_MEMBAR = 0, /* membar.cta, then mbarrier arrive (the page's adopted fix) */
+  QLA_RELEASE_PROXY = 1,  /* fence.proxy.async.shared::cta, then arrive */
+  QLA_RELEASE_DELAY = 2,  /* arrive only at the end of the step (longer slot lifetime) */
+  QLA_RELEASE_NONE = 3    /* mbarrier arrive alone (its default .release semantics) */
+};
+
+/*
+ * The state correction with the library's default choices.
+ * Arguments as described at the top of this file.  Returns QLA_OK or a
+ * negative QLA_ERR_* code; nothing is launched unless QLA_OK.
+ */
+QLA_API int qla_cp_correct(const float* H, const float* M, const float* h_init, float* out, int B,
+                   int heads, int S, int K, int V, int layout, int direction, void* stream);
+
+/*
+ * As qla_cp_correct, with explicit choices:
+ *   final_state  NULL, or a [B][heads][state] buffer that receives the state
+ *                after the last segment (reads H and M of the last segment
+ *                visited as well).  out may be NULL when final_state is not.
+ *   variant      QLA_VARIANT_*;  engine QLA_ENGINE_*;  release QLA_RELEASE_*
+ *                (ignored by engines without a TMA producer).
+ *   scan_group   segments per scan group (QLA_VARIANT_SCAN), 0 = automatic.
+ * The scan variant needs qla_scan_workspace_bytes() of device scratch, which
+ * it takes from the stream-ordered allocator (cudaMallocAsync on `stream`) and
+ * returns on the same stream.
+ */
+QLA_API int qla_cp_correct_ex(const float* H, const float* M, const float* h_init, float* out,
+                      float* final_state, int B, int heads, int S, int K, int V, int layout,
+                      int direction, int variant, int engine, int release, int scan_group,
+                      void* stream);
+
+/* Bytes of device scratch the scan variant uses for this shape and group
+ * size (0 = automatic); 0 when the scan does not apply. */
+QLA_API size_t qla_scan_workspace_bytes(int B, int heads, int S, int K, int V, int scan_group);
+
+/* The variant and engine QLA_*_AUTO resolve to for this shape on the current
+ * device (written to *variant and *engine; either may be NULL). */
+QLA_API int qla_resolve(int B, int heads, int S, int K, int V, int layout, int* variant, int* engine);
+
+/* Static text for a status code. */
+QLA_API const char* qla_status_string(int status);
+
+/* Detail of the last failure on the calling host thread ("" if none). */
+QLA_API const char* qla_last_error(void);
+
+/*
+ * Reads and clears the device-side status word of the current device, which
+ * a kernel sets when one of its bounded waits gives up (the kernel then drains
+ * its copies in flight and returns early, leaving its outputs incomplete).
+ * Synchronises the device.  *flags receives the word (0 = no event); returns
+ * QLA_ERR_TIMEOUT if it was non-zero, QLA_OK otherwise, QLA_ERR_CUDA on error.
+ */
+QLA_API int qla_device_status(int* flags);
+
+/*
+ * Self-test of the bounded waits: launches the warp-specialised pipeline on a
+ * tiny problem in a mode where one consumer waits on a barrier that nothing
+ * arrives on.  The wait gives up after `wait_limit_us` microseconds, the kernel
+ * records QLA_ERR_TIMEOUT in the device status word, drains and returns.  The
+ * buffers are as for qla_cp_correct with K = V = 128; returns the launch
+ * status.  Used by the tests to show that a stalled pipeline ends on its own.
+ */
+QLA_API int qla_selftest_stalled_wait(const float* H, const float* M, float* out, int S,
+                              int wait_limit_us, void* stream);
+
+/* ABI version of this header (major * 100 + minor). */
+QLA_API int qla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QLA_H_ */

@@ -1,0 +1,183 @@
+"""GB300 (sm_103a) context-parallel state-correction pass for chunked linear
+attention.
+
+This module is a thin binding of the C ABI in ``include/qla.h``: it checks and
+marshals torch tensors (device memory and the current CUDA stream) and calls
+the library.  Every step of the recurrence runs in the library's CUDA kernels;
+there is no CPU or PyTorch fallback, and the import fails loudly when the
+library has not been built.
+
+The recurrence (Antarx Memos, "一次 TileLang Warp Specialization 数值错误的定位与
+修复", sections "从版本升级后的数值偏差开始" and "理解三个缓冲区"):
+X_0 = h_init, X_{i+1} = propagate(M_i, X_i) + H_i, propagate = M X (kv) or
+X M^T (vk) forward and with M^T in reverse; out[i] is the state entering
+segment i in visiting order.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+LAYOUTS = {"kv": 0, "vk": 1}
+DIRECTIONS = {"fwd": 0, "rev": 1}
+VARIANTS = {"auto": 0, "seq": 1, "scan": 2}
+ENGINES = {"auto": 0, "simt": 1, "ws_simt": 2, "tc": 3}
+RELEASES = {"membar": 0, "proxy": 1, "delay": 2, "none": 3}
+
+QLA_OK = 0
+STATUS = {0: "QLA_OK", -1: "QLA_ERR_INVALID_ARG", -2: "QLA_ERR_UNSUPPORTED", -3: "QLA_ERR_ALIGNMENT",
+          -4: "QLA_ERR_ALIAS", -5: "QLA_ERR_CUDA", -6: "QLA_ERR_ARCH", -7: "QLA_ERR_TIMEOUT"}
+
+# Every function include/qla.h declares.
+EXPORTS = ("qla_cp_correct", "qla_cp_correct_ex", "qla_scan_workspace_bytes", "qla_resolve",
+           "qla_status_string", "qla_last_error", "qla_device_status", "qla_selftest_stalled_wait",
+           "qla_version")
+
+
+class QlaError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        super().__init__(f"{STATUS.get(status, status)}: {detail}")
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return _build.library_path()
+
+
+def lib():
+    """The loaded C library (ctypes).  Raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is missing: build it with __graft_entry__.build() "
+                              "(or python -m linear_attention_context_gb300._build)")
+        L = ctypes.CDLL(path)
+        vp, ci, cz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.qla_cp_correct.argtypes = [vp, vp, vp, vp] + [ci] * 7 + [vp]
+        L.qla_cp_correct.restype = ci
+        L.qla_cp_correct_ex.argtypes = [vp, vp, vp, vp, vp] + [ci] * 11 + [vp]
+        L.qla_cp_correct_ex.restype = ci
+        L.qla_scan_workspace_bytes.argtypes = [ci] * 6
+        L.qla_scan_workspace_bytes.restype = cz
+        L.qla_resolve.argtypes = [ci] * 6 + [ctypes.POINTER(ci), ctypes.POINTER(ci)]
+        L.qla_resolve.restype = ci
+        L.qla_status_string.argtypes = [ci]
+        L.qla_status_string.restype = ctypes.c_char_p
+        L.qla_last_error.argtypes = []
+        L.qla_last_error.restype = ctypes.c_char_p
+        L.qla_device_status.argtypes = [ctypes.POINTER(ci)]
+        L.qla_device_status.restype = ci
+        L.qla_selftest_stalled_wait.argtypes = [vp, vp, vp, ci, ci, vp]
+        L.qla_selftest_stalled_wait.restype = ci
+        L.qla_version.argtypes = []
+        L.qla_version.restype = ci
+        _LIB = L
+    return _LIB
+
+
+def last_error() -> str:
+    return lib().qla_last_error().decode()
+
+
+def check(status: int):
+    if status != QLA_OK:
+        raise QlaError(status, last_error())
+    return status
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _shape(H, M, layout):
+    if H.dim() != 5:
+        raise ValueError(f"H must be [B, heads, S, rows, cols], got {tuple(H.shape)}")
+    B, nh, S, r, c = H.shape
+    K, V = (r, c) if layout == "kv" else (c, r)
+    if tuple(M.shape) != (B, nh, S, K, K):
+        raise ValueError(f"M must be {(B, nh, S, K, K)}, got {tuple(M.shape)}")
+    return B, nh, S, K, V
+
+
+def _check_tensor(name, t, dev, shape=None):
+    import torch
+    if t is None:
+        return
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    if t.device != dev:
+        raise ValueError(f"{name} is on {t.device}, expected {dev}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def cp_correct(H, M, h_init=None, out=None, *, layout="kv", direction="fwd", final_state=None,
+               variant="auto", engine="auto", release="membar", scan_group=0, stream=None,
+               want_out=True):
+    """Corrected states for every segment (see the module docstring).
+
+    H: [B, heads, S, K, V] (kv) or [B, heads, S, V, K] (vk) float32 CUDA tensor;
+    M: [B, heads, S, K, K]; h_init: [B, heads, state] or None for zeros;
+    out: preallocated like H (may be H itself: in place), or None to allocate;
+    final_state: preallocated [B, heads, state] to also receive the state after
+    the last segment.  Runs on ``stream`` (default: torch's current stream) and
+    returns ``out`` (None when ``want_out`` is False)."""
+    import torch
+    if layout not in LAYOUTS or direction not in DIRECTIONS:
+        raise ValueError(f"layout {layout!r} / direction {direction!r}")
+    B, nh, S, K, V = _shape(H, M, layout)
+    dev = H.device
+    if dev.type != "cuda":
+        raise ValueError("H must be a CUDA tensor")
+    st = tuple(H.shape[3:])
+    _check_tensor("H", H, dev)
+    _check_tensor("M", M, dev)
+    _check_tensor("h_init", h_init, dev, (B, nh) + st)
+    _check_tensor("final_state", final_state, dev, (B, nh) + st)
+    if want_out and out is None:
+        out = torch.empty_like(H)
+    if out is not None:
+        _check_tensor("out", out, dev, H.shape)
+    with torch.cuda.device(dev):
+        rc = lib().qla_cp_correct_ex(_ptr(H), _ptr(M), _ptr(h_init), _ptr(out), _ptr(final_state),
+                                     B, nh, S, K, V, LAYOUTS[layout], DIRECTIONS[direction],
+                                     VARIANTS[variant], ENGINES[engine], RELEASES[release],
+                                     int(scan_group), _stream_handle(stream))
+    check(rc)
+    return out
+
+
+def scan_workspace_bytes(B, heads, S, K, V, scan_group=0) -> int:
+    return int(lib().qla_scan_workspace_bytes(B, heads, S, K, V, scan_group))
+
+
+def resolve(B, heads, S, K, V, layout="kv"):
+    """(variant, engine) names that 'auto' resolves to on the current device."""
+    v, e = ctypes.c_int(), ctypes.c_int()
+    check(lib().qla_resolve(B, heads, S, K, V, LAYOUTS[layout], ctypes.byref(v), ctypes.byref(e)))
+    inv_v = {b: a for a, b in VARIANTS.items()}
+    inv_e = {b: a for a, b in ENGINES.items()}
+    return inv_v[v.value], inv_e[e.value]
+
+
+def device_status() -> int:
+    """Reads and clears the device status word (synchronises); 0 = no event."""
+    f = ctypes.c_int()
+    rc = lib().qla_device_status(ctypes.byref(f))
+    if rc not in (QLA_OK, -7):
+        check(rc)
+    return f.value

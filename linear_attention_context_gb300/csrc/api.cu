@@ -1,0 +1,377 @@
+// Host side of the C ABI declared in include/qla.h: argument checks, the
+// per-device architecture check, variant/engine selection, the scan
+// orchestration and the device status word.  No compute happens here: every
+// step of the recurrence runs in the kernels of the other files.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "qla.h"
+#include "qla_internal.h"
+
+namespace qla {
+
+// Set by a kernel whose bounded wait gave up; read and cleared by
+// qla_device_status().  Kernels receive its device address as a parameter.
+__device__ unsigned int g_device_status;
+
+namespace {
+
+thread_local std::string t_last_error;
+
+int fail(int status, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(QLA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool probed = false;
+  bool is_sm103 = false;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  unsigned int* status_word = nullptr;
+};
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+
+// Probes the current device once: compute capability, SM count, status word.
+int current_device(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(QLA_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.probed) {
+    if ((e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(major)");
+    if ((e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(minor)");
+    if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(sm count)");
+    d.is_sm103 = (d.cc_major == 10 && d.cc_minor == 3);
+    if (d.is_sm103) {
+      void* p = nullptr;
+      if ((e = cudaGetSymbolAddress(&p, g_device_status)) != cudaSuccess)
+        return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+      d.status_word = static_cast<unsigned int*>(p);
+    }
+    d.probed = true;
+  }
+  if (!d.is_sm103)
+    return fail(QLA_ERR_ARCH, "device %d is sm_%d%d; this library is built for sm_103 (GB300) only", dev,
+                d.cc_major, d.cc_minor);
+  *out = &d;
+  return QLA_OK;
+}
+
+struct Range {
+  uintptr_t lo, hi;
+  const char* name;
+};
+
+bool overlap(const Range& a, const Range& b) { return a.lo < b.hi && b.lo < a.hi; }
+
+struct Shape {
+  int B, heads, S, K, V, layout, direction;
+  int64_t chains() const { return (int64_t)B * heads; }
+  int64_t state() const { return (int64_t)K * V; }
+};
+
+int check_args(const float* H, const float* M, const float* h_init, const float* out, const float* fin,
+               const Shape& s) {
+  if (s.B < 1 || s.heads < 1 || s.S < 1 || s.K < 1 || s.V < 1)
+    return fail(QLA_ERR_INVALID_ARG, "B, heads, S, K, V must be >= 1 (got %d, %d, %d, %d, %d)", s.B, s.heads, s.S,
+                s.K, s.V);
+  if (s.layout != QLA_LAYOUT_KV && s.layout != QLA_LAYOUT_VK)
+    return fail(QLA_ERR_INVALID_ARG, "layout must be QLA_LAYOUT_KV or QLA_LAYOUT_VK (got %d)", s.layout);
+  if (s.direction != QLA_FORWARD && s.direction != QLA_REVERSE)
+    return fail(QLA_ERR_INVALID_ARG, "direction must be QLA_FORWARD or QLA_REVERSE (got %d)", s.direction);
+  if (!H || !M) return fail(QLA_ERR_INVALID_ARG, "H and M must not be NULL");
+  if (!out && !fin) return fail(QLA_ERR_INVALID_ARG, "out and final_state are both NULL: nothing to compute");
+  if (s.K % 32 || s.K > 256 || s.V % 32 || s.V > 256)
+    return fail(QLA_ERR_UNSUPPORTED, "K and V must be multiples of 32 in [32, 256] (got K=%d, V=%d)", s.K, s.V);
+  const double elems = (double)s.chains() * s.S * s.K * std::max(s.K, s.V);
+  if (elems >= 4.6e18) return fail(QLA_ERR_INVALID_ARG, "problem too large for 64-bit indexing");
+  if (s.chains() * s.S > (int64_t)1 << 31) return fail(QLA_ERR_UNSUPPORTED, "B*heads*S must be below 2^31");
+  const void* ptrs[] = {H, M, h_init, out, fin};
+  const char* names[] = {"H", "M", "h_init", "out", "final_state"};
+  for (int i = 0; i < 5; ++i)
+    if (ptrs[i] && (reinterpret_cast<uintptr_t>(ptrs[i]) & 15))
+      return fail(QLA_ERR_ALIGNMENT, "%s is not 16-byte aligned", names[i]);
+  const uintptr_t sb = (uintptr_t)(s.chains() * s.S * s.state() * 4);
+  Range r[5];
+  int n = 0;
+  r[n++] = {(uintptr_t)H, (uintptr_t)H + sb, "H"};
+  r[n++] = {(uintptr_t)M, (uintptr_t)M + (uintptr_t)(s.chains() * s.S * s.K * s.K * 4), "M"};
+  if (h_init) r[n++] = {(uintptr_t)h_init, (uintptr_t)h_init + (uintptr_t)(s.chains() * s.state() * 4), "h_init"};
+  if (fin) r[n++] = {(uintptr_t)fin, (uintptr_t)fin + (uintptr_t)(s.chains() * s.state() * 4), "final_state"};
+  if (out && out != H) r[n++] = {(uintptr_t)out, (uintptr_t)out + sb, "out"};
+  for (int a = 0; a < n; ++a)
+    for (int b = a + 1; b < n; ++b)
+      if (overlap(r[a], r[b]))
+        return fail(QLA_ERR_ALIAS, "%s and %s overlap (only out == H is allowed)", r[a].name, r[b].name);
+  return QLA_OK;
+}
+
+// Scan group count for S segments: the critical path is about 2L + G steps
+// with G*L >= S, smallest near G = sqrt(2S).
+int auto_groups(int S) {
+  int G = std::max(1, (int)std::lround(std::sqrt(2.0 * S)));
+  const int L = (S + G - 1) / G;
+  return (S + L - 1) / L;
+}
+
+int resolve_engine(const Shape& s, int engine) {
+  (void)s;
+  if (engine == QLA_ENGINE_AUTO) return QLA_ENGINE_SIMT;
+  return engine;
+}
+
+int resolve_variant(const Shape& s, int variant, const DeviceInfo* d) {
+  (void)s;
+  (void)d;
+  if (variant == QLA_VARIANT_AUTO) return QLA_VARIANT_SEQ;
+  return variant;
+}
+
+int launch_seq(const SeqJob& j, int engine, int release, cudaStream_t stream) {
+  (void)release;
+  cudaError_t e;
+  switch (engine) {
+    case QLA_ENGINE_SIMT:
+      e = launch_seq_simt(j, stream);
+      break;
+    default:
+      return fail(QLA_ERR_UNSUPPORTED, "engine %d is not available in this build", engine);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return QLA_OK;
+}
+
+SeqJob plain_job(const float* H, const float* M, const float* h_init, float* out, float* fin, const Shape& s) {
+  SeqJob j{};
+  j.H = H;
+  j.M = M;
+  j.init = h_init;
+  j.out = out;
+  j.fin = fin;
+  j.h_chain_stride = (int64_t)s.S * s.state();
+  j.m_chain_stride = (int64_t)s.S * s.K * s.K;
+  j.init_unit_stride = s.state();
+  j.fin_unit_stride = s.state();
+  j.nchains = (int)s.chains();
+  j.S = s.S;
+  j.L = s.S;
+  j.G = 1;
+  j.K = s.K;
+  j.V = s.V;
+  j.layout = s.layout;
+  j.direction = s.direction;
+  j.init_mode = h_init ? kInitPointer : kInitZero;
+  return j;
+}
+
+size_t scan_bytes(const Shape& s, int G) {
+  // A_agg [chains][G][K][K], b_agg and carries [chains][G][state]
+  return (size_t)s.chains() * G * ((size_t)s.K * s.K + 2 * (size_t)s.state()) * sizeof(float);
+}
+
+// The scan variant.  For groups g of L consecutive segments (by index):
+//  1a. A_g = M_{last} ... M_{first} over the group's segments (forward products
+//      from the identity, kv view, V' = K); in reverse this is the transpose of
+//      the group's reverse aggregate.
+//  1b. b_g = the group's recurrence from a zero state, in the caller's layout
+//      and direction (its final state).
+//  2.  The same recurrence over the G aggregates, (M', H') = (A_g, b_g), from
+//      h_init: its exclusive outputs are the states entering each group.
+//  3.  Every group re-run from its entering state, writing out.
+int run_scan(const float* H, const float* M, const float* h_init, float* out, float* fin, const Shape& s,
+             int engine, int release, int group, cudaStream_t stream) {
+  const int G = group > 0 ? std::min(group, s.S) : auto_groups(s.S);
+  const int L = (s.S + G - 1) / G;
+  const int Gr = (s.S + L - 1) / L;  // groups actually formed
+  const size_t bytes = scan_bytes(s, Gr);
+  float* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), bytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(scan workspace)");
+  float* Aagg = ws;
+  float* bagg = Aagg + (size_t)s.chains() * Gr * s.K * s.K;
+  float* carry = bagg + (size_t)s.chains() * Gr * s.state();
+  const SeqJob base = plain_job(H, M, h_init, out, fin, s);
+  int st = QLA_OK;
+
+  {  // 1a: group products of M, forward, kv view, from the identity
+    SeqJob j = base;
+    j.H = nullptr;
+    j.init = nullptr;
+    j.init_mode = kInitIdentity;
+    j.out = nullptr;
+    j.fin = Aagg;
+    j.fin_unit_stride = (int64_t)s.K * s.K;
+    j.L = L;
+    j.G = Gr;
+    j.V = s.K;
+    j.layout = QLA_LAYOUT_KV;
+    j.direction = QLA_FORWARD;
+    st = launch_seq(j, engine, release, stream);
+  }
+  if (st == QLA_OK) {  // 1b: group recurrences from zero
+    SeqJob j = base;
+    j.init = nullptr;
+    j.init_mode = kInitZero;
+    j.out = nullptr;
+    j.fin = bagg;
+    j.fin_unit_stride = s.state();
+    j.L = L;
+    j.G = Gr;
+    st = launch_seq(j, engine, release, stream);
+  }
+  if (st == QLA_OK) {  // 2: carries across the group aggregates
+    SeqJob j = base;
+    j.H = bagg;
+    j.M = Aagg;
+    j.h_chain_stride = (int64_t)Gr * s.state();
+    j.m_chain_stride = (int64_t)Gr * s.K * s.K;
+    j.out = carry;
+    j.fin = fin;
+    j.S = Gr;
+    j.L = Gr;
+    j.G = 1;
+    st = launch_seq(j, engine, release, stream);
+  }
+  if (st == QLA_OK && out) {  // 3: re-run each group from its entering state
+    SeqJob j = base;
+    j.init = carry;
+    j.init_mode = kInitPointer;
+    j.init_unit_stride = s.state();
+    j.fin = nullptr;
+    j.L = L;
+    j.G = Gr;
+    st = launch_seq(j, engine, release, stream);
+  }
+  e = cudaFreeAsync(ws, stream);
+  if (st == QLA_OK && e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(scan workspace)");
+  return st;
+}
+
+}  // namespace
+}  // namespace qla
+
+using namespace qla;
+
+extern "C" {
+
+int qla_version(void) { return 100; }
+
+const char* qla_status_string(int status) {
+  switch (status) {
+    case QLA_OK: return "QLA_OK";
+    case QLA_ERR_INVALID_ARG: return "QLA_ERR_INVALID_ARG: invalid argument";
+    case QLA_ERR_UNSUPPORTED: return "QLA_ERR_UNSUPPORTED: unsupported shape or option";
+    case QLA_ERR_ALIGNMENT: return "QLA_ERR_ALIGNMENT: pointer not 16-byte aligned";
+    case QLA_ERR_ALIAS: return "QLA_ERR_ALIAS: overlapping buffers";
+    case QLA_ERR_CUDA: return "QLA_ERR_CUDA: CUDA runtime error";
+    case QLA_ERR_ARCH: return "QLA_ERR_ARCH: device is not sm_103";
+    case QLA_ERR_TIMEOUT: return "QLA_ERR_TIMEOUT: a bounded device wait gave up";
+    default: return "unknown status";
+  }
+}
+
+const char* qla_last_error(void) { return t_last_error.c_str(); }
+
+size_t qla_scan_workspace_bytes(int B, int heads, int S, int K, int V, int scan_group) {
+  if (B < 1 || heads < 1 || S < 1 || K < 1 || V < 1) return 0;
+  Shape s{B, heads, S, K, V, 0, 0};
+  const int G = scan_group > 0 ? std::min(scan_group, S) : auto_groups(S);
+  const int L = (S + G - 1) / G;
+  return scan_bytes(s, (S + L - 1) / L);
+}
+
+int qla_resolve(int B, int heads, int S, int K, int V, int layout, int* variant, int* engine) {
+  t_last_error.clear();
+  DeviceInfo* d = nullptr;
+  int st = current_device(&d);
+  if (st != QLA_OK) return st;
+  Shape s{B, heads, S, K, V, layout, 0};
+  if (variant) *variant = resolve_variant(s, QLA_VARIANT_AUTO, d);
+  if (engine) *engine = resolve_engine(s, QLA_ENGINE_AUTO);
+  return QLA_OK;
+}
+
+int qla_cp_correct_ex(const float* H, const float* M, const float* h_init, float* out, float* final_state, int B,
+                      int heads, int S, int K, int V, int layout, int direction, int variant, int engine,
+                      int release, int scan_group, void* stream) {
+  t_last_error.clear();
+  Shape s{B, heads, S, K, V, layout, direction};
+  int st = check_args(H, M, h_init, out, final_state, s);
+  if (st != QLA_OK) return st;
+  if (variant < QLA_VARIANT_AUTO || variant > QLA_VARIANT_SCAN)
+    return fail(QLA_ERR_INVALID_ARG, "unknown variant %d", variant);
+  if (engine < QLA_ENGINE_AUTO || engine > QLA_ENGINE_TC) return fail(QLA_ERR_INVALID_ARG, "unknown engine %d", engine);
+  if (release < QLA_RELEASE_MEMBAR || release > QLA_RELEASE_NONE)
+    return fail(QLA_ERR_INVALID_ARG, "unknown release mode %d", release);
+  if (scan_group < 0) return fail(QLA_ERR_INVALID_ARG, "scan_group must be >= 0");
+  DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != QLA_OK) return st;
+  const int v = resolve_variant(s, variant, d);
+  const int eng = resolve_engine(s, engine);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (v == QLA_VARIANT_SCAN && S > 1) return run_scan(H, M, h_init, out, final_state, s, eng, release, scan_group, cs);
+  return launch_seq(plain_job(H, M, h_init, out, final_state, s), eng, release, cs);
+}
+
+int qla_cp_correct(const float* H, const float* M, const float* h_init, float* out, int B, int heads, int S, int K,
+                   int V, int layout, int direction, void* stream) {
+  return qla_cp_correct_ex(H, M, h_init, out, nullptr, B, heads, S, K, V, layout, direction, QLA_VARIANT_AUTO,
+                           QLA_ENGINE_AUTO, QLA_RELEASE_MEMBAR, 0, stream);
+}
+
+int qla_device_status(int* flags) {
+  t_last_error.clear();
+  DeviceInfo* d = nullptr;
+  int st = current_device(&d);
+  if (st != QLA_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  unsigned int w = 0;
+  if ((e = cudaMemcpy(&w, d->status_word, sizeof w, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "read status word");
+  const unsigned int zero = 0;
+  if ((e = cudaMemcpy(d->status_word, &zero, sizeof zero, cudaMemcpyHostToDevice)) != cudaSuccess)
+    return cuda_fail(e, "clear status word");
+  if (flags) *flags = (int)w;
+  return w ? QLA_ERR_TIMEOUT : QLA_OK;
+}
+
+int qla_selftest_stalled_wait(const float* H, const float* M, float* out, int S, int wait_limit_us, void* stream) {
+  (void)H;
+  (void)M;
+  (void)out;
+  (void)S;
+  (void)wait_limit_us;
+  (void)stream;
+  return fail(QLA_ERR_UNSUPPORTED, "the warp-specialised engine is not available in this build");
+}
+
+}  // extern "C"

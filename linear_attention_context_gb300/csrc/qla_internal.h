@@ -1,0 +1,38 @@
+// Internal interfaces between the host API (api.cpp) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qla {
+
+// One launch of the sequential recurrence over a set of independent units.
+//
+// A unit is (chain, group): chain c in [0, nchains) selects H, M (and out)
+// through the chain strides; group g in [0, G) covers the segments
+// [g*L, min(g*L + L, S)).  Inside a unit the segments are visited ascending
+// (forward) or descending (reverse); the unit writes out[seg] for each of its
+// segments (the state entering that segment, in visiting order) and, when
+// `fin` is set, the state after its last segment.  The plain call is G = 1,
+// L = S; the scan variant uses the other forms.
+struct SeqJob {
+  const float* H;       // local states, [nchains][S][state]; nullptr = zero local states
+  const float* M;       // propagation matrices, [nchains][S][K][K]
+  const float* init;    // initial state per unit (init_mode 1)
+  float* out;           // [nchains][S][state] or nullptr
+  float* fin;           // final state per unit or nullptr
+  int64_t h_chain_stride;    // elements between chains of H and out
+  int64_t m_chain_stride;    // elements between chains of M
+  int64_t init_unit_stride;  // elements between units' initial states
+  int64_t fin_unit_stride;   // elements between units' final states
+  int nchains, S, L, G;
+  int K, V, layout, direction;
+  int init_mode;  // 0 zeros, 1 pointer, 2 identity (K == V)
+};
+
+enum InitMode { kInitZero = 0, kInitPointer = 1, kInitIdentity = 2 };
+
+// seq_simt.cu: plain FFMA kernel, any K, V that are multiples of 32 up to 256.
+cudaError_t launch_seq_simt(const SeqJob& job, cudaStream_t stream);
+
+}  // namespace qla

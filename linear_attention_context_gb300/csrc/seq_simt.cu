@@ -1,0 +1,206 @@
+// Sequential state correction, plain FFMA engine (no TMA, no warp roles).
+//
+// Computes the recurrence of Antarx Memos, "一次 TileLang Warp Specialization 数
+// 值错误的定位与修复", section "理解三个缓冲区，才能判断哪里需要同步":
+// X_{i+1} = propagate(M_i, X_i) + H_i, with out[seg] = the state entering seg.
+// It plays the role of that page's WS-off kernel (section "先恢复正确性：只关闭
+// 问题 kernel 的 WS"): one thread group does the loads and the math, so there
+// is no slot handoff to get wrong.  It serves every supported shape and is the
+// reference point for the warp-specialised engines.
+//
+// One CTA owns a 32-column tile of the kv-view state of one unit (chain,
+// group) for all of that unit's segments.  Per step it streams the
+// propagation matrix through shared memory in 32-row chunks of A (A = M going
+// forward, M^T in reverse), keeps the state tile in shared memory, and each of
+// its 256 threads accumulates R x 4 outputs (R = K / 32 rows spaced 32 apart,
+// 4 adjacent columns) in registers.
+//
+// In-place (out == H): a thread reads its H_seg elements before it writes
+// out[seg] over the same addresses, and no other thread touches them.
+#include "qla_internal.h"
+
+namespace qla {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTileV = 32;
+constexpr int kXsLd = kTileV + 4;  // padded row of the state tile (bank spread, keeps float4 alignment)
+
+__device__ __forceinline__ int64_t state_index(int layout, int K, int V, int k, int v) {
+  return layout == 0 ? (int64_t)k * V + v : (int64_t)v * K + k;
+}
+
+template <int R, int LAYOUT>
+__global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
+  constexpr int K = R * 32;
+  extern __shared__ __align__(16) float smem[];
+  float* Xs = smem;                 // [K][kXsLd]    state tile, kv view
+  float* As = smem + K * kXsLd;     // [32][K + 1]   chunk of A, transposed: As[kk][m] = A[m][kc + kk]
+
+  const int t = threadIdx.x;
+  // kv: 8 column groups across a warp, so float4 global accesses along v coalesce.
+  // vk: 32 consecutive rows across a warp, so scalar global accesses along k coalesce.
+  const int cg = LAYOUT == 0 ? (t & 7) : (t >> 5);
+  const int rg = LAYOUT == 0 ? (t >> 3) : (t & 31);
+  const int V = j.V;
+  const int v0 = blockIdx.x * kTileV + cg * 4;
+
+  const int u = blockIdx.y;
+  const int chain = u / j.G;
+  const int g = u - chain * j.G;
+  const int s_lo = g * j.L;
+  const int n = min(j.L, j.S - s_lo);
+  const int64_t st = (int64_t)K * V;
+
+  const float* Hc = j.H ? j.H + chain * j.h_chain_stride : nullptr;
+  float* Oc = j.out ? j.out + chain * j.h_chain_stride : nullptr;
+  const float* Mc = j.M + chain * j.m_chain_stride;
+
+  float x[R][4];
+#pragma unroll
+  for (int q = 0; q < R; ++q) {
+    const int k = rg + 32 * q;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float val = 0.f;
+      if (j.init_mode == kInitPointer)
+        val = j.init[u * j.init_unit_stride + state_index(LAYOUT, K, V, k, v0 + e)];
+      else if (j.init_mode == kInitIdentity)
+        val = (k == v0 + e) ? 1.f : 0.f;
+      x[q][e] = val;
+    }
+  }
+
+  const int nsteps = n - 1 + (j.fin ? 1 : 0);
+  for (int jj = 0; jj < n; ++jj) {
+    const int seg = j.direction == 0 ? s_lo + jj : s_lo + n - 1 - jj;
+    const bool do_step = jj < nsteps;
+    float h[R][4];
+#pragma unroll
+    for (int q = 0; q < R; ++q)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) h[q][e] = 0.f;
+    if (do_step && Hc) {
+      const float* Hs = Hc + seg * st;
+#pragma unroll
+      for (int q = 0; q < R; ++q) {
+        const int k = rg + 32 * q;
+        if (LAYOUT == 0) {
+          const float4 hv = *reinterpret_cast<const float4*>(Hs + (int64_t)k * V + v0);
+          h[q][0] = hv.x; h[q][1] = hv.y; h[q][2] = hv.z; h[q][3] = hv.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) h[q][e] = Hs[(int64_t)(v0 + e) * K + k];
+        }
+      }
+    }
+    if (Oc) {
+      float* Os = Oc + seg * st;
+#pragma unroll
+      for (int q = 0; q < R; ++q) {
+        const int k = rg + 32 * q;
+        if (LAYOUT == 0) {
+          *reinterpret_cast<float4*>(Os + (int64_t)k * V + v0) = make_float4(x[q][0], x[q][1], x[q][2], x[q][3]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) Os[(int64_t)(v0 + e) * K + k] = x[q][e];
+        }
+      }
+    }
+    if (!do_step) break;
+
+    __syncthreads();  // the previous step's readers of Xs and As are done
+#pragma unroll
+    for (int q = 0; q < R; ++q)
+      *reinterpret_cast<float4*>(Xs + (rg + 32 * q) * kXsLd + cg * 4) =
+          make_float4(x[q][0], x[q][1], x[q][2], x[q][3]);
+
+    float acc[R][4];
+#pragma unroll
+    for (int q = 0; q < R; ++q)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[q][e] = 0.f;
+
+    const float* Ms = Mc + (int64_t)seg * K * K;
+    for (int kc = 0; kc < K; kc += 32) {
+      __syncthreads();  // Xs written; the previous chunk's readers of As are done
+      if (j.direction == 0) {
+        // A = M: As[kk][m] = M[m][kc + kk]; 32 consecutive kk per m keep the global reads coalesced.
+        for (int e = t; e < 32 * K; e += kThreads) {
+          const int m = e >> 5, kk = e & 31;
+          As[kk * (K + 1) + m] = __ldg(Ms + (int64_t)m * K + kc + kk);
+        }
+      } else {
+        // A = M^T: As[kk][m] = M[kc + kk][m].
+        for (int e = t; e < 32 * K; e += kThreads) {
+          const int kk = e / K, m = e - kk * K;
+          As[kk * (K + 1) + m] = __ldg(Ms + (int64_t)(kc + kk) * K + m);
+        }
+      }
+      __syncthreads();
+#pragma unroll 8
+      for (int kk = 0; kk < 32; ++kk) {
+        const float4 xv = *reinterpret_cast<const float4*>(Xs + (kc + kk) * kXsLd + cg * 4);
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+          const float a = As[kk * (K + 1) + rg + 32 * q];
+          acc[q][0] = fmaf(a, xv.x, acc[q][0]);
+          acc[q][1] = fmaf(a, xv.y, acc[q][1]);
+          acc[q][2] = fmaf(a, xv.z, acc[q][2]);
+          acc[q][3] = fmaf(a, xv.w, acc[q][3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < R; ++q)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[q][e] = acc[q][e] + h[q][e];
+  }
+
+  if (j.fin) {
+    float* F = j.fin + u * j.fin_unit_stride;
+#pragma unroll
+    for (int q = 0; q < R; ++q) {
+      const int k = rg + 32 * q;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) F[state_index(LAYOUT, K, V, k, v0 + e)] = x[q][e];
+    }
+  }
+}
+
+template <int R, int LAYOUT>
+cudaError_t launch_one(const SeqJob& j, cudaStream_t stream) {
+  constexpr int K = R * 32;
+  const size_t smem = sizeof(float) * ((size_t)K * kXsLd + 32 * (size_t)(K + 1));
+  auto kern = seq_simt_kernel<R, LAYOUT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(j.V / kTileV, j.nchains * j.G);
+  kern<<<grid, kThreads, smem, stream>>>(j);
+  return cudaGetLastError();
+}
+
+template <int LAYOUT>
+cudaError_t dispatch_r(const SeqJob& j, cudaStream_t s) {
+  switch (j.K / 32) {
+    case 1: return launch_one<1, LAYOUT>(j, s);
+    case 2: return launch_one<2, LAYOUT>(j, s);
+    case 3: return launch_one<3, LAYOUT>(j, s);
+    case 4: return launch_one<4, LAYOUT>(j, s);
+    case 5: return launch_one<5, LAYOUT>(j, s);
+    case 6: return launch_one<6, LAYOUT>(j, s);
+    case 7: return launch_one<7, LAYOUT>(j, s);
+    case 8: return launch_one<8, LAYOUT>(j, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_seq_simt(const SeqJob& job, cudaStream_t stream) {
+  if (job.K % 32 || job.K < 32 || job.K > 256 || job.V % kTileV) return cudaErrorInvalidValue;
+  if ((int64_t)job.nchains * job.G > 65535) return cudaErrorInvalidValue;
+  return job.layout == 0 ? dispatch_r<0>(job, stream) : dispatch_r<1>(job, stream);
+}
+
+}  // namespace qla

@@ -1,0 +1,121 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function the
+header declares, and rejects bad arguments with the documented status before
+it makes any CUDA call (so fake, never-dereferenced pointers are enough)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_attention_context_gb300 as qla
+from linear_attention_context_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qla.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(_build.library_path()):
+        _build.build()
+    return qla.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qla_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(qla.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_only_the_c_abi_is_exported(L):
+    # hidden visibility keeps kernels and helpers out of the dynamic symbol table
+    import subprocess
+    r = subprocess.run(["nm", "-D", "--defined-only", _build.library_path()], capture_output=True, text=True)
+    if r.returncode != 0:
+        pytest.skip("nm unavailable")
+    names = {ln.split()[-1] for ln in r.stdout.splitlines() if " T " in ln}
+    qla_names = {n for n in names if n.startswith("qla_")}
+    assert qla_names == set(declared_functions())
+
+
+def test_version_and_status_strings(L):
+    assert L.qla_version() == 100
+    for code, name in qla.STATUS.items():
+        assert L.qla_status_string(code).decode().startswith(name)
+    assert L.qla_status_string(12345).decode() == "unknown status"
+
+
+FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
+
+
+def call(L, H=FAKE, M=FAKE + (1 << 32), h0=None, out=FAKE + (2 << 32), fin=None, B=1, heads=2, S=4, K=64,
+         V=64, layout=0, direction=0, variant=0, engine=0, release=0, group=0):
+    vp = ctypes.c_void_p
+    return L.qla_cp_correct_ex(vp(H), vp(M), vp(h0), vp(out), vp(fin), B, heads, S, K, V, layout, direction,
+                               variant, engine, release, group, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(H=None), -1), (dict(M=None), -1), (dict(out=None), -1),
+    (dict(B=0), -1), (dict(heads=-1), -1), (dict(S=0), -1), (dict(K=0), -1),
+    (dict(layout=2), -1), (dict(direction=-1), -1),
+    (dict(variant=3), -1), (dict(engine=9), -1), (dict(release=7), -1), (dict(group=-1), -1),
+    (dict(K=48), -2), (dict(V=288), -2), (dict(K=16), -2), (dict(V=100), -2),
+    (dict(H=FAKE + 4), -3), (dict(M=FAKE + (1 << 32) + 8), -3), (dict(out=FAKE + (2 << 32) + 12), -3),
+    (dict(h0=FAKE + (3 << 32) + 2), -3), (dict(fin=FAKE + (4 << 32) + 1), -3),
+    # overlaps: out partially over H; M over H; h_init inside M; final over out
+    (dict(out=FAKE + 16), -4), (dict(M=FAKE + 4096), -4), (dict(h0=FAKE + (1 << 32) + 64), -4),
+    (dict(fin=FAKE + (2 << 32) + 1024), -4),
+])
+def test_argument_checks(L, kw, status):
+    assert call(L, **kw) == status
+    assert L.qla_last_error().decode() != ""
+
+
+# The next three calls pass validation, so with a GPU present they would launch
+# on the fake pointers; they run only where no GPU is visible.
+no_gpu_only = pytest.mark.skipif("_has_gpu()", reason="would launch on fake pointers")
+
+
+@no_gpu_only
+def test_out_equal_to_H_passes_the_checks(L):
+    # exact alias is the in-place mode: validation passes and the call stops
+    # at the device probe
+    assert call(L, out=FAKE) == -5
+
+
+@no_gpu_only
+def test_valid_call_without_gpu_reports_cuda_error(L):
+    assert call(L) == -5
+    assert "cuda" in L.qla_last_error().decode().lower()
+
+
+@no_gpu_only
+def test_final_state_only_is_accepted_by_checks(L):
+    assert call(L, out=None, fin=FAKE + (4 << 32)) == -5
+
+
+def test_scan_workspace_bytes(L):
+    # chains * G * (K*K + 2*K*V) * 4 with G the groups actually formed
+    assert L.qla_scan_workspace_bytes(1, 1, 128, 128, 128, 16) == 1 * 16 * (128 * 128 + 2 * 128 * 128) * 4
+    assert L.qla_scan_workspace_bytes(2, 3, 10, 64, 32, 4) == 6 * 4 * (64 * 64 + 2 * 64 * 32) * 4
+    # S = 10 with 3 groups: L = 4, so groups actually formed = 3
+    assert L.qla_scan_workspace_bytes(1, 1, 10, 32, 32, 3) == 3 * (32 * 32 + 2 * 32 * 32) * 4
+    assert L.qla_scan_workspace_bytes(0, 1, 10, 32, 32, 3) == 0
+
+
+def _has_gpu():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False

@@ -1,0 +1,152 @@
+"""GPU parity: the CUDA path against the fp64 oracle on the same seeded inputs.
+
+Bar (per output state): rel-L2 <= 1e-5 and max|err| <= 1e-4 * max|ref|; exact
+when the reference state is all zero; bitwise on the exact-integer cases.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import qla_inputs as qi
+from gpu_util import engine_supports, engines_under_test, run
+from qla_check import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+LAYOUTS = ("kv", "vk")
+DIRS = ("fwd", "rev")
+ENGINES = engines_under_test()
+
+
+def skip_unsupported(engine, K, V):
+    if not engine_supports(engine, K, V):
+        pytest.skip(f"engine {engine} does not take K={K}, V={V}")
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+@pytest.mark.parametrize("direction", DIRS)
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("name", ["c0", "c1", "c2"])
+def test_workloads(name, layout, direction, engine):
+    c = qi.WORKLOADS[name]
+    skip_unsupported(engine, c.K, c.V)
+    H, M, h0 = qi.make_inputs(c, layout)
+    ref, rfin = oracle.cp_correct(H, M, h0, layout, direction, want_final=True)
+    got, fin = run(H, M, h0, layout, direction, engine=engine, final=True)
+    assert_parity(got, ref, what=f"{name} {layout} {direction} {engine}")
+    assert_parity(fin, rfin, what=f"{name} final")
+
+
+@pytest.mark.parametrize("engine", ["auto"] + [e for e in ENGINES if e != "simt"])
+@pytest.mark.parametrize("direction", DIRS)
+def test_large_workload_sampled(direction, engine):
+    """B=4, 64 heads, K=V=256, S=32 at full size on the GPU; the oracle checks
+    a sample of chains (first, last, and two in between)."""
+    c = qi.WORKLOADS["c3"]
+    skip_unsupported(engine, c.K, c.V)
+    H, M, h0 = qi.make_inputs(c, "kv")
+    got, _ = run(H, M, h0, "kv", direction, engine=engine)
+    n = c.chains
+    for ch in sorted({0, n // 3, (2 * n) // 3, n - 1}):
+        b, h = divmod(ch, c.heads)
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref, _ = oracle.cp_correct(H[sl], M[sl], h0[sl], "kv", direction)
+        assert_parity(got[sl], ref, what=f"c3 chain {ch} {direction} {engine}")
+
+
+@pytest.mark.parametrize("direction", DIRS)
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("heads", qi.SWEEP_HEADS)
+@pytest.mark.parametrize("S", qi.SWEEP_S)
+def test_sweep_seq_and_scan(S, heads, layout, direction):
+    c = qi.sweep_case(heads, S)
+    H, M, h0 = qi.make_inputs(c, layout)
+    ref, rfin = oracle.cp_correct(H, M, h0, layout, direction, want_final=True)
+    for variant in ("seq", "scan"):
+        got, fin = run(H, M, h0, layout, direction, variant=variant, final=True)
+        assert_parity(got, ref, what=f"sweep S={S} heads={heads} {layout} {direction} {variant}")
+        assert_parity(fin, rfin, what=f"sweep final {variant}")
+
+
+EDGE = [
+    # (B, heads, S, K, V, init)
+    (1, 1, 1, 64, 64, True),
+    (1, 1, 1, 128, 128, False),
+    (1, 2, 2, 128, 128, False),
+    (3, 5, 3, 32, 256, True),
+    (2, 3, 5, 256, 32, True),
+    (1, 7, 4, 96, 160, True),
+    (2, 1, 9, 128, 64, True),
+    (1, 3, 6, 256, 128, False),
+    (1, 1, 3, 224, 96, True),
+]
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+@pytest.mark.parametrize("direction", DIRS)
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("shape", EDGE, ids=lambda s: "B{}h{}S{}K{}V{}{}".format(*s[:5], "i" if s[5] else "z"))
+def test_edge_shapes(shape, layout, direction, engine):
+    B, nh, S, K, V, init = shape
+    skip_unsupported(engine, K, V)
+    c = qi.Case(B=B, heads=nh, S=S, K=K, V=V, seed=77, m_kind="householder", h_scale=0.5,
+                init_kind="gaussian" if init else "none")
+    H, M, h0 = qi.make_inputs(c, layout)
+    ref, rfin = oracle.cp_correct(H, M, h0, layout, direction, want_final=True)
+    got, fin = run(H, M, h0, layout, direction, engine=engine, final=True)
+    assert_parity(got, ref, what=f"edge {shape} {layout} {direction} {engine}")
+    assert_parity(fin, rfin, what="edge final")
+    # final state alone (no out)
+    _, fin2 = run(H, M, h0, layout, direction, engine=engine, final=True, want_out=False)
+    assert_parity(fin2, rfin, what="edge final only")
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+@pytest.mark.parametrize("direction", DIRS)
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_in_place_matches_separate_output(layout, direction, engine):
+    c = qi.WORKLOADS["c1"].with_(heads=4)
+    H, M, h0 = qi.make_inputs(c, layout)
+    ref, _ = oracle.cp_correct(H, M, h0, layout, direction)
+    got, _ = run(H, M, h0, layout, direction, engine=engine, in_place=True)
+    assert_parity(got, ref, what=f"in place {layout} {direction} {engine}")
+    sep, _ = run(H, M, h0, layout, direction, engine=engine)
+    assert np.array_equal(got, sep)
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+@pytest.mark.parametrize("direction", DIRS)
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("K,V", [(128, 128), (256, 64), (64, 32)])
+def test_integer_exact_bitwise(K, V, layout, direction, engine):
+    skip_unsupported(engine, K, V)
+    c = qi.Case(B=1, heads=3, S=8, K=K, V=V, seed=5, m_kind="signed_perm", h_kind="small_int",
+                init_kind="small_int")
+    H, M, h0 = qi.make_inputs(c, layout)
+    ref, rfin = oracle.cp_correct(H, M, h0, layout, direction, want_final=True)
+    got, fin = run(H, M, h0, layout, direction, engine=engine, final=True)
+    assert np.array_equal(got, ref)
+    assert np.array_equal(fin, rfin)
+
+
+@pytest.mark.parametrize("direction", DIRS)
+@pytest.mark.parametrize("group", [1, 2, 3, 7, 10])
+def test_scan_groups_ragged(group, direction):
+    c = qi.sweep_case(heads=2, S=10)
+    for layout in LAYOUTS:
+        H, M, h0 = qi.make_inputs(c, layout)
+        ref, rfin = oracle.cp_correct(H, M, h0, layout, direction, want_final=True)
+        got, fin = run(H, M, h0, layout, direction, variant="scan", scan_group=group, final=True)
+        assert_parity(got, ref, what=f"scan group {group} {layout} {direction}")
+        assert_parity(fin, rfin, what="scan final")
+
+
+@pytest.mark.parametrize("direction", DIRS)
+def test_scan_integer_exact(direction):
+    c = qi.Case(B=1, heads=2, S=12, K=128, V=64, seed=8, m_kind="signed_perm", h_kind="small_int",
+                init_kind="small_int")
+    for layout in LAYOUTS:
+        H, M, h0 = qi.make_inputs(c, layout)
+        ref, _ = oracle.cp_correct(H, M, h0, layout, direction)
+        got, _ = run(H, M, h0, layout, direction, variant="scan", scan_group=4)
+        assert np.array_equal(got, ref)
