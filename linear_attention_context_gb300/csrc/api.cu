@@ -148,6 +148,12 @@ int resolve_engine(const Shape& s, int engine) {
   return engine;
 }
 
+// The engine a scan phase runs on: phase 1a's V' = K may differ from V.
+int engine_for(const SeqJob& j, int engine) {
+  if (engine == QLA_ENGINE_TC && !tc_supports(j.K, j.V)) return QLA_ENGINE_SIMT;
+  return engine;
+}
+
 int resolve_variant(const Shape& s, int variant, const DeviceInfo* d) {
   (void)s;
   (void)d;
@@ -155,12 +161,16 @@ int resolve_variant(const Shape& s, int variant, const DeviceInfo* d) {
   return variant;
 }
 
-int launch_seq(const SeqJob& j, int engine, int release, cudaStream_t stream) {
-  (void)release;
+int launch_seq(const SeqJob& j, int engine, int release, const DeviceInfo* d, cudaStream_t stream) {
   cudaError_t e;
   switch (engine) {
     case QLA_ENGINE_SIMT:
       e = launch_seq_simt(j, stream);
+      break;
+    case QLA_ENGINE_TC:
+      if (!tc_supports(j.K, j.V))
+        return fail(QLA_ERR_UNSUPPORTED, "the tensor-core engine takes K in {128, 256} (got K=%d, V=%d)", j.K, j.V);
+      e = launch_seq_tc(j, release, d->status_word, kWaitLimitNs, 0, stream);
       break;
     default:
       return fail(QLA_ERR_UNSUPPORTED, "engine %d is not available in this build", engine);
@@ -207,7 +217,7 @@ size_t scan_bytes(const Shape& s, int G) {
 //      h_init: its exclusive outputs are the states entering each group.
 //  3.  Every group re-run from its entering state, writing out.
 int run_scan(const float* H, const float* M, const float* h_init, float* out, float* fin, const Shape& s,
-             int engine, int release, int group, cudaStream_t stream) {
+             int engine, int release, int group, const DeviceInfo* d, cudaStream_t stream) {
   const int G = group > 0 ? std::min(group, s.S) : auto_groups(s.S);
   const int L = (s.S + G - 1) / G;
   const int Gr = (s.S + L - 1) / L;  // groups actually formed
@@ -234,7 +244,7 @@ int run_scan(const float* H, const float* M, const float* h_init, float* out, fl
     j.V = s.K;
     j.layout = QLA_LAYOUT_KV;
     j.direction = QLA_FORWARD;
-    st = launch_seq(j, engine, release, stream);
+    st = launch_seq(j, engine_for(j, engine), release, d, stream);
   }
   if (st == QLA_OK) {  // 1b: group recurrences from zero
     SeqJob j = base;
@@ -245,7 +255,7 @@ int run_scan(const float* H, const float* M, const float* h_init, float* out, fl
     j.fin_unit_stride = s.state();
     j.L = L;
     j.G = Gr;
-    st = launch_seq(j, engine, release, stream);
+    st = launch_seq(j, engine_for(j, engine), release, d, stream);
   }
   if (st == QLA_OK) {  // 2: carries across the group aggregates
     SeqJob j = base;
@@ -258,7 +268,7 @@ int run_scan(const float* H, const float* M, const float* h_init, float* out, fl
     j.S = Gr;
     j.L = Gr;
     j.G = 1;
-    st = launch_seq(j, engine, release, stream);
+    st = launch_seq(j, engine_for(j, engine), release, d, stream);
   }
   if (st == QLA_OK && out) {  // 3: re-run each group from its entering state
     SeqJob j = base;
@@ -268,7 +278,7 @@ int run_scan(const float* H, const float* M, const float* h_init, float* out, fl
     j.fin = nullptr;
     j.L = L;
     j.G = Gr;
-    st = launch_seq(j, engine, release, stream);
+    st = launch_seq(j, engine_for(j, engine), release, d, stream);
   }
   e = cudaFreeAsync(ws, stream);
   if (st == QLA_OK && e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(scan workspace)");
@@ -337,8 +347,9 @@ int qla_cp_correct_ex(const float* H, const float* M, const float* h_init, float
   const int v = resolve_variant(s, variant, d);
   const int eng = resolve_engine(s, engine);
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (v == QLA_VARIANT_SCAN && S > 1) return run_scan(H, M, h_init, out, final_state, s, eng, release, scan_group, cs);
-  return launch_seq(plain_job(H, M, h_init, out, final_state, s), eng, release, cs);
+  if (v == QLA_VARIANT_SCAN && S > 1)
+    return run_scan(H, M, h_init, out, final_state, s, eng, release, scan_group, d, cs);
+  return launch_seq(plain_job(H, M, h_init, out, final_state, s), eng, release, d, cs);
 }
 
 int qla_cp_correct(const float* H, const float* M, const float* h_init, float* out, int B, int heads, int S, int K,
@@ -365,13 +376,19 @@ int qla_device_status(int* flags) {
 }
 
 int qla_selftest_stalled_wait(const float* H, const float* M, float* out, int S, int wait_limit_us, void* stream) {
-  (void)H;
-  (void)M;
-  (void)out;
-  (void)S;
-  (void)wait_limit_us;
-  (void)stream;
-  return fail(QLA_ERR_UNSUPPORTED, "the warp-specialised engine is not available in this build");
+  t_last_error.clear();
+  Shape s{1, 1, S, 128, 128, QLA_LAYOUT_KV, QLA_FORWARD};
+  int st = check_args(H, M, nullptr, out, nullptr, s);
+  if (st != QLA_OK) return st;
+  if (S < 2) return fail(QLA_ERR_INVALID_ARG, "the stalled-wait self-test needs S >= 2");
+  if (wait_limit_us < 1 || wait_limit_us > 10000000)
+    return fail(QLA_ERR_INVALID_ARG, "wait_limit_us must be in [1, 10^7]");
+  DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != QLA_OK) return st;
+  cudaError_t e = launch_seq_tc(plain_job(H, M, nullptr, out, nullptr, s), QLA_RELEASE_MEMBAR, d->status_word,
+                                (uint64_t)wait_limit_us * 1000ull, 1, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return QLA_OK;
 }
 
 }  // extern "C"

@@ -35,4 +35,16 @@ enum InitMode { kInitZero = 0, kInitPointer = 1, kInitIdentity = 2 };
 // seq_simt.cu: plain FFMA kernel, any K, V that are multiples of 32 up to 256.
 cudaError_t launch_seq_simt(const SeqJob& job, cudaStream_t stream);
 
+// seq_tc.cu: warp-specialised TMA/mbarrier pipeline with a tcgen05 3xTF32
+// propagate.  K in {128, 256}, V a multiple of 32.  `release` selects the
+// slot-release fence (QLA_RELEASE_*); `status` is the device status word a
+// timed-out wait sets; `limit_ns` bounds every wait; `stall_test` makes the
+// epilogue wait on a barrier nothing arrives on.
+bool tc_supports(int K, int V);
+cudaError_t launch_seq_tc(const SeqJob& job, int release, unsigned int* status, uint64_t limit_ns,
+                          int stall_test, cudaStream_t stream);
+
+// Bound on every device-side wait of the pipelined engines.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
 }  // namespace qla

@@ -1,0 +1,576 @@
+// Sequential state correction, warp-specialised tensor-core engine (sm_103a).
+//
+// Computes the recurrence of Antarx Memos, "一次 TileLang Warp Specialization 数
+// 值错误的定位与修复", section "理解三个缓冲区，才能判断哪里需要同步":
+// X_{j+1} = A_j X_j + H_j in the kv view, A_j = M (forward) or M^T (reverse),
+// out[seg] = the state entering seg.  The page's kernel streams h and m tiles
+// into two-slot shared buffers with a TMA producer and lets consumers do the
+// GEMM; its bug was a slot released before its last ordinary read.  This
+// engine keeps that producer/consumer shape and moves the contraction onto
+// tcgen05 with fp32 accuracy from three TF32 products:
+//     A X ~= A_hi X_hi + A_hi X_lo + A_lo X_hi,
+// with hi = the value with its 13 low mantissa bits cleared and lo = x - hi
+// (exact in fp32).  The dropped A_lo X_lo term is below 2^-22 relative.
+//
+// One CTA owns a VT-column tile of one unit (chain, group) for all of the
+// unit's segments.  Roles, storage, handoff and lifetime (the table the
+// mlc.ai page "调试 Warp-Specialized Kernels", section "先写清楚数据如何交接",
+// asks for):
+//
+//  role      warps    does
+//  producer  0 (1 th) TMA: H_j tile -> h slot j&1; A_j in 32-column chunks
+//                     -> m ring (NM stages).  Needs no state: runs ahead.
+//  mma       1 (1 th) tcgen05.mma kind::tf32, A from TMEM, B (= X_j hi/lo,
+//                     K-major, 128-byte swizzle) from shared memory, D in TMEM.
+//  splitter  4..7     m chunk (ordinary shared loads) -> hi/lo -> TMEM A ring
+//                     (NA slots of 64 columns).
+//  epilogue  8..11    D (tcgen05.ld) + H_j (ordinary shared loads) -> out via
+//                     per-warp TMA stores; X_{j+1} hi/lo -> B operand.
+//
+//  storage        written by           read by             reusable after
+//  m ring [s]     TMA (async)          splitter (generic)  splitter's last read: fence + m_empty arrive
+//  h slot [j&1]   TMA (async)          epilogue (generic)  epilogue's last read: fence + h_empty arrive
+//  A ring (TMEM)  splitter tcgen05.st  mma (async)         mma commit -> a_empty
+//  B hi/lo        epilogue st.shared   mma (async)         d_full (all MMAs of the step done)
+//                 + fence.proxy.async
+//  D (TMEM)       mma                  epilogue tcgen05.ld x_ready (epilogue's wait::ld done)
+//  out staging    epilogue st.shared   TMA store (async)   bulk wait_group.read
+//                 + fence.proxy.async
+//
+// Barriers: m_full/h_full count 1 + transaction bytes; m_empty, h_empty,
+// a_full, x_ready count 4 (one arrive per warp after __syncwarp); a_empty,
+// d_full count 1 (tcgen05.commit).  Producers wait their empty barriers with
+// the parity of (use / slots) ^ 1, consumers their full barriers with
+// (use / slots), so the first producer wait passes at once.
+//
+// The slot-release fence (the page's section "三个可用源码方案的具体差别") is
+// selectable: membar.cta, fence.proxy.async.shared::cta, none, or a release
+// delayed to the end of the slot's use.  It sits between the last ordinary
+// shared load of a slot and the arrive on its empty barrier, and every asm
+// here carries a "memory" clobber so the compiler keeps that order.
+//
+// In place (out == H): out[seg] is stored over H[seg] only after the TMA load
+// of that tile of H[seg] has completed (its full barrier has been observed).
+//
+// Every wait is bounded (see ptx.cuh); on expiry the CTA drains its copies in
+// flight, frees TMEM and returns with the device status word set.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "ptx.cuh"
+#include "qla_internal.h"
+
+namespace qla {
+namespace {
+
+using namespace ptx;
+
+constexpr int VT = 32;            // state columns per CTA
+constexpr int kThreads = 384;     // 12 warps
+constexpr uint32_t kChunkBytes = 128 * 32 * 4;  // one A chunk: 128 rows x 32 columns fp32
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kDCols = 64;   // D at columns [0, 64); the A ring follows
+constexpr int NA = 6;             // TMEM A slots (64 columns: hi then lo)
+
+template <int K>
+struct Cfg {
+  static constexpr int HALVES = K / 128;           // 128-row MMA blocks of the output
+  static constexpr int KCH = K / 32;               // 32-wide k chunks per block
+  static constexpr int CPS = HALVES * KCH;         // chunks per step
+  static constexpr int NM = K == 128 ? 6 : 4;      // m ring stages
+  static constexpr int NOUT = K == 128 ? 2 : 1;    // out staging buffers
+  static constexpr uint32_t TILE = (uint32_t)K * VT * 4;  // one state tile (bytes)
+  static constexpr uint32_t OFF_M = 0;
+  static constexpr uint32_t OFF_H = OFF_M + NM * kChunkBytes;
+  static constexpr uint32_t OFF_BHI = OFF_H + 2 * TILE;
+  static constexpr uint32_t OFF_BLO = OFF_BHI + TILE;
+  static constexpr uint32_t OFF_OUT = OFF_BLO + TILE;
+  static constexpr uint32_t OFF_CTRL = OFF_OUT + NOUT * TILE;
+  static constexpr uint32_t CTRL_BYTES = 512;
+  static constexpr uint32_t SMEM = OFF_CTRL + CTRL_BYTES + 1024;  // + alignment slack
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct TcParams {
+  CUtensorMap map_h;    // H (load)
+  CUtensorMap map_out;  // out (store)
+  CUtensorMap map_m;    // M chunks (load)
+  SeqJob job;
+  unsigned int* status;
+  uint64_t limit_ns;
+  int has_h;
+  int in_place;
+  int release;          // 0 membar, 1 proxy, 2 delay, 3 none
+  int stall_test;       // epilogue waits on a barrier nothing arrives on
+};
+
+struct Ctrl {
+  uint64_t m_full[6], m_empty[6];
+  uint64_t a_full[NA], a_empty[NA];
+  uint64_t h_full[2], h_empty[2];
+  uint64_t x_ready, d_full, never, mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(Ctrl) <= 512, "control block");
+
+__device__ __forceinline__ void release_fence(int mode) {
+  if (mode == 0) membar_cta();
+  else if (mode == 1) fence_proxy_async_smem();
+}
+
+// Warp-uniform bounded wait: every lane polls, the warp agrees on the outcome.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& c) {
+  const bool ok = mbar_wait(bar, parity, c);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ uint32_t tf32_hi_bits(float x) { return __float_as_uint(x) & 0xFFFFE000u; }
+
+template <int K>
+__global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_constant__ TcParams p) {
+  using C = Cfg<K>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + C::OFF_CTRL);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const SeqJob& j = p.job;
+  const int u = blockIdx.y;
+  const int chain = u / j.G;
+  const int g = u - chain * j.G;
+  const int s_lo = g * j.L;
+  const int n = min(j.L, j.S - s_lo);
+  const int nsteps = n - 1 + (j.fin ? 1 : 0);
+  const int v0 = blockIdx.x * VT;
+  const bool fwd = j.direction == 0;
+  auto seg_of = [&](int step) { return fwd ? s_lo + step : s_lo + n - 1 - step; };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NM; ++i) {
+      mbar_init(&ctl->m_full[i], 1);
+      mbar_init(&ctl->m_empty[i], 4);
+    }
+    for (int i = 0; i < NA; ++i) {
+      mbar_init(&ctl->a_full[i], 4);
+      mbar_init(&ctl->a_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl->h_full[i], 1);
+      mbar_init(&ctl->h_empty[i], 4);
+    }
+    mbar_init(&ctl->x_ready, 4);
+    mbar_init(&ctl->d_full, 1);
+    mbar_init(&ctl->never, 1);
+    mbar_init(&ctl->mma_done, 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  WaitCtl wc{&ctl->abort, p.status, p.limit_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&p.map_m);
+      if (p.has_h) prefetch_tensormap(&p.map_h);
+      if (j.out) prefetch_tensormap(&p.map_out);
+      uint32_t mit = 0;
+      int hissued = 0;
+      bool ok = true;
+      const int hrows = j.layout == 0 ? K : j.V;  // rows of one state in the 2-D view of H
+      for (int step = 0; step < nsteps && ok; ++step) {
+        const int seg = seg_of(step);
+        const int64_t mrow0 = ((int64_t)chain * j.S + seg) * K;
+        if (p.has_h) {
+          const int slot = step & 1;
+          if (!(ok = mbar_wait(&ctl->h_empty[slot], ((step >> 1) & 1) ^ 1, wc))) break;
+          mbar_arrive_expect_tx(&ctl->h_full[slot], C::TILE);
+          const int64_t hrow0 = ((int64_t)chain * j.S + seg) * hrows;
+          if (j.layout == 0)
+            tma_load_2d(smem + C::OFF_H + slot * C::TILE, &p.map_h, v0, (int32_t)hrow0, &ctl->h_full[slot]);
+          else
+            tma_load_2d(smem + C::OFF_H + slot * C::TILE, &p.map_h, 0, (int32_t)(hrow0 + v0), &ctl->h_full[slot]);
+          ++hissued;
+        }
+        for (int c = 0; c < C::CPS; ++c, ++mit) {
+          const int stage = mit % C::NM;
+          if (!(ok = mbar_wait(&ctl->m_empty[stage], ((mit / C::NM) & 1) ^ 1, wc))) break;
+          mbar_arrive_expect_tx(&ctl->m_full[stage], kChunkBytes);
+          const int h = c / C::KCH, kc = c % C::KCH;
+          uint8_t* dst = smem + C::OFF_M + stage * kChunkBytes;
+          if (fwd)  // A = M: rows 128h.., columns 32kc..  (128-byte swizzle, box 32 x 128)
+            tma_load_2d(dst, &p.map_m, 32 * kc, (int32_t)(mrow0 + 128 * h), &ctl->m_full[stage]);
+          else      // A = M^T: M rows 32kc.., columns 128h..  (box 128 x 32)
+            tma_load_2d(dst, &p.map_m, 128 * h, (int32_t)(mrow0 + 32 * kc), &ctl->m_full[stage]);
+        }
+      }
+      // Drain: every issued load must land before shared memory goes away.
+      const uint64_t drain = 200000000ull;  // 200 ms
+      for (int s = 0; s < C::NM; ++s) {
+        const uint32_t uses = mit > (uint32_t)s ? (mit - 1 - s) / C::NM + 1 : 0;
+        if (uses) mbar_wait_drain(&ctl->m_full[s], (uses - 1) & 1, drain);
+      }
+      for (int s = 0; s < 2; ++s) {
+        const int uses = hissued > s ? (hissued - 1 - s) / 2 + 1 : 0;
+        if (uses) mbar_wait_drain(&ctl->h_full[s], (uses - 1) & 1, drain);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ mma issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_tf32(128, VT);
+      const uint32_t bhi = smem_u32(smem + C::OFF_BHI);
+      const uint32_t blo = smem_u32(smem + C::OFF_BLO);
+      uint32_t ait = 0;
+      bool ok = true;
+      for (int step = 0; step < nsteps && ok; ++step) {
+        if (!(ok = mbar_wait(&ctl->x_ready, step & 1, wc))) break;
+        tc_fence_after();
+        for (int h = 0; h < C::HALVES && ok; ++h) {
+          const uint32_t d = tmem + (uint32_t)(h * VT);
+          for (int kc = 0; kc < C::KCH; ++kc, ++ait) {
+            const int slot = ait % NA;
+            if (!(ok = mbar_wait(&ctl->a_full[slot], (ait / NA) & 1, wc))) break;
+            tc_fence_after();
+            const uint32_t a_hi = tmem + kDCols + slot * 64;
+            const uint32_t a_lo = a_hi + 32;
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+              // B rows k in [32kc + 8s, +8): k-block kc, 32 bytes per 8 tf32 inside the swizzled row
+              const uint32_t off = (uint32_t)kc * (VT * 128) + (uint32_t)s * 32;
+              const uint64_t dh = smem_desc_sw128(bhi + off, 1024);
+              const uint64_t dl = smem_desc_sw128(blo + off, 1024);
+              mma_tf32_ts(d, a_hi + s * 8, dh, idesc, (kc | s) != 0);
+              mma_tf32_ts(d, a_hi + s * 8, dl, idesc, 1);
+              mma_tf32_ts(d, a_lo + s * 8, dh, idesc, 1);
+            }
+            mma_commit(&ctl->a_empty[slot]);
+          }
+        }
+        if (ok) mma_commit(&ctl->d_full);
+      }
+      // All MMAs this thread issued must finish before TMEM is freed.
+      mma_commit(&ctl->mma_done);
+      mbar_wait_drain(&ctl->mma_done, 0, 200000000ull);
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ A splitter
+    const int t = threadIdx.x - 128;                 // A row within the 128-row block = TMEM lane
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    uint32_t mit = 0;
+    bool ok = true;
+    for (int step = 0; step < nsteps && ok; ++step) {
+      for (int c = 0; c < C::CPS; ++c, ++mit) {
+        const int stage = mit % C::NM;
+        if (!(ok = warp_wait(&ctl->m_full[stage], (mit / C::NM) & 1, wc))) break;
+        const uint8_t* chunk = smem + C::OFF_M + stage * kChunkBytes;
+        float x[32];
+        if (fwd) {  // row t of a [128][32] tile, 16-byte pieces swizzled by (t & 7)
+          const uint8_t* row = chunk + t * 128;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 v = *reinterpret_cast<const float4*>(row + ((q ^ (t & 7)) << 4));
+            x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
+          }
+        } else {    // column t of a [32][128] tile
+          const float* col = reinterpret_cast<const float*>(chunk) + t;
+#pragma unroll
+          for (int k = 0; k < 32; ++k) x[k] = col[k * 128];
+        }
+        if (p.release != 2) {  // the slot's last ordinary read is done: release it
+          release_fence(p.release);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->m_empty[stage]);
+        }
+        uint32_t hi[32], lo[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          hi[k] = tf32_hi_bits(x[k]);
+          lo[k] = __float_as_uint(x[k] - __uint_as_float(hi[k]));
+        }
+        const int slot = mit % NA;
+        if (!(ok = warp_wait(&ctl->a_empty[slot], ((mit / NA) & 1) ^ 1, wc))) break;
+        tc_fence_after();
+        const uint32_t a = tmem + lane_off + kDCols + slot * 64;
+        tmem_st32(a, hi);
+        tmem_st32(a + 32, lo);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->a_full[slot]);
+        if (p.release == 2) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->m_empty[stage]);
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ epilogue
+    const int t = threadIdx.x - 256;                 // output row within a 128-row block = TMEM lane
+    const int wq = warp & 3;
+    const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
+    const int V = j.V;
+    uint8_t* bhi = smem + C::OFF_BHI;
+    uint8_t* blo = smem + C::OFF_BLO;
+    float y[C::HALVES][VT];
+    int out_count = 0;
+    bool ok = true;
+
+    // initial state
+#pragma unroll
+    for (int h = 0; h < C::HALVES; ++h) {
+      const int k = t + 128 * h;
+      if (j.init_mode == kInitPointer) {
+        const float* src = j.init + u * j.init_unit_stride;
+        if (j.layout == 0) {
+#pragma unroll
+          for (int q = 0; q < VT / 4; ++q) {
+            const float4 v = *reinterpret_cast<const float4*>(src + (int64_t)k * V + v0 + 4 * q);
+            y[h][4 * q] = v.x; y[h][4 * q + 1] = v.y; y[h][4 * q + 2] = v.z; y[h][4 * q + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < VT; ++c) y[h][c] = src[(int64_t)(v0 + c) * K + k];
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < VT; ++c) y[h][c] = (j.init_mode == kInitIdentity && k == v0 + c) ? 1.f : 0.f;
+      }
+    }
+
+    // out[seg] <- y through per-warp staging and TMA stores
+    auto store_out = [&](int seg) {
+      const int b = out_count % C::NOUT;
+      if (lane == 0) bulk_wait_read<C::NOUT - 1>();
+      __syncwarp();
+#pragma unroll
+      for (int h = 0; h < C::HALVES; ++h) {
+        uint8_t* stg = smem + C::OFF_OUT + b * C::TILE + (h * 4 + wq) * 4096;
+        if (j.layout == 0) {  // [32 rows][32 floats], 128-byte swizzle: this lane's row
+          uint8_t* row = stg + lane * 128;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(row + ((q ^ (lane & 7)) << 4)) =
+                make_float4(y[h][4 * q], y[h][4 * q + 1], y[h][4 * q + 2], y[h][4 * q + 3]);
+        } else {              // [VT rows][32 floats]: column `lane`
+          float* f = reinterpret_cast<float*>(stg);
+#pragma unroll
+          for (int c = 0; c < VT; ++c) f[c * 32 + lane] = y[h][c];
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < C::HALVES; ++h) {
+          const uint8_t* stg = smem + C::OFF_OUT + b * C::TILE + (h * 4 + wq) * 4096;
+          if (j.layout == 0)
+            tma_store_2d(&p.map_out, stg, v0, (int32_t)(((int64_t)chain * j.S + seg) * K + 128 * h + 32 * wq));
+          else
+            tma_store_2d(&p.map_out, stg, 128 * h + 32 * wq, (int32_t)(((int64_t)chain * j.S + seg) * V + v0));
+        }
+        bulk_commit();
+      }
+      ++out_count;
+    };
+
+    // X -> B operand (hi and lo), K-major, 128-byte swizzle: element (n, k) of
+    // B^T sits in k-block k/32, row n, 16-byte piece ((k%32)/4) ^ (n%8).
+    auto write_b = [&]() {
+#pragma unroll
+      for (int h = 0; h < C::HALVES; ++h) {
+        const int k = t + 128 * h;
+        const uint32_t base = (uint32_t)(k >> 5) * (VT * 128) + (uint32_t)(k & 3) * 4;
+        const int piece = (k & 31) >> 2;
+#pragma unroll
+        for (int c = 0; c < VT; ++c) {
+          const uint32_t off = base + (uint32_t)(c >> 3) * 1024 + (uint32_t)(c & 7) * 128 +
+                               (uint32_t)((piece ^ (c & 7)) << 4);
+          const uint32_t hb = tf32_hi_bits(y[h][c]);
+          *reinterpret_cast<uint32_t*>(bhi + off) = hb;
+          *reinterpret_cast<float*>(blo + off) = y[h][c] - __uint_as_float(hb);
+        }
+      }
+      fence_proxy_async_smem();  // generic writes -> read by tcgen05.mma (async proxy)
+    };
+
+    if (j.out) {
+      if (p.in_place && p.has_h && nsteps > 0) ok = warp_wait(&ctl->h_full[0], 0, wc);
+      if (ok) store_out(seg_of(0));
+    }
+    if (ok && nsteps > 0) {
+      write_b();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->x_ready);
+    }
+    for (int step = 0; step < nsteps && ok; ++step) {
+      uint64_t* dbar = (p.stall_test && step == 0) ? &ctl->never : &ctl->d_full;
+      if (!(ok = warp_wait(dbar, step & 1, wc))) break;
+      tc_fence_after();
+      float d[32];
+#pragma unroll
+      for (int h = 0; h < C::HALVES; ++h) {
+        tmem_ld32(tmem + lane_off + (uint32_t)(h * VT), d);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < VT; ++c) y[h][c] = d[c];
+      }
+      const int slot = step & 1;
+      if (p.has_h) {
+        if (!(ok = warp_wait(&ctl->h_full[slot], (step >> 1) & 1, wc))) break;
+        const uint8_t* ht = smem + C::OFF_H + slot * C::TILE;
+#pragma unroll
+        for (int h = 0; h < C::HALVES; ++h) {
+          const int k = t + 128 * h;
+          if (j.layout == 0) {  // [K rows][32 floats], 128-byte swizzle
+            const uint8_t* row = ht + k * 128;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 v = *reinterpret_cast<const float4*>(row + ((q ^ (k & 7)) << 4));
+              y[h][4 * q] += v.x; y[h][4 * q + 1] += v.y; y[h][4 * q + 2] += v.z; y[h][4 * q + 3] += v.w;
+            }
+          } else {              // [VT rows][K floats]
+            const float* f = reinterpret_cast<const float*>(ht) + k;
+#pragma unroll
+            for (int c = 0; c < VT; ++c) y[h][c] += f[c * K];
+          }
+        }
+        if (p.release != 2) {
+          release_fence(p.release);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->h_empty[slot]);
+        }
+      }
+      if (step + 1 < n && j.out) {
+        if (p.in_place && p.has_h && step + 1 < nsteps)
+          if (!(ok = warp_wait(&ctl->h_full[(step + 1) & 1], ((step + 1) >> 1) & 1, wc))) break;
+        store_out(seg_of(step + 1));
+      }
+      if (step + 1 < nsteps) {
+        write_b();
+        tc_fence_before();  // D has been read (wait::ld above)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->x_ready);
+      } else if (j.fin) {
+        float* F = j.fin + u * j.fin_unit_stride;
+#pragma unroll
+        for (int h = 0; h < C::HALVES; ++h) {
+          const int k = t + 128 * h;
+          if (j.layout == 0) {
+#pragma unroll
+            for (int q = 0; q < VT / 4; ++q)
+              *reinterpret_cast<float4*>(F + (int64_t)k * V + v0 + 4 * q) =
+                  make_float4(y[h][4 * q], y[h][4 * q + 1], y[h][4 * q + 2], y[h][4 * q + 3]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < VT; ++c) F[(int64_t)(v0 + c) * K + k] = y[h][c];
+          }
+        }
+      }
+      if (p.has_h && p.release == 2) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->h_empty[slot]);
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D fp32 tensor map: `rows` x `cols` row-major at `base`, box box_cols x box_rows.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows,
+              bool swizzle128) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int K>
+cudaError_t launch_k(const SeqJob& j, int release, unsigned int* status, uint64_t limit_ns, int stall_test,
+                     cudaStream_t stream) {
+  using C = Cfg<K>;
+  TcParams p;
+  memset(&p, 0, sizeof p);
+  p.job = j;
+  p.status = status;
+  p.limit_ns = limit_ns;
+  p.has_h = j.H != nullptr;
+  p.in_place = j.out != nullptr && (const void*)j.out == (const void*)j.H;
+  p.release = release;
+  p.stall_test = stall_test;
+  const uint64_t states = (uint64_t)j.nchains * j.S;
+  const bool kv = j.layout == 0;
+  const uint64_t rows = states * (kv ? (uint64_t)K : (uint64_t)j.V);
+  const uint64_t cols = kv ? (uint64_t)j.V : (uint64_t)K;
+  // kv: box 32 columns x K rows (128-byte swizzle); vk: K columns x VT rows (TMA stores use 32-wide boxes)
+  if (p.has_h && !make_map(&p.map_h, j.H, rows, cols, kv ? 32 : K, kv ? K : VT, kv)) return cudaErrorInvalidValue;
+  if (j.out && !make_map(&p.map_out, j.out, rows, cols, 32, kv ? 32 : VT, kv)) return cudaErrorInvalidValue;
+  const bool fwd = j.direction == 0;
+  if (!make_map(&p.map_m, j.M, states * K, K, fwd ? 32 : 128, fwd ? 128 : 32, fwd)) return cudaErrorInvalidValue;
+  auto kern = seq_tc_kernel<K>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid(j.V / VT, j.nchains * j.G);
+  kern<<<grid, kThreads, C::SMEM, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supports(int K, int V) { return (K == 128 || K == 256) && V % VT == 0 && V >= VT; }
+
+cudaError_t launch_seq_tc(const SeqJob& job, int release, unsigned int* status, uint64_t limit_ns, int stall_test,
+                          cudaStream_t stream) {
+  if (!tc_supports(job.K, job.V)) return cudaErrorInvalidValue;
+  if ((int64_t)job.nchains * job.G > 65535) return cudaErrorInvalidValue;
+  if (job.h_chain_stride != (int64_t)job.S * job.K * job.V || job.m_chain_stride != (int64_t)job.S * job.K * job.K)
+    return cudaErrorInvalidValue;
+  return job.K == 128 ? launch_k<128>(job, release, status, limit_ns, stall_test, stream)
+                      : launch_k<256>(job, release, status, limit_ns, stall_test, stream);
+}
+
+}  // namespace qla
