@@ -9,8 +9,14 @@
 // engine keeps that producer/consumer shape and moves the contraction onto
 // tcgen05 with fp32 accuracy from three TF32 products:
 //     A X ~= A_hi X_hi + A_hi X_lo + A_lo X_hi,
-// with hi = the value with its 13 low mantissa bits cleared and lo = x - hi
-// (exact in fp32).  The dropped A_lo X_lo term is below 2^-22 relative.
+// with hi = x rounded to the nearest TF32 value and lo = x - hi (exact in
+// fp32) rounded to the nearest TF32 value.  Both operands reach the tensor
+// core already exact in TF32, so it drops no bits of them.  Rounding to
+// nearest matters: the tensor core cuts the 13 low mantissa bits of an fp32
+// operand toward zero, and a lo taken by truncation carries x's sign, which
+// turned that cut into a coherent shrink of about 2^-20 per step.  The
+// remaining errors (the rounding of lo, the dropped A_lo X_lo term, both
+// below 2^-22 relative) are unbiased.
 //
 // One CTA owns a VT-column tile of one unit (chain, group) for all of the
 // unit's segments.  Roles, storage, handoff and lifetime (the table the
@@ -127,7 +133,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ uint32_t tf32_hi_bits(float x) { return __float_as_uint(x) & 0xFFFFE000u; }
+// Nearest TF32 value (ties away from zero) as fp32 bits: add half of the
+// 13-bit tail, then clear the tail; a carry correctly bumps the exponent.
+__device__ __forceinline__ uint32_t tf32_rn_bits(float x) { return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u; }
+
+// x = hi + lo + r with hi, lo exact TF32 values and |r| <= 2^-22 |x|.
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = tf32_rn_bits(x);
+  lo = tf32_rn_bits(x - __uint_as_float(hi));
+}
 
 template <int K>
 __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_constant__ TcParams p) {
@@ -297,10 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
         }
         uint32_t hi[32], lo[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          hi[k] = tf32_hi_bits(x[k]);
-          lo[k] = __float_as_uint(x[k] - __uint_as_float(hi[k]));
-        }
+        for (int k = 0; k < 32; ++k) split_tf32(x[k], hi[k], lo[k]);
         const int slot = mit % NA;
         if (!(ok = warp_wait(&ctl->a_empty[slot], ((mit / NA) & 1) ^ 1, wc))) break;
         tc_fence_after();
@@ -399,9 +410,10 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
         for (int c = 0; c < VT; ++c) {
           const uint32_t off = base + (uint32_t)(c >> 3) * 1024 + (uint32_t)(c & 7) * 128 +
                                (uint32_t)((piece ^ (c & 7)) << 4);
-          const uint32_t hb = tf32_hi_bits(y[h][c]);
+          uint32_t hb, lb;
+          split_tf32(y[h][c], hb, lb);
           *reinterpret_cast<uint32_t*>(bhi + off) = hb;
-          *reinterpret_cast<float*>(blo + off) = y[h][c] - __uint_as_float(hb);
+          *reinterpret_cast<uint32_t*>(blo + off) = lb;
         }
       }
       fence_proxy_async_smem();  // generic writes -> read by tcgen05.mma (async proxy)
