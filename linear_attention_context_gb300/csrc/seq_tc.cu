@@ -18,6 +18,14 @@
 // remaining errors (the rounding of lo, the dropped A_lo X_lo term, both
 // below 2^-22 relative) are unbiased.
 //
+// Accumulation: the tensor core also rounds its fp32 accumulator toward zero,
+// so a long chain of MMAs into one accumulator shrinks the result coherently
+// (measured about -6e-7 per step with 48 MMAs per output).  The big A_hi X_hi
+// terms therefore go into a fresh partial accumulator per 32-wide k chunk
+// (4 MMAs each), which the epilogue drains into fp32 registers with
+// round-to-nearest adds while the next chunk runs; the small terms, 2^-11 of
+// the result, keep one accumulator per 128-row block.
+//
 // One CTA owns a VT-column tile of one unit (chain, group) for all of the
 // unit's segments.  Roles, storage, handoff and lifetime (the table the
 // mlc.ai page "调试 Warp-Specialized Kernels", section "先写清楚数据如何交接",
@@ -27,11 +35,14 @@
 //  producer  0 (1 th) TMA: H_j tile -> h slot j&1; A_j in 32-column chunks
 //                     -> m ring (NM stages).  Needs no state: runs ahead.
 //  mma       1 (1 th) tcgen05.mma kind::tf32, A from TMEM, B (= X_j hi/lo,
-//                     K-major, 128-byte swizzle) from shared memory, D in TMEM.
+//                     K-major, 128-byte swizzle) from shared memory; big terms
+//                     into a 2-deep ring of partial accumulators P, small
+//                     terms into Ds, all in TMEM.
 //  splitter  4..7     m chunk (ordinary shared loads) -> hi/lo -> TMEM A ring
 //                     (NA slots of 64 columns).
-//  epilogue  8..11    D (tcgen05.ld) + H_j (ordinary shared loads) -> out via
-//                     per-warp TMA stores; X_{j+1} hi/lo -> B operand.
+//  epilogue  8..11    sum of P (drained per chunk) + Ds (tcgen05.ld) + H_j
+//                     (ordinary shared loads) -> out via per-warp TMA
+//                     stores; X_{j+1} hi/lo -> B operand.
 //
 //  storage        written by           read by             reusable after
 //  m ring [s]     TMA (async)          splitter (generic)  splitter's last read: fence + m_empty arrive
@@ -39,13 +50,14 @@
 //  A ring (TMEM)  splitter tcgen05.st  mma (async)         mma commit -> a_empty
 //  B hi/lo        epilogue st.shared   mma (async)         d_full (all MMAs of the step done)
 //                 + fence.proxy.async
-//  D (TMEM)       mma                  epilogue tcgen05.ld x_ready (epilogue's wait::ld done)
+//  P ring (TMEM)  mma                  epilogue tcgen05.ld p_empty (epilogue's wait::ld done)
+//  Ds (TMEM)      mma                  epilogue tcgen05.ld x_ready (epilogue's wait::ld done)
 //  out staging    epilogue st.shared   TMA store (async)   bulk wait_group.read
 //                 + fence.proxy.async
 //
 // Barriers: m_full/h_full count 1 + transaction bytes; m_empty, h_empty,
-// a_full, x_ready count 4 (one arrive per warp after __syncwarp); a_empty,
-// d_full count 1 (tcgen05.commit).  Producers wait their empty barriers with
+// a_full, p_empty, x_ready count 4 (one arrive per warp after __syncwarp);
+// a_empty, p_full, d_full count 1 (tcgen05.commit).  Producers wait their empty barriers with
 // the parity of (use / slots) ^ 1, consumers their full barriers with
 // (use / slots), so the first producer wait passes at once.
 //
@@ -77,8 +89,11 @@ constexpr int VT = 32;            // state columns per CTA
 constexpr int kThreads = 384;     // 12 warps
 constexpr uint32_t kChunkBytes = 128 * 32 * 4;  // one A chunk: 128 rows x 32 columns fp32
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kDCols = 64;   // D at columns [0, 64); the A ring follows
-constexpr int NA = 6;             // TMEM A slots (64 columns: hi then lo)
+constexpr uint32_t kPCol = 0;     // partial accumulator ring: 2 x VT columns
+constexpr uint32_t kDsCol = 64;   // small-term accumulators: one VT block per 128-row block
+constexpr uint32_t kACol = 128;   // A ring: NA slots of 64 columns (hi then lo)
+constexpr int NA = 6;
+constexpr int NP = 2;
 
 template <int K>
 struct Cfg {
@@ -115,6 +130,7 @@ struct TcParams {
 struct Ctrl {
   uint64_t m_full[6], m_empty[6];
   uint64_t a_full[NA], a_empty[NA];
+  uint64_t p_full[NP], p_empty[NP];
   uint64_t h_full[2], h_empty[2];
   uint64_t x_ready, d_full, never, mma_done;
   uint32_t tmem_base;
@@ -171,6 +187,10 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
     for (int i = 0; i < NA; ++i) {
       mbar_init(&ctl->a_full[i], 4);
       mbar_init(&ctl->a_empty[i], 1);
+    }
+    for (int i = 0; i < NP; ++i) {
+      mbar_init(&ctl->p_full[i], 1);
+      mbar_init(&ctl->p_empty[i], 4);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->h_full[i], 1);
@@ -247,18 +267,21 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       constexpr uint32_t idesc = idesc_tf32(128, VT);
       const uint32_t bhi = smem_u32(smem + C::OFF_BHI);
       const uint32_t blo = smem_u32(smem + C::OFF_BLO);
-      uint32_t ait = 0;
+      uint32_t ait = 0, pit = 0;
       bool ok = true;
       for (int step = 0; step < nsteps && ok; ++step) {
         if (!(ok = mbar_wait(&ctl->x_ready, step & 1, wc))) break;
         tc_fence_after();
         for (int h = 0; h < C::HALVES && ok; ++h) {
-          const uint32_t d = tmem + (uint32_t)(h * VT);
-          for (int kc = 0; kc < C::KCH; ++kc, ++ait) {
+          const uint32_t ds = tmem + kDsCol + (uint32_t)(h * VT);
+          for (int kc = 0; kc < C::KCH; ++kc, ++ait, ++pit) {
             const int slot = ait % NA;
             if (!(ok = mbar_wait(&ctl->a_full[slot], (ait / NA) & 1, wc))) break;
+            const int pb = pit % NP;
+            if (!(ok = mbar_wait(&ctl->p_empty[pb], ((pit / NP) & 1) ^ 1, wc))) break;
             tc_fence_after();
-            const uint32_t a_hi = tmem + kDCols + slot * 64;
+            const uint32_t pacc = tmem + kPCol + (uint32_t)(pb * VT);
+            const uint32_t a_hi = tmem + kACol + slot * 64;
             const uint32_t a_lo = a_hi + 32;
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
@@ -266,11 +289,12 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
               const uint32_t off = (uint32_t)kc * (VT * 128) + (uint32_t)s * 32;
               const uint64_t dh = smem_desc_sw128(bhi + off, 1024);
               const uint64_t dl = smem_desc_sw128(blo + off, 1024);
-              mma_tf32_ts(d, a_hi + s * 8, dh, idesc, (kc | s) != 0);
-              mma_tf32_ts(d, a_hi + s * 8, dl, idesc, 1);
-              mma_tf32_ts(d, a_lo + s * 8, dh, idesc, 1);
+              mma_tf32_ts(pacc, a_hi + s * 8, dh, idesc, s != 0);
+              mma_tf32_ts(ds, a_hi + s * 8, dl, idesc, (kc | s) != 0);
+              mma_tf32_ts(ds, a_lo + s * 8, dh, idesc, 1);
             }
             mma_commit(&ctl->a_empty[slot]);
+            mma_commit(&ctl->p_full[pb]);
           }
         }
         if (ok) mma_commit(&ctl->d_full);
@@ -315,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
         const int slot = mit % NA;
         if (!(ok = warp_wait(&ctl->a_empty[slot], ((mit / NA) & 1) ^ 1, wc))) break;
         tc_fence_after();
-        const uint32_t a = tmem + lane_off + kDCols + slot * 64;
+        const uint32_t a = tmem + lane_off + kACol + slot * 64;
         tmem_st32(a, hi);
         tmem_st32(a + 32, lo);
         tmem_wait_st();
@@ -338,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
     uint8_t* blo = smem + C::OFF_BLO;
     float y[C::HALVES][VT];
     int out_count = 0;
+    uint32_t pit = 0;
     bool ok = true;
 
     // initial state
@@ -429,16 +454,37 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       if (lane == 0) mbar_arrive(&ctl->x_ready);
     }
     for (int step = 0; step < nsteps && ok; ++step) {
-      uint64_t* dbar = (p.stall_test && step == 0) ? &ctl->never : &ctl->d_full;
-      if (!(ok = warp_wait(dbar, step & 1, wc))) break;
-      tc_fence_after();
+      // big terms: drain the partial accumulators chunk by chunk (round-to-nearest adds)
+#pragma unroll
+      for (int h = 0; h < C::HALVES; ++h)
+#pragma unroll
+        for (int c = 0; c < VT; ++c) y[h][c] = 0.f;
       float d[32];
+      for (int h = 0; h < C::HALVES && ok; ++h) {
+        for (int kc = 0; kc < C::KCH; ++kc, ++pit) {
+          const int pb = pit % NP;
+          uint64_t* pbar = (p.stall_test && step == 0) ? &ctl->never : &ctl->p_full[pb];
+          if (!(ok = warp_wait(pbar, (pit / NP) & 1, wc))) break;
+          tc_fence_after();
+          tmem_ld32(tmem + lane_off + kPCol + (uint32_t)(pb * VT), d);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->p_empty[pb]);
+#pragma unroll
+          for (int c = 0; c < VT; ++c) y[h][c] += d[c];
+        }
+      }
+      if (!ok) break;
+      // small terms
+      if (!(ok = warp_wait(&ctl->d_full, step & 1, wc))) break;
+      tc_fence_after();
 #pragma unroll
       for (int h = 0; h < C::HALVES; ++h) {
-        tmem_ld32(tmem + lane_off + (uint32_t)(h * VT), d);
+        tmem_ld32(tmem + lane_off + kDsCol + (uint32_t)(h * VT), d);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < VT; ++c) y[h][c] = d[c];
+        for (int c = 0; c < VT; ++c) y[h][c] += d[c];
       }
       const int slot = step & 1;
       if (p.has_h) {
@@ -473,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       }
       if (step + 1 < nsteps) {
         write_b();
-        tc_fence_before();  // D has been read (wait::ld above)
+        tc_fence_before();  // Ds has been read (wait::ld above)
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->x_ready);
       } else if (j.fin) {
