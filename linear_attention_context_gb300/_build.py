@@ -36,8 +36,8 @@ def compile_flags(extra=()):
             *extra]
 
 
-def _compile(src, extra):
-    obj = os.path.join(OBJ, os.path.basename(src) + ".o")
+def _compile(src, extra, objdir=OBJ):
+    obj = os.path.join(objdir, os.path.basename(src) + ".o")
     cmd = [nvcc(), *compile_flags(extra), "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -46,17 +46,20 @@ def _compile(src, extra):
     return obj, r.stderr
 
 
-def build(extra=(), verbose=False):
-    os.makedirs(OBJ, exist_ok=True)
+def build(extra=(), verbose=False, out=None):
+    """Compiles and links the library; `extra` adds nvcc flags, `out` writes a
+    variant build to another path (its objects go to a sibling folder)."""
+    objdir = OBJ if out is None else out + ".obj"
+    os.makedirs(objdir, exist_ok=True)
     srcs = sources()
     with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
-        results = list(ex.map(lambda s: _compile(s, extra), srcs))
+        results = list(ex.map(lambda s: _compile(s, extra, objdir), srcs))
     if verbose:
         for _, err in results:
             if err:
                 sys.stderr.write(err)
     objs = [o for o, _ in results]
-    out = library_path()
+    out = out or library_path()
     tmp = out + ".tmp"
     cmd = [nvcc(), "-gencode", GENCODE, "-shared", "-Xcompiler", "-fPIC", "-cudart", "static",
            *objs, "-o", tmp]

@@ -80,6 +80,21 @@
 #include "ptx.cuh"
 #include "qla_internal.h"
 
+// Optional pipeline trace (compile with -DQLA_TRACE): clock64() stamps of
+// every handoff of CTA (0, 0), read back with qla_debug_trace().  Slots are
+// [role][step][event][chunk]; roles 0 producer, 1 mma, 2 splitter, 3 epilogue.
+#ifdef QLA_TRACE
+__device__ long long g_qla_trace[4 * 8 * 8 * 16];
+#define QLA_TR(role, step, ev, ch)                                                         \
+  do {                                                                                   \
+    if (tr && (step) < 8 && (ch) < 16) g_qla_trace[(((role) * 8 + (step)) * 8 + (ev)) * 16 + (ch)] = clock64(); \
+  } while (0)
+#else
+#define QLA_TR(role, step, ev, ch) \
+  do {                             \
+  } while (0)
+#endif
+
 namespace qla {
 namespace {
 
@@ -178,6 +193,10 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
   const int v0 = blockIdx.x * VT;
   const bool fwd = j.direction == 0;
   auto seg_of = [&](int step) { return fwd ? s_lo + step : s_lo + n - 1 - step; };
+#ifdef QLA_TRACE
+  const bool tr = blockIdx.x == 0 && blockIdx.y == 0 &&
+                  (threadIdx.x == 0 || threadIdx.x == 32 || threadIdx.x == 128 || threadIdx.x == 256);
+#endif
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NM; ++i) {
@@ -212,6 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   WaitCtl wc{&ctl->abort, p.status, p.limit_ns};
+  QLA_TR(0, 0, 7, 0);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -236,10 +256,12 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
           else
             tma_load_2d(smem + C::OFF_H + slot * C::TILE, &p.map_h, 0, (int32_t)(hrow0 + v0), &ctl->h_full[slot]);
           ++hissued;
+          QLA_TR(0, step, 0, 0);
         }
         for (int c = 0; c < C::CPS; ++c, ++mit) {
           const int stage = mit % C::NM;
           if (!(ok = mbar_wait(&ctl->m_empty[stage], ((mit / C::NM) & 1) ^ 1, wc))) break;
+          QLA_TR(0, step, 1, c);
           mbar_arrive_expect_tx(&ctl->m_full[stage], kChunkBytes);
           const int h = c / C::KCH, kc = c % C::KCH;
           uint8_t* dst = smem + C::OFF_M + stage * kChunkBytes;
@@ -271,14 +293,17 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       bool ok = true;
       for (int step = 0; step < nsteps && ok; ++step) {
         if (!(ok = mbar_wait(&ctl->x_ready, step & 1, wc))) break;
+        QLA_TR(1, step, 0, 0);
         tc_fence_after();
         for (int h = 0; h < C::HALVES && ok; ++h) {
           const uint32_t ds = tmem + kDsCol + (uint32_t)(h * VT);
           for (int kc = 0; kc < C::KCH; ++kc, ++ait, ++pit) {
             const int slot = ait % NA;
             if (!(ok = mbar_wait(&ctl->a_full[slot], (ait / NA) & 1, wc))) break;
+            QLA_TR(1, step, 1, h * C::KCH + kc);
             const int pb = pit % NP;
             if (!(ok = mbar_wait(&ctl->p_empty[pb], ((pit / NP) & 1) ^ 1, wc))) break;
+            QLA_TR(1, step, 2, h * C::KCH + kc);
             tc_fence_after();
             const uint32_t pacc = tmem + kPCol + (uint32_t)(pb * VT);
             const uint32_t a_hi = tmem + kACol + slot * 64;
@@ -295,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
             }
             mma_commit(&ctl->a_empty[slot]);
             mma_commit(&ctl->p_full[pb]);
+            QLA_TR(1, step, 3, h * C::KCH + kc);
           }
         }
         if (ok) mma_commit(&ctl->d_full);
@@ -314,6 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       for (int c = 0; c < C::CPS; ++c, ++mit) {
         const int stage = mit % C::NM;
         if (!(ok = warp_wait(&ctl->m_full[stage], (mit / C::NM) & 1, wc))) break;
+        QLA_TR(2, step, 0, c);
         const uint8_t* chunk = smem + C::OFF_M + stage * kChunkBytes;
         float x[32];
         if (fwd) {  // row t of a [128][32] tile, 16-byte pieces swizzled by (t & 7)
@@ -338,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
         for (int k = 0; k < 32; ++k) split_tf32(x[k], hi[k], lo[k]);
         const int slot = mit % NA;
         if (!(ok = warp_wait(&ctl->a_empty[slot], ((mit / NA) & 1) ^ 1, wc))) break;
+        QLA_TR(2, step, 1, c);
         tc_fence_after();
         const uint32_t a = tmem + lane_off + kACol + slot * 64;
         tmem_st32(a, hi);
@@ -346,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->a_full[slot]);
+        QLA_TR(2, step, 2, c);
         if (p.release == 2) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl->m_empty[stage]);
@@ -465,6 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
           const int pb = pit % NP;
           uint64_t* pbar = (p.stall_test && step == 0) ? &ctl->never : &ctl->p_full[pb];
           if (!(ok = warp_wait(pbar, (pit / NP) & 1, wc))) break;
+          QLA_TR(3, step, 0, h * C::KCH + kc);
           tc_fence_after();
           tmem_ld32(tmem + lane_off + kPCol + (uint32_t)(pb * VT), d);
           tmem_wait_ld();
@@ -478,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       if (!ok) break;
       // small terms
       if (!(ok = warp_wait(&ctl->d_full, step & 1, wc))) break;
+      QLA_TR(3, step, 1, 0);
       tc_fence_after();
 #pragma unroll
       for (int h = 0; h < C::HALVES; ++h) {
@@ -489,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       const int slot = step & 1;
       if (p.has_h) {
         if (!(ok = warp_wait(&ctl->h_full[slot], (step >> 1) & 1, wc))) break;
+        QLA_TR(3, step, 2, 0);
         const uint8_t* ht = smem + C::OFF_H + slot * C::TILE;
 #pragma unroll
         for (int h = 0; h < C::HALVES; ++h) {
@@ -516,12 +548,14 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
         if (p.in_place && p.has_h && step + 1 < nsteps)
           if (!(ok = warp_wait(&ctl->h_full[(step + 1) & 1], ((step + 1) >> 1) & 1, wc))) break;
         store_out(seg_of(step + 1));
+        QLA_TR(3, step, 3, 0);
       }
       if (step + 1 < nsteps) {
         write_b();
         tc_fence_before();  // Ds has been read (wait::ld above)
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->x_ready);
+        QLA_TR(3, step, 4, 0);
       } else if (j.fin) {
         float* F = j.fin + u * j.fin_unit_stride;
 #pragma unroll
@@ -618,6 +652,14 @@ cudaError_t launch_k(const SeqJob& j, int release, unsigned int* status, uint64_
 }
 
 }  // namespace
+
+#ifdef QLA_TRACE
+extern "C" __attribute__((visibility("default"))) int qla_debug_trace(long long* out, int n) {
+  const int total = 4 * 8 * 8 * 16;
+  if (n > total) n = total;
+  return cudaMemcpyFromSymbol(out, g_qla_trace, sizeof(long long) * n) == cudaSuccess ? n : -1;
+}
+#endif
 
 bool tc_supports(int K, int V) { return (K == 128 || K == 256) && V % VT == 0 && V >= VT; }
 
