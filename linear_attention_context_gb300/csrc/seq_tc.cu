@@ -20,12 +20,16 @@
 //
 // Accumulation: the tensor core also rounds its fp32 accumulator toward zero,
 // so a long chain of MMAs into one accumulator shrinks the result coherently
-// (measured about -6e-7 per step with 48 MMAs per output).  The big A_hi X_hi
-// terms therefore go into a fresh partial accumulator per 32-wide k chunk
-// (4 MMAs each), which the epilogue drains into fp32 registers with
-// round-to-nearest adds while the next chunk runs; the small terms, 2^-11 of
-// the result, keep one accumulator per 128-row block.
-//
+// (measured about -6e-7 per step with 48 MMAs per output).  And an MMA that
+// accumulates into the result of the one just issued waits for it: with
+// N = 32 such a dependent chain runs at about 120 cycles per MMA instead of
+// the tensor pipe's ~16.  Both are solved by spreading the k reduction over
+// independent accumulators: per 128-row block, NB "big" chains take A_hi X_hi
+// of k-steps ks = r (mod NB) and NS "small" chains take the A_hi X_lo and
+// A_lo X_hi terms, so no chain sees more than 4 big MMAs per step and
+// dependent MMAs are at least 6 issues apart.  The epilogue adds the chains
+// pairwise with round-to-nearest fp32 adds.
+
 // One CTA owns a VT-column tile of one unit (chain, group) for all of the
 // unit's segments.  Roles, storage, handoff and lifetime (the table the
 // mlc.ai page "调试 Warp-Specialized Kernels", section "先写清楚数据如何交接",
@@ -35,14 +39,14 @@
 //  producer  0 (1 th) TMA: H_j tile -> h slot j&1; A_j in 32-column chunks
 //                     -> m ring (NM stages).  Needs no state: runs ahead.
 //  mma       1 (1 th) tcgen05.mma kind::tf32, A from TMEM, B (= X_j hi/lo,
-//                     K-major, 128-byte swizzle) from shared memory; big terms
-//                     into a 2-deep ring of partial accumulators P, small
-//                     terms into Ds, all in TMEM.
+//                     K-major, 128-byte swizzle) from shared memory, into the
+//                     NB + NS accumulator chains per 128-row block (TMEM).
 //  splitter  4..7     m chunk (ordinary shared loads) -> hi/lo -> TMEM A ring
 //                     (NA slots of 64 columns).
-//  epilogue  8..11    sum of P (drained per chunk) + Ds (tcgen05.ld) + H_j
-//                     (ordinary shared loads) -> out via per-warp TMA
-//                     stores; X_{j+1} hi/lo -> B operand.
+//  epilogue  8..11    sum of the chains (tcgen05.ld) + H_j (ordinary shared
+//                     loads) = X_{j+1}; its hi/lo -> B operand first (the
+//                     next step waits on it), then the h-slot release and
+//                     out via per-warp TMA stores.
 //
 //  storage        written by           read by             reusable after
 //  m ring [s]     TMA (async)          splitter (generic)  splitter's last read: fence + m_empty arrive
@@ -50,14 +54,14 @@
 //  A ring (TMEM)  splitter tcgen05.st  mma (async)         mma commit -> a_empty
 //  B hi/lo        epilogue st.shared   mma (async)         d_full (all MMAs of the step done)
 //                 + fence.proxy.async
-//  P ring (TMEM)  mma                  epilogue tcgen05.ld p_empty (epilogue's wait::ld done)
-//  Ds (TMEM)      mma                  epilogue tcgen05.ld x_ready (epilogue's wait::ld done)
+//  chains (TMEM)  mma                  epilogue tcgen05.ld x_ready (epilogue's wait::ld done)
 //  out staging    epilogue st.shared   TMA store (async)   bulk wait_group.read
 //                 + fence.proxy.async
 //
-// Barriers: m_full/h_full count 1 + transaction bytes; m_empty, h_empty,
-// a_full, p_empty, x_ready count 4 (one arrive per warp after __syncwarp);
-// a_empty, p_full, d_full count 1 (tcgen05.commit).  Producers wait their empty barriers with
+// Chunks go kc-major: chunk c = kc * HALVES + h is A[128h.., 32kc..], so the
+// two row blocks of K = 256 interleave.  Barriers: m_full/h_full count 1 +
+// transaction bytes; m_empty, h_empty, a_full, x_ready count 4 (one arrive per
+// warp after __syncwarp); a_empty, d_full count 1 (tcgen05.commit).  Producers wait their empty barriers with
 // the parity of (use / slots) ^ 1, consumers their full barriers with
 // (use / slots), so the first producer wait passes at once.
 //
@@ -104,11 +108,8 @@ constexpr int VT = 32;            // state columns per CTA
 constexpr int kThreads = 384;     // 12 warps
 constexpr uint32_t kChunkBytes = 128 * 32 * 4;  // one A chunk: 128 rows x 32 columns fp32
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kPCol = 0;     // partial accumulator ring: 2 x VT columns
-constexpr uint32_t kDsCol = 64;   // small-term accumulators: one VT block per 128-row block
-constexpr uint32_t kACol = 128;   // A ring: NA slots of 64 columns (hi then lo)
-constexpr int NA = 6;
-constexpr int NP = 2;
+constexpr uint32_t kACol = 256;   // accumulator chains in [0, 256); A ring: NA slots of 64 columns (hi, lo)
+constexpr int NA = 4;
 
 template <int K>
 struct Cfg {
@@ -117,6 +118,9 @@ struct Cfg {
   static constexpr int CPS = HALVES * KCH;         // chunks per step
   static constexpr int NM = K == 128 ? 6 : 4;      // m ring stages
   static constexpr int NOUT = K == 128 ? 2 : 1;    // out staging buffers
+  static constexpr int NB = K == 128 ? 4 : 2;      // big-term chains per 128-row block
+  static constexpr int NS = K == 128 ? 4 : 2;      // small-term chains per 128-row block
+  static_assert(HALVES * (NB + NS) * VT <= (int)kACol, "accumulator columns");
   static constexpr uint32_t TILE = (uint32_t)K * VT * 4;  // one state tile (bytes)
   static constexpr uint32_t OFF_M = 0;
   static constexpr uint32_t OFF_H = OFF_M + NM * kChunkBytes;
@@ -145,7 +149,6 @@ struct TcParams {
 struct Ctrl {
   uint64_t m_full[6], m_empty[6];
   uint64_t a_full[NA], a_empty[NA];
-  uint64_t p_full[NP], p_empty[NP];
   uint64_t h_full[2], h_empty[2];
   uint64_t x_ready, d_full, never, mma_done;
   uint32_t tmem_base;
@@ -207,10 +210,6 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       mbar_init(&ctl->a_full[i], 4);
       mbar_init(&ctl->a_empty[i], 1);
     }
-    for (int i = 0; i < NP; ++i) {
-      mbar_init(&ctl->p_full[i], 1);
-      mbar_init(&ctl->p_empty[i], 4);
-    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->h_full[i], 1);
       mbar_init(&ctl->h_empty[i], 4);
@@ -263,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
           if (!(ok = mbar_wait(&ctl->m_empty[stage], ((mit / C::NM) & 1) ^ 1, wc))) break;
           QLA_TR(0, step, 1, c);
           mbar_arrive_expect_tx(&ctl->m_full[stage], kChunkBytes);
-          const int h = c / C::KCH, kc = c % C::KCH;
+          const int kc = c / C::HALVES, h = c % C::HALVES;
           uint8_t* dst = smem + C::OFF_M + stage * kChunkBytes;
           if (fwd)  // A = M: rows 128h.., columns 32kc..  (128-byte swizzle, box 32 x 128)
             tma_load_2d(dst, &p.map_m, 32 * kc, (int32_t)(mrow0 + 128 * h), &ctl->m_full[stage]);
@@ -289,39 +288,41 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       constexpr uint32_t idesc = idesc_tf32(128, VT);
       const uint32_t bhi = smem_u32(smem + C::OFF_BHI);
       const uint32_t blo = smem_u32(smem + C::OFF_BLO);
-      uint32_t ait = 0, pit = 0;
+      uint32_t ait = 0;
       bool ok = true;
       for (int step = 0; step < nsteps && ok; ++step) {
         if (!(ok = mbar_wait(&ctl->x_ready, step & 1, wc))) break;
         QLA_TR(1, step, 0, 0);
         tc_fence_after();
-        for (int h = 0; h < C::HALVES && ok; ++h) {
-          const uint32_t ds = tmem + kDsCol + (uint32_t)(h * VT);
-          for (int kc = 0; kc < C::KCH; ++kc, ++ait, ++pit) {
-            const int slot = ait % NA;
-            if (!(ok = mbar_wait(&ctl->a_full[slot], (ait / NA) & 1, wc))) break;
-            QLA_TR(1, step, 1, h * C::KCH + kc);
-            const int pb = pit % NP;
-            if (!(ok = mbar_wait(&ctl->p_empty[pb], ((pit / NP) & 1) ^ 1, wc))) break;
-            QLA_TR(1, step, 2, h * C::KCH + kc);
-            tc_fence_after();
-            const uint32_t pacc = tmem + kPCol + (uint32_t)(pb * VT);
-            const uint32_t a_hi = tmem + kACol + slot * 64;
-            const uint32_t a_lo = a_hi + 32;
+        uint32_t written = 0;  // chains already holding a value this step
+        for (int c = 0; c < C::CPS; ++c, ++ait) {
+          const int kc = c / C::HALVES, h = c % C::HALVES;
+          const int slot = ait % NA;
+          if (!(ok = mbar_wait(&ctl->a_full[slot], (ait / NA) & 1, wc))) break;
+          QLA_TR(1, step, 1, c);
+          tc_fence_after();
+          const uint32_t a_hi = tmem + kACol + slot * 64;
+          const uint32_t a_lo = a_hi + 32;
+          const int q0 = h * (C::NB + C::NS);
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-              // B rows k in [32kc + 8s, +8): k-block kc, 32 bytes per 8 tf32 inside the swizzled row
-              const uint32_t off = (uint32_t)kc * (VT * 128) + (uint32_t)s * 32;
-              const uint64_t dh = smem_desc_sw128(bhi + off, 1024);
-              const uint64_t dl = smem_desc_sw128(blo + off, 1024);
-              mma_tf32_ts(pacc, a_hi + s * 8, dh, idesc, s != 0);
-              mma_tf32_ts(ds, a_hi + s * 8, dl, idesc, (kc | s) != 0);
-              mma_tf32_ts(ds, a_lo + s * 8, dh, idesc, 1);
-            }
-            mma_commit(&ctl->a_empty[slot]);
-            mma_commit(&ctl->p_full[pb]);
-            QLA_TR(1, step, 3, h * C::KCH + kc);
+          for (int s = 0; s < 4; ++s) {
+            const int ks = kc * 4 + s;
+            const int qb = q0 + ks % C::NB;
+            const int q1 = q0 + C::NB + ks % C::NS;
+            const int q2 = q0 + C::NB + (ks + C::NS / 2) % C::NS;
+            // B rows k in [32kc + 8s, +8): k-block kc, 32 bytes per 8 tf32 inside the swizzled row
+            const uint32_t off = (uint32_t)kc * (VT * 128) + (uint32_t)s * 32;
+            const uint64_t dh = smem_desc_sw128(bhi + off, 1024);
+            const uint64_t dl = smem_desc_sw128(blo + off, 1024);
+            mma_tf32_ts(tmem + qb * VT, a_hi + s * 8, dh, idesc, (written >> qb) & 1);
+            written |= 1u << qb;
+            mma_tf32_ts(tmem + q1 * VT, a_hi + s * 8, dl, idesc, (written >> q1) & 1);
+            written |= 1u << q1;
+            mma_tf32_ts(tmem + q2 * VT, a_lo + s * 8, dh, idesc, (written >> q2) & 1);
+            written |= 1u << q2;
           }
+          mma_commit(&ctl->a_empty[slot]);
+          QLA_TR(1, step, 3, c);
         }
         if (ok) mma_commit(&ctl->d_full);
       }
@@ -391,7 +392,6 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
     uint8_t* blo = smem + C::OFF_BLO;
     float y[C::HALVES][VT];
     int out_count = 0;
-    uint32_t pit = 0;
     bool ok = true;
 
     // initial state
@@ -473,50 +473,55 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       fence_proxy_async_smem();  // generic writes -> read by tcgen05.mma (async proxy)
     };
 
-    if (j.out) {
-      if (p.in_place && p.has_h && nsteps > 0) ok = warp_wait(&ctl->h_full[0], 0, wc);
-      if (ok) store_out(seg_of(0));
-    }
-    if (ok && nsteps > 0) {
+    // Sum of the accumulator chains of one 128-row block: pairwise, round-to-nearest.
+    auto drain = [&](int h, float (&acc)[VT]) {
+      float a[32], b[32];
+      const uint32_t base = tmem + lane_off + (uint32_t)(h * (C::NB + C::NS) * VT);
+      tmem_ld32(base + 0 * VT, a);
+      tmem_ld32(base + 1 * VT, b);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < VT; ++c) acc[c] = a[c] + b[c];
+      if (C::NB == 4) {
+        tmem_ld32(base + 2 * VT, a);
+        tmem_ld32(base + 3 * VT, b);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < VT; ++c) acc[c] += a[c] + b[c];
+      }
+      float sm[VT];
+      tmem_ld32(base + (C::NB + 0) * VT, a);
+      tmem_ld32(base + (C::NB + 1) * VT, b);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < VT; ++c) sm[c] = a[c] + b[c];
+      if (C::NS == 4) {
+        tmem_ld32(base + (C::NB + 2) * VT, a);
+        tmem_ld32(base + (C::NB + 3) * VT, b);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < VT; ++c) sm[c] += a[c] + b[c];
+      }
+#pragma unroll
+      for (int c = 0; c < VT; ++c) acc[c] += sm[c];
+    };
+
+    if (nsteps > 0) {  // X_0 -> B operand first: the first step's MMAs wait on it
       write_b();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->x_ready);
     }
+    if (j.out) {
+      if (p.in_place && p.has_h && nsteps > 0) ok = warp_wait(&ctl->h_full[0], 0, wc);
+      if (ok) store_out(seg_of(0));
+    }
     for (int step = 0; step < nsteps && ok; ++step) {
-      // big terms: drain the partial accumulators chunk by chunk (round-to-nearest adds)
-#pragma unroll
-      for (int h = 0; h < C::HALVES; ++h)
-#pragma unroll
-        for (int c = 0; c < VT; ++c) y[h][c] = 0.f;
-      float d[32];
-      for (int h = 0; h < C::HALVES && ok; ++h) {
-        for (int kc = 0; kc < C::KCH; ++kc, ++pit) {
-          const int pb = pit % NP;
-          uint64_t* pbar = (p.stall_test && step == 0) ? &ctl->never : &ctl->p_full[pb];
-          if (!(ok = warp_wait(pbar, (pit / NP) & 1, wc))) break;
-          QLA_TR(3, step, 0, h * C::KCH + kc);
-          tc_fence_after();
-          tmem_ld32(tmem + lane_off + kPCol + (uint32_t)(pb * VT), d);
-          tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl->p_empty[pb]);
-#pragma unroll
-          for (int c = 0; c < VT; ++c) y[h][c] += d[c];
-        }
-      }
-      if (!ok) break;
-      // small terms
-      if (!(ok = warp_wait(&ctl->d_full, step & 1, wc))) break;
+      uint64_t* dbar = (p.stall_test && step == 0) ? &ctl->never : &ctl->d_full;
+      if (!(ok = warp_wait(dbar, step & 1, wc))) break;
       QLA_TR(3, step, 1, 0);
       tc_fence_after();
 #pragma unroll
-      for (int h = 0; h < C::HALVES; ++h) {
-        tmem_ld32(tmem + lane_off + kDsCol + (uint32_t)(h * VT), d);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < VT; ++c) y[h][c] += d[c];
-      }
+      for (int h = 0; h < C::HALVES; ++h) drain(h, y[h]);
       const int slot = step & 1;
       if (p.has_h) {
         if (!(ok = warp_wait(&ctl->h_full[slot], (step >> 1) & 1, wc))) break;
@@ -538,21 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
             for (int c = 0; c < VT; ++c) y[h][c] += f[c * K];
           }
         }
-        if (p.release != 2) {
-          release_fence(p.release);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl->h_empty[slot]);
-        }
       }
-      if (step + 1 < n && j.out) {
-        if (p.in_place && p.has_h && step + 1 < nsteps)
-          if (!(ok = warp_wait(&ctl->h_full[(step + 1) & 1], ((step + 1) >> 1) & 1, wc))) break;
-        store_out(seg_of(step + 1));
-        QLA_TR(3, step, 3, 0);
-      }
-      if (step + 1 < nsteps) {
+      if (step + 1 < nsteps) {  // X_{j+1} -> B operand: the critical path to the next step
         write_b();
-        tc_fence_before();  // Ds has been read (wait::ld above)
+        tc_fence_before();  // the chains have been read (wait::ld in drain)
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->x_ready);
         QLA_TR(3, step, 4, 0);
@@ -571,6 +565,17 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
             for (int c = 0; c < VT; ++c) F[(int64_t)(v0 + c) * K + k] = y[h][c];
           }
         }
+      }
+      if (p.has_h && p.release != 2) {  // the h slot's last ordinary read is done: release it
+        release_fence(p.release);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->h_empty[slot]);
+      }
+      if (step + 1 < n && j.out) {
+        if (p.in_place && p.has_h && step + 1 < nsteps)
+          if (!(ok = warp_wait(&ctl->h_full[(step + 1) & 1], ((step + 1) >> 1) & 1, wc))) break;
+        store_out(seg_of(step + 1));
+        QLA_TR(3, step, 3, 0);
       }
       if (p.has_h && p.release == 2) {
         __syncwarp();
