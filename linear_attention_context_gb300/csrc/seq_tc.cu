@@ -43,10 +43,10 @@
 //                     NB + NS accumulator chains per 128-row block (TMEM).
 //  splitter  4..7     m chunk (ordinary shared loads) -> hi/lo -> TMEM A ring
 //                     (NA slots of 64 columns).
-//  epilogue  8..11    sum of the chains (tcgen05.ld) + H_j (ordinary shared
-//                     loads) = X_{j+1}; its hi/lo -> B operand first (the
-//                     next step waits on it), then the h-slot release and
-//                     out via per-warp TMA stores.
+//  epilogue  8..11    H_j (ordinary shared loads, then the h-slot release)
+//                     + the chains (tcgen05.ld) = X_{j+1}; its hi/lo -> B
+//                     operand first (the next step waits on it), then out
+//                     via per-warp TMA stores.
 //
 //  storage        written by           read by             reusable after
 //  m ring [s]     TMA (async)          splitter (generic)  splitter's last read: fence + m_empty arrive
@@ -177,6 +177,33 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) 
   lo = tf32_rn_bits(x - __uint_as_float(hi));
 }
 
+// The 12 MMAs of chunk c (k-block kc = c / HALVES, row block h = c % HALVES).
+// With c a compile-time constant every chain index and accumulate flag below
+// folds to a constant, which keeps the single issuing thread off integer
+// dependency chains between MMAs.
+template <int K>
+__device__ __forceinline__ void mma_chunk(const int c, uint32_t tmem, uint32_t a_hi, uint64_t dh0, uint64_t dl0) {
+  using C = Cfg<K>;
+  constexpr uint32_t idesc = idesc_tf32(128, VT);
+  const int kc = c / C::HALVES, h = c % C::HALVES;
+  const int q0 = h * (C::NB + C::NS);
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int ks = kc * 4 + s;  // k-step within the row block: B rows [8 ks, 8 ks + 8)
+    const int qb = q0 + ks % C::NB;
+    const int q1 = q0 + C::NB + ks % C::NS;
+    const int q2 = q0 + C::NB + (ks + C::NS / 2) % C::NS;
+    // a chain's first MMA of the step overwrites, later ones accumulate
+    const uint32_t acc_b = ks >= C::NB;
+    const uint32_t acc_1 = ks >= C::NS || (ks % C::NS) >= C::NS / 2;
+    const uint32_t acc_2 = ks >= C::NS / 2;
+    const uint64_t off = (uint64_t)(((uint32_t)kc * (VT * 128) + (uint32_t)s * 32) >> 4);
+    mma_tf32_ts(tmem + qb * VT, a_hi + s * 8, dh0 + off, idesc, acc_b);
+    mma_tf32_ts(tmem + q1 * VT, a_hi + s * 8, dl0 + off, idesc, acc_1);
+    mma_tf32_ts(tmem + q2 * VT, a_hi + 32 + s * 8, dh0 + off, idesc, acc_2);
+  }
+}
+
 template <int K>
 __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_constant__ TcParams p) {
   using C = Cfg<K>;
@@ -288,42 +315,28 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       constexpr uint32_t idesc = idesc_tf32(128, VT);
       const uint32_t bhi = smem_u32(smem + C::OFF_BHI);
       const uint32_t blo = smem_u32(smem + C::OFF_BLO);
+      // Descriptors of the k-block 0 rows of B hi / lo; every other k-step
+      // adds a compile-time byte offset (>> 4) to the start-address field.
+      const uint64_t dh0 = smem_desc_sw128(bhi, 1024);
+      const uint64_t dl0 = smem_desc_sw128(blo, 1024);
       uint32_t ait = 0;
       bool ok = true;
       for (int step = 0; step < nsteps && ok; ++step) {
         if (!(ok = mbar_wait(&ctl->x_ready, step & 1, wc))) break;
         QLA_TR(1, step, 0, 0);
         tc_fence_after();
-        uint32_t written = 0;  // chains already holding a value this step
-        for (int c = 0; c < C::CPS; ++c, ++ait) {
-          const int kc = c / C::HALVES, h = c % C::HALVES;
-          const int slot = ait % NA;
-          if (!(ok = mbar_wait(&ctl->a_full[slot], (ait / NA) & 1, wc))) break;
+#pragma unroll
+        for (int c = 0; c < C::CPS; ++c) {
+          const int slot = (ait + c) % NA;
+          if (!(ok = mbar_wait(&ctl->a_full[slot], ((ait + c) / NA) & 1, wc))) break;
           QLA_TR(1, step, 1, c);
           tc_fence_after();
           const uint32_t a_hi = tmem + kACol + slot * 64;
-          const uint32_t a_lo = a_hi + 32;
-          const int q0 = h * (C::NB + C::NS);
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            const int ks = kc * 4 + s;
-            const int qb = q0 + ks % C::NB;
-            const int q1 = q0 + C::NB + ks % C::NS;
-            const int q2 = q0 + C::NB + (ks + C::NS / 2) % C::NS;
-            // B rows k in [32kc + 8s, +8): k-block kc, 32 bytes per 8 tf32 inside the swizzled row
-            const uint32_t off = (uint32_t)kc * (VT * 128) + (uint32_t)s * 32;
-            const uint64_t dh = smem_desc_sw128(bhi + off, 1024);
-            const uint64_t dl = smem_desc_sw128(blo + off, 1024);
-            mma_tf32_ts(tmem + qb * VT, a_hi + s * 8, dh, idesc, (written >> qb) & 1);
-            written |= 1u << qb;
-            mma_tf32_ts(tmem + q1 * VT, a_hi + s * 8, dl, idesc, (written >> q1) & 1);
-            written |= 1u << q1;
-            mma_tf32_ts(tmem + q2 * VT, a_lo + s * 8, dh, idesc, (written >> q2) & 1);
-            written |= 1u << q2;
-          }
+          mma_chunk<K>(c, tmem, a_hi, dh0, dl0);
           mma_commit(&ctl->a_empty[slot]);
           QLA_TR(1, step, 3, c);
         }
+        ait += C::CPS;
         if (ok) mma_commit(&ctl->d_full);
       }
       // All MMAs this thread issued must finish before TMEM is freed.
@@ -458,12 +471,15 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
 #pragma unroll
       for (int h = 0; h < C::HALVES; ++h) {
         const int k = t + 128 * h;
-        const uint32_t base = (uint32_t)(k >> 5) * (VT * 128) + (uint32_t)(k & 3) * 4;
-        const int piece = (k & 31) >> 2;
+        // byte offset of (n = c, k): kblock(k) + (c/8)*1024 + (c%8)*128 + ((piece ^ (c%8)) << 4) + (k%4)*4
+        const uint32_t kb = (uint32_t)(k >> 5) * (VT * 128) + (uint32_t)(k & 3) * 4;
+        const uint32_t piece = (uint32_t)((k & 31) >> 2);
+        uint32_t rowoff[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) rowoff[m] = kb + (uint32_t)m * 128 + ((piece ^ (uint32_t)m) << 4);
 #pragma unroll
         for (int c = 0; c < VT; ++c) {
-          const uint32_t off = base + (uint32_t)(c >> 3) * 1024 + (uint32_t)(c & 7) * 128 +
-                               (uint32_t)((piece ^ (c & 7)) << 4);
+          const uint32_t off = rowoff[c & 7] + (uint32_t)(c >> 3) * 1024;
           uint32_t hb, lb;
           split_tf32(y[h][c], hb, lb);
           *reinterpret_cast<uint32_t*>(bhi + off) = hb;
@@ -473,37 +489,18 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       fence_proxy_async_smem();  // generic writes -> read by tcgen05.mma (async proxy)
     };
 
-    // Sum of the accumulator chains of one 128-row block: pairwise, round-to-nearest.
-    auto drain = [&](int h, float (&acc)[VT]) {
+    // acc += the accumulator chains of one 128-row block, in pairs, round-to-nearest.
+    auto drain_add = [&](int h, float (&acc)[VT]) {
       float a[32], b[32];
       const uint32_t base = tmem + lane_off + (uint32_t)(h * (C::NB + C::NS) * VT);
-      tmem_ld32(base + 0 * VT, a);
-      tmem_ld32(base + 1 * VT, b);
-      tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < VT; ++c) acc[c] = a[c] + b[c];
-      if (C::NB == 4) {
-        tmem_ld32(base + 2 * VT, a);
-        tmem_ld32(base + 3 * VT, b);
+      for (int q = 0; q < C::NB + C::NS; q += 2) {  // big pairs first, then small pairs
+        tmem_ld32(base + q * VT, a);
+        tmem_ld32(base + (q + 1) * VT, b);
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < VT; ++c) acc[c] += a[c] + b[c];
       }
-      float sm[VT];
-      tmem_ld32(base + (C::NB + 0) * VT, a);
-      tmem_ld32(base + (C::NB + 1) * VT, b);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < VT; ++c) sm[c] = a[c] + b[c];
-      if (C::NS == 4) {
-        tmem_ld32(base + (C::NB + 2) * VT, a);
-        tmem_ld32(base + (C::NB + 3) * VT, b);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < VT; ++c) sm[c] += a[c] + b[c];
-      }
-#pragma unroll
-      for (int c = 0; c < VT; ++c) acc[c] += sm[c];
     };
 
     if (nsteps > 0) {  // X_0 -> B operand first: the first step's MMAs wait on it
@@ -516,12 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       if (ok) store_out(seg_of(0));
     }
     for (int step = 0; step < nsteps && ok; ++step) {
-      uint64_t* dbar = (p.stall_test && step == 0) ? &ctl->never : &ctl->d_full;
-      if (!(ok = warp_wait(dbar, step & 1, wc))) break;
-      QLA_TR(3, step, 1, 0);
-      tc_fence_after();
-#pragma unroll
-      for (int h = 0; h < C::HALVES; ++h) drain(h, y[h]);
+      // H_j into the accumulator registers first: it does not depend on the MMAs
       const int slot = step & 1;
       if (p.has_h) {
         if (!(ok = warp_wait(&ctl->h_full[slot], (step >> 1) & 1, wc))) break;
@@ -535,15 +527,31 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               const float4 v = *reinterpret_cast<const float4*>(row + ((q ^ (k & 7)) << 4));
-              y[h][4 * q] += v.x; y[h][4 * q + 1] += v.y; y[h][4 * q + 2] += v.z; y[h][4 * q + 3] += v.w;
+              y[h][4 * q] = v.x; y[h][4 * q + 1] = v.y; y[h][4 * q + 2] = v.z; y[h][4 * q + 3] = v.w;
             }
           } else {              // [VT rows][K floats]
             const float* f = reinterpret_cast<const float*>(ht) + k;
 #pragma unroll
-            for (int c = 0; c < VT; ++c) y[h][c] += f[c * K];
+            for (int c = 0; c < VT; ++c) y[h][c] = f[c * K];
           }
         }
+        if (p.release != 2) {  // the h slot's last ordinary read is done: release it
+          release_fence(p.release);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->h_empty[slot]);
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < C::HALVES; ++h)
+#pragma unroll
+          for (int c = 0; c < VT; ++c) y[h][c] = 0.f;
       }
+      uint64_t* dbar = (p.stall_test && step == 0) ? &ctl->never : &ctl->d_full;
+      if (!(ok = warp_wait(dbar, step & 1, wc))) break;
+      QLA_TR(3, step, 1, 0);
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < C::HALVES; ++h) drain_add(h, y[h]);
       if (step + 1 < nsteps) {  // X_{j+1} -> B operand: the critical path to the next step
         write_b();
         tc_fence_before();  // the chains have been read (wait::ld in drain)
@@ -565,11 +573,6 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
             for (int c = 0; c < VT; ++c) F[(int64_t)(v0 + c) * K + k] = y[h][c];
           }
         }
-      }
-      if (p.has_h && p.release != 2) {  // the h slot's last ordinary read is done: release it
-        release_fence(p.release);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->h_empty[slot]);
       }
       if (step + 1 < n && j.out) {
         if (p.in_place && p.has_h && step + 1 < nsteps)
