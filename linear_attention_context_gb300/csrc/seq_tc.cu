@@ -20,16 +20,18 @@
 //
 // Accumulation: the tensor core also rounds its fp32 accumulator toward zero,
 // so a long chain of MMAs into one accumulator shrinks the result coherently
-// (measured about -6e-7 per step with 48 MMAs per output).  And an MMA that
-// accumulates into the result of the one just issued waits for it: with
-// N = 32 such a dependent chain runs at about 120 cycles per MMA instead of
-// the tensor pipe's ~16.  Both are solved by spreading the k reduction over
-// independent accumulators: per 128-row block, NB "big" chains take A_hi X_hi
-// of k-steps ks = r (mod NB) and NS "small" chains take the A_hi X_lo and
-// A_lo X_hi terms, so no chain sees more than 4 big MMAs per step and
-// dependent MMAs are at least 6 issues apart.  The epilogue adds the chains
-// pairwise with round-to-nearest fp32 adds.
-
+// (measured about -6e-7 per step with 48 MMAs per output).  The big A_hi X_hi
+// terms are therefore spread over NB chains by k-step (no chain sees more than
+// 4 big MMAs per step); the two small terms, 2^-11 of the result, take one
+// chain each.  The epilogue adds the chains in pairs with round-to-nearest
+// fp32 adds.
+//
+// Issue rate: one thread issues a tcgen05.mma about every 45 cycles, while
+// an M=128, N=32, K=8 tf32 MMA keeps the tensor pipe busy for about 17, so
+// three threads issue: one the big terms, one A_hi X_lo, one A_lo X_hi, each
+// into its own accumulators (no two threads ever accumulate into the same
+// TMEM columns).
+//
 // One CTA owns a VT-column tile of one unit (chain, group) for all of the
 // unit's segments.  Roles, storage, handoff and lifetime (the table the
 // mlc.ai page "调试 Warp-Specialized Kernels", section "先写清楚数据如何交接",
@@ -38,21 +40,22 @@
 //  role      warps    does
 //  producer  0 (1 th) TMA: H_j tile -> h slot j&1; A_j in 32-column chunks
 //                     -> m ring (NM stages).  Needs no state: runs ahead.
-//  mma       1 (1 th) tcgen05.mma kind::tf32, A from TMEM, B (= X_j hi/lo,
-//                     K-major, 128-byte swizzle) from shared memory, into the
-//                     NB + NS accumulator chains per 128-row block (TMEM).
-//  splitter  4..7     m chunk (ordinary shared loads) -> hi/lo -> TMEM A ring
-//                     (NA slots of 64 columns).
-//  epilogue  8..11    H_j (ordinary shared loads, then the h-slot release)
-//                     + the chains (tcgen05.ld) = X_{j+1}; its hi/lo -> B
-//                     operand first (the next step waits on it), then out
-//                     via per-warp TMA stores.
+//  mma       1, 2, 3  (1 thread each) tcgen05.mma kind::tf32, A from TMEM,
+//                     B (= X_j hi/lo, K-major, 128-byte swizzle) from shared
+//                     memory, D in the accumulator chains (TMEM).
+//  splitter  4..11    two warpgroups, alternate chunks: m chunk (ordinary
+//                     shared loads) -> hi/lo -> TMEM A ring (NA slots).
+//  epilogue  12..19   two warpgroups, 16 columns each: H_j (ordinary shared
+//                     loads, then the h-slot release) + the chains
+//                     (tcgen05.ld) = X_{j+1}; its hi/lo -> B operand first
+//                     (the next step waits on it), then out via per-warp
+//                     TMA stores.
 //
 //  storage        written by           read by             reusable after
 //  m ring [s]     TMA (async)          splitter (generic)  splitter's last read: fence + m_empty arrive
 //  h slot [j&1]   TMA (async)          epilogue (generic)  epilogue's last read: fence + h_empty arrive
-//  A ring (TMEM)  splitter tcgen05.st  mma (async)         mma commit -> a_empty
-//  B hi/lo        epilogue st.shared   mma (async)         d_full (all MMAs of the step done)
+//  A ring (TMEM)  splitter tcgen05.st  mma (async)         3 commits -> a_empty
+//  B hi/lo        epilogue st.shared   mma (async)         d_full (3 commits: all MMAs of the step done)
 //                 + fence.proxy.async
 //  chains (TMEM)  mma                  epilogue tcgen05.ld x_ready (epilogue's wait::ld done)
 //  out staging    epilogue st.shared   TMA store (async)   bulk wait_group.read
@@ -60,9 +63,10 @@
 //
 // Chunks go kc-major: chunk c = kc * HALVES + h is A[128h.., 32kc..], so the
 // two row blocks of K = 256 interleave.  Barriers: m_full/h_full count 1 +
-// transaction bytes; m_empty, h_empty, a_full, x_ready count 4 (one arrive per
-// warp after __syncwarp); a_empty, d_full count 1 (tcgen05.commit).  Producers wait their empty barriers with
-// the parity of (use / slots) ^ 1, consumers their full barriers with
+// transaction bytes; m_empty, a_full count 4 (the splitter warpgroup's warps);
+// h_empty, x_ready count 8 (the epilogue warps); a_empty, d_full count 3 (one
+// tcgen05.commit per issuing thread).  Producers wait their empty barriers
+// with the parity of (use / slots) ^ 1, consumers their full barriers with
 // (use / slots), so the first producer wait passes at once.
 //
 // The slot-release fence (the page's section "三个可用源码方案的具体差别") is
@@ -89,8 +93,8 @@
 // [role][step][event][chunk]; roles 0 producer, 1 mma, 2 splitter, 3 epilogue.
 #ifdef QLA_TRACE
 __device__ long long g_qla_trace[4 * 8 * 8 * 16];
-#define QLA_TR(role, step, ev, ch)                                                         \
-  do {                                                                                   \
+#define QLA_TR(role, step, ev, ch)                                                                        \
+  do {                                                                                                    \
     if (tr && (step) < 8 && (ch) < 16) g_qla_trace[(((role) * 8 + (step)) * 8 + (ev)) * 16 + (ch)] = clock64(); \
   } while (0)
 #else
@@ -104,23 +108,23 @@ namespace {
 
 using namespace ptx;
 
-constexpr int VT = 32;            // state columns per CTA
-constexpr int kThreads = 384;     // 12 warps
+constexpr int VT = 32;                          // state columns per CTA
+constexpr int EC = 16;                          // state columns per epilogue warpgroup
+constexpr int kThreads = 640;                   // 20 warps
 constexpr uint32_t kChunkBytes = 128 * 32 * 4;  // one A chunk: 128 rows x 32 columns fp32
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kACol = 256;   // accumulator chains in [0, 256); A ring: NA slots of 64 columns (hi, lo)
-constexpr int NA = 4;
 
 template <int K>
 struct Cfg {
-  static constexpr int HALVES = K / 128;           // 128-row MMA blocks of the output
-  static constexpr int KCH = K / 32;               // 32-wide k chunks per block
-  static constexpr int CPS = HALVES * KCH;         // chunks per step
-  static constexpr int NM = K == 128 ? 6 : 4;      // m ring stages
-  static constexpr int NOUT = K == 128 ? 2 : 1;    // out staging buffers
-  static constexpr int NB = K == 128 ? 4 : 2;      // big-term chains per 128-row block
-  static constexpr int NS = K == 128 ? 4 : 2;      // small-term chains per 128-row block
-  static_assert(HALVES * (NB + NS) * VT <= (int)kACol, "accumulator columns");
+  static constexpr int HALVES = K / 128;          // 128-row MMA blocks of the output
+  static constexpr int KCH = K / 32;              // 32-wide k chunks per block
+  static constexpr int CPS = HALVES * KCH;        // chunks per step
+  static constexpr int NB = K == 128 ? 4 : 2;     // big-term chains per row block
+  static constexpr int NQ = NB + 2;               // chains per row block (+ A_hi X_lo, A_lo X_hi)
+  static constexpr uint32_t ACOL = HALVES * NQ * VT;  // first column of the A ring
+  static constexpr int NA = (int)((kTmemCols - ACOL) / 64);  // A ring slots (hi, lo: 64 columns)
+  static constexpr int NM = K == 128 ? 6 : 4;     // m ring stages
+  static constexpr int NOUT = K == 128 ? 2 : 1;   // out staging buffers
   static constexpr uint32_t TILE = (uint32_t)K * VT * 4;  // one state tile (bytes)
   static constexpr uint32_t OFF_M = 0;
   static constexpr uint32_t OFF_H = OFF_M + NM * kChunkBytes;
@@ -131,6 +135,7 @@ struct Cfg {
   static constexpr uint32_t CTRL_BYTES = 512;
   static constexpr uint32_t SMEM = OFF_CTRL + CTRL_BYTES + 1024;  // + alignment slack
   static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(NA >= 2 && NA <= 6, "A ring");
 };
 
 struct TcParams {
@@ -148,9 +153,10 @@ struct TcParams {
 
 struct Ctrl {
   uint64_t m_full[6], m_empty[6];
-  uint64_t a_full[NA], a_empty[NA];
+  uint64_t a_full[6], a_empty[6];
   uint64_t h_full[2], h_empty[2];
-  uint64_t x_ready, d_full, never, mma_done;
+  uint64_t x_ready, d_full, never;
+  uint64_t mma_done[3];
   uint32_t tmem_base;
   int abort;
 };
@@ -177,31 +183,69 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) 
   lo = tf32_rn_bits(x - __uint_as_float(hi));
 }
 
-// The 12 MMAs of chunk c (k-block kc = c / HALVES, row block h = c % HALVES).
-// With c a compile-time constant every chain index and accumulate flag below
-// folds to a constant, which keeps the single issuing thread off integer
-// dependency chains between MMAs.
-template <int K>
+// The MMAs one issuing thread owes chunk c (k-block kc = c / HALVES, row
+// block h = c % HALVES): role 0 the four A_hi X_hi k-steps, role 1 the A_hi X_lo
+// ones, role 2 the A_lo X_hi ones.  With c and the role compile-time
+// constants every chain index and accumulate flag folds to a constant.
+template <int K, int ROLE>
 __device__ __forceinline__ void mma_chunk(const int c, uint32_t tmem, uint32_t a_hi, uint64_t dh0, uint64_t dl0) {
   using C = Cfg<K>;
   constexpr uint32_t idesc = idesc_tf32(128, VT);
   const int kc = c / C::HALVES, h = c % C::HALVES;
-  const int q0 = h * (C::NB + C::NS);
+  const int q0 = h * C::NQ;
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const int ks = kc * 4 + s;  // k-step within the row block: B rows [8 ks, 8 ks + 8)
-    const int qb = q0 + ks % C::NB;
-    const int q1 = q0 + C::NB + ks % C::NS;
-    const int q2 = q0 + C::NB + (ks + C::NS / 2) % C::NS;
-    // a chain's first MMA of the step overwrites, later ones accumulate
-    const uint32_t acc_b = ks >= C::NB;
-    const uint32_t acc_1 = ks >= C::NS || (ks % C::NS) >= C::NS / 2;
-    const uint32_t acc_2 = ks >= C::NS / 2;
+    // B rows of k-step ks: k-block kc, 32 bytes per 8 tf32 inside the swizzled row
     const uint64_t off = (uint64_t)(((uint32_t)kc * (VT * 128) + (uint32_t)s * 32) >> 4);
-    mma_tf32_ts(tmem + qb * VT, a_hi + s * 8, dh0 + off, idesc, acc_b);
-    mma_tf32_ts(tmem + q1 * VT, a_hi + s * 8, dl0 + off, idesc, acc_1);
-    mma_tf32_ts(tmem + q2 * VT, a_hi + 32 + s * 8, dh0 + off, idesc, acc_2);
+    if (ROLE == 0)
+      mma_tf32_ts(tmem + (q0 + ks % C::NB) * VT, a_hi + s * 8, dh0 + off, idesc, ks >= C::NB);
+    else if (ROLE == 1)
+      mma_tf32_ts(tmem + (q0 + C::NB) * VT, a_hi + s * 8, dl0 + off, idesc, ks > 0);
+    else
+      mma_tf32_ts(tmem + (q0 + C::NB + 1) * VT, a_hi + 32 + s * 8, dh0 + off, idesc, ks > 0);
   }
+}
+
+template <int K, int ROLE>
+__device__ __forceinline__ void mma_role(const SeqJob& j, Ctrl* ctl, uint8_t* smem, uint32_t tmem, int nsteps,
+                                         const WaitCtl& wc
+#ifdef QLA_TRACE
+                                         ,
+                                         bool tr
+#endif
+) {
+  using C = Cfg<K>;
+  (void)j;
+  // Descriptors of the k-block 0 rows of B hi / lo; every other k-step adds a
+  // compile-time byte offset (>> 4) to the start-address field.
+  const uint64_t dh0 = smem_desc_sw128(smem_u32(smem + C::OFF_BHI), 1024);
+  const uint64_t dl0 = smem_desc_sw128(smem_u32(smem + C::OFF_BLO), 1024);
+  int slot = 0;
+  uint32_t phase = 0;
+  bool ok = true;
+  for (int step = 0; step < nsteps && ok; ++step) {
+    if (!(ok = mbar_wait(&ctl->x_ready, step & 1, wc))) break;
+    if (ROLE == 0) QLA_TR(1, step, 0, 0);
+    tc_fence_after();
+#pragma unroll
+    for (int c = 0; c < C::CPS; ++c) {
+      if (!(ok = mbar_wait(&ctl->a_full[slot], phase, wc))) break;
+      if (ROLE == 0) QLA_TR(1, step, 1, c);
+      tc_fence_after();
+      mma_chunk<K, ROLE>(c, tmem, tmem + C::ACOL + slot * 64, dh0, dl0);
+      mma_commit(&ctl->a_empty[slot]);
+      if (ROLE == 0) QLA_TR(1, step, 3, c);
+      if (++slot == C::NA) {
+        slot = 0;
+        phase ^= 1;
+      }
+    }
+    if (ok) mma_commit(&ctl->d_full);
+  }
+  // All MMAs this thread issued must finish before TMEM is freed.
+  mma_commit(&ctl->mma_done[ROLE]);
+  mbar_wait_drain(&ctl->mma_done[ROLE], 0, 200000000ull);
 }
 
 template <int K>
@@ -225,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
   auto seg_of = [&](int step) { return fwd ? s_lo + step : s_lo + n - 1 - step; };
 #ifdef QLA_TRACE
   const bool tr = blockIdx.x == 0 && blockIdx.y == 0 &&
-                  (threadIdx.x == 0 || threadIdx.x == 32 || threadIdx.x == 128 || threadIdx.x == 256);
+                  (threadIdx.x == 0 || threadIdx.x == 32 || threadIdx.x == 128 || threadIdx.x == 384);
 #endif
 
   if (threadIdx.x == 0) {
@@ -233,18 +277,18 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       mbar_init(&ctl->m_full[i], 1);
       mbar_init(&ctl->m_empty[i], 4);
     }
-    for (int i = 0; i < NA; ++i) {
+    for (int i = 0; i < C::NA; ++i) {
       mbar_init(&ctl->a_full[i], 4);
-      mbar_init(&ctl->a_empty[i], 1);
+      mbar_init(&ctl->a_empty[i], 3);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->h_full[i], 1);
-      mbar_init(&ctl->h_empty[i], 4);
+      mbar_init(&ctl->h_empty[i], 8);
     }
-    mbar_init(&ctl->x_ready, 4);
-    mbar_init(&ctl->d_full, 1);
+    mbar_init(&ctl->x_ready, 8);
+    mbar_init(&ctl->d_full, 3);
     mbar_init(&ctl->never, 1);
-    mbar_init(&ctl->mma_done, 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&ctl->mma_done[i], 1);
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -309,101 +353,95 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ mma issuer
+  } else if (warp <= 3) {
+    // ------------------------------------------------------------ mma issuers
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_tf32(128, VT);
-      const uint32_t bhi = smem_u32(smem + C::OFF_BHI);
-      const uint32_t blo = smem_u32(smem + C::OFF_BLO);
-      // Descriptors of the k-block 0 rows of B hi / lo; every other k-step
-      // adds a compile-time byte offset (>> 4) to the start-address field.
-      const uint64_t dh0 = smem_desc_sw128(bhi, 1024);
-      const uint64_t dl0 = smem_desc_sw128(blo, 1024);
-      uint32_t ait = 0;
-      bool ok = true;
-      for (int step = 0; step < nsteps && ok; ++step) {
-        if (!(ok = mbar_wait(&ctl->x_ready, step & 1, wc))) break;
-        QLA_TR(1, step, 0, 0);
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < C::CPS; ++c) {
-          const int slot = (ait + c) % NA;
-          if (!(ok = mbar_wait(&ctl->a_full[slot], ((ait + c) / NA) & 1, wc))) break;
-          QLA_TR(1, step, 1, c);
-          tc_fence_after();
-          const uint32_t a_hi = tmem + kACol + slot * 64;
-          mma_chunk<K>(c, tmem, a_hi, dh0, dl0);
-          mma_commit(&ctl->a_empty[slot]);
-          QLA_TR(1, step, 3, c);
-        }
-        ait += C::CPS;
-        if (ok) mma_commit(&ctl->d_full);
-      }
-      // All MMAs this thread issued must finish before TMEM is freed.
-      mma_commit(&ctl->mma_done);
-      mbar_wait_drain(&ctl->mma_done, 0, 200000000ull);
+#ifdef QLA_TRACE
+      if (warp == 1) mma_role<K, 0>(j, ctl, smem, tmem, nsteps, wc, tr);
+      else if (warp == 2) mma_role<K, 1>(j, ctl, smem, tmem, nsteps, wc, tr);
+      else mma_role<K, 2>(j, ctl, smem, tmem, nsteps, wc, tr);
+#else
+      if (warp == 1) mma_role<K, 0>(j, ctl, smem, tmem, nsteps, wc);
+      else if (warp == 2) mma_role<K, 1>(j, ctl, smem, tmem, nsteps, wc);
+      else mma_role<K, 2>(j, ctl, smem, tmem, nsteps, wc);
+#endif
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------ A splitter
-    const int t = threadIdx.x - 128;                 // A row within the 128-row block = TMEM lane
+  } else if (warp < 12) {
+    // ------------------------------------------------------------ A splitters
+    const int grp = (warp - 4) >> 2;                 // takes chunks grp, grp + 2, grp + 4, ...
+    const int t = 32 * (warp & 3) + lane;            // A row within the 128-row block = TMEM lane
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-    uint32_t mit = 0;
+    const int total = nsteps * C::CPS;
+    int stage = grp, aslot = grp;
+    uint32_t mphase = 0, aphase = 0;
     bool ok = true;
-    for (int step = 0; step < nsteps && ok; ++step) {
-      for (int c = 0; c < C::CPS; ++c, ++mit) {
-        const int stage = mit % C::NM;
-        if (!(ok = warp_wait(&ctl->m_full[stage], (mit / C::NM) & 1, wc))) break;
-        QLA_TR(2, step, 0, c);
-        const uint8_t* chunk = smem + C::OFF_M + stage * kChunkBytes;
-        float x[32];
-        if (fwd) {  // row t of a [128][32] tile, 16-byte pieces swizzled by (t & 7)
-          const uint8_t* row = chunk + t * 128;
+    for (int mit = grp; mit < total && ok; mit += 2) {
+      const int step = mit / C::CPS, c = mit % C::CPS;
+      (void)step;
+      (void)c;
+      if (!(ok = warp_wait(&ctl->m_full[stage], mphase, wc))) break;
+      QLA_TR(2, step, 0, c);
+      const uint8_t* chunk = smem + C::OFF_M + stage * kChunkBytes;
+      float x[32];
+      if (fwd) {  // row t of a [128][32] tile, 16-byte pieces swizzled by (t & 7)
+        const uint8_t* row = chunk + t * 128;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 v = *reinterpret_cast<const float4*>(row + ((q ^ (t & 7)) << 4));
-            x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
-          }
-        } else {    // column t of a [32][128] tile
-          const float* col = reinterpret_cast<const float*>(chunk) + t;
-#pragma unroll
-          for (int k = 0; k < 32; ++k) x[k] = col[k * 128];
+        for (int q = 0; q < 8; ++q) {
+          const float4 v = *reinterpret_cast<const float4*>(row + ((q ^ (t & 7)) << 4));
+          x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
         }
-        if (p.release != 2) {  // the slot's last ordinary read is done: release it
-          release_fence(p.release);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl->m_empty[stage]);
-        }
-        uint32_t hi[32], lo[32];
+      } else {    // column t of a [32][128] tile
+        const float* col = reinterpret_cast<const float*>(chunk) + t;
 #pragma unroll
-        for (int k = 0; k < 32; ++k) split_tf32(x[k], hi[k], lo[k]);
-        const int slot = mit % NA;
-        if (!(ok = warp_wait(&ctl->a_empty[slot], ((mit / NA) & 1) ^ 1, wc))) break;
-        QLA_TR(2, step, 1, c);
-        tc_fence_after();
-        const uint32_t a = tmem + lane_off + kACol + slot * 64;
-        tmem_st32(a, hi);
-        tmem_st32(a + 32, lo);
-        tmem_wait_st();
-        tc_fence_before();
+        for (int k = 0; k < 32; ++k) x[k] = col[k * 128];
+      }
+      if (p.release != 2) {  // the slot's last ordinary read is done: release it
+        release_fence(p.release);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->a_full[slot]);
-        QLA_TR(2, step, 2, c);
-        if (p.release == 2) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl->m_empty[stage]);
-        }
+        if (lane == 0) mbar_arrive(&ctl->m_empty[stage]);
+      }
+      if (!(ok = warp_wait(&ctl->a_empty[aslot], aphase ^ 1, wc))) break;
+      QLA_TR(2, step, 1, c);
+      tc_fence_after();
+      const uint32_t a = tmem + lane_off + C::ACOL + aslot * 64;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) split_tf32(x[16 * half + k], hi[k], lo[k]);
+        tmem_st16(a + 16 * half, hi);
+        tmem_st16(a + 32 + 16 * half, lo);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->a_full[aslot]);
+      QLA_TR(2, step, 2, c);
+      if (p.release == 2) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->m_empty[stage]);
+      }
+      if ((stage += 2) >= C::NM) {
+        stage -= C::NM;
+        mphase ^= 1;
+      }
+      if ((aslot += 2) >= C::NA) {
+        aslot -= C::NA;
+        aphase ^= 1;
       }
     }
-  } else if (warp >= 8) {
+  } else {
     // ------------------------------------------------------------ epilogue
-    const int t = threadIdx.x - 256;                 // output row within a 128-row block = TMEM lane
+    const int e = (warp - 12) >> 2;                  // column half: columns [16e, 16e + 16) of the tile
     const int wq = warp & 3;
+    const int t = 32 * wq + lane;                    // output row within a 128-row block = TMEM lane
     const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
     const int V = j.V;
+    const int c0 = e * EC;
     uint8_t* bhi = smem + C::OFF_BHI;
     uint8_t* blo = smem + C::OFF_BLO;
-    float y[C::HALVES][VT];
+    float y[C::HALVES][EC];
     int out_count = 0;
     bool ok = true;
 
@@ -415,38 +453,36 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
         const float* src = j.init + u * j.init_unit_stride;
         if (j.layout == 0) {
 #pragma unroll
-          for (int q = 0; q < VT / 4; ++q) {
-            const float4 v = *reinterpret_cast<const float4*>(src + (int64_t)k * V + v0 + 4 * q);
+          for (int q = 0; q < EC / 4; ++q) {
+            const float4 v = *reinterpret_cast<const float4*>(src + (int64_t)k * V + v0 + c0 + 4 * q);
             y[h][4 * q] = v.x; y[h][4 * q + 1] = v.y; y[h][4 * q + 2] = v.z; y[h][4 * q + 3] = v.w;
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < VT; ++c) y[h][c] = src[(int64_t)(v0 + c) * K + k];
+          for (int c = 0; c < EC; ++c) y[h][c] = src[(int64_t)(v0 + c0 + c) * K + k];
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < VT; ++c) y[h][c] = (j.init_mode == kInitIdentity && k == v0 + c) ? 1.f : 0.f;
+        for (int c = 0; c < EC; ++c) y[h][c] = (j.init_mode == kInitIdentity && k == v0 + c0 + c) ? 1.f : 0.f;
       }
     }
 
-    // out[seg] <- y through per-warp staging and TMA stores
+    // out[seg] <- y through per-warp staging (2 KB per row block) and TMA stores
     auto store_out = [&](int seg) {
       const int b = out_count % C::NOUT;
       if (lane == 0) bulk_wait_read<C::NOUT - 1>();
       __syncwarp();
 #pragma unroll
       for (int h = 0; h < C::HALVES; ++h) {
-        uint8_t* stg = smem + C::OFF_OUT + b * C::TILE + (h * 4 + wq) * 4096;
-        if (j.layout == 0) {  // [32 rows][32 floats], 128-byte swizzle: this lane's row
-          uint8_t* row = stg + lane * 128;
+        float* stg = reinterpret_cast<float*>(smem + C::OFF_OUT + b * C::TILE + ((h * 2 + e) * 4 + wq) * 2048);
+        if (j.layout == 0) {  // [32 rows][16 floats]: this lane's row
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(row + ((q ^ (lane & 7)) << 4)) =
+          for (int q = 0; q < EC / 4; ++q)
+            *reinterpret_cast<float4*>(stg + lane * EC + 4 * q) =
                 make_float4(y[h][4 * q], y[h][4 * q + 1], y[h][4 * q + 2], y[h][4 * q + 3]);
-        } else {              // [VT rows][32 floats]: column `lane`
-          float* f = reinterpret_cast<float*>(stg);
+        } else {              // [16 rows][32 floats]: column `lane`
 #pragma unroll
-          for (int c = 0; c < VT; ++c) f[c * 32 + lane] = y[h][c];
+          for (int c = 0; c < EC; ++c) stg[c * 32 + lane] = y[h][c];
         }
       }
       fence_proxy_async_smem();
@@ -454,11 +490,12 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       if (lane == 0) {
 #pragma unroll
         for (int h = 0; h < C::HALVES; ++h) {
-          const uint8_t* stg = smem + C::OFF_OUT + b * C::TILE + (h * 4 + wq) * 4096;
+          const uint8_t* stg = smem + C::OFF_OUT + b * C::TILE + ((h * 2 + e) * 4 + wq) * 2048;
           if (j.layout == 0)
-            tma_store_2d(&p.map_out, stg, v0, (int32_t)(((int64_t)chain * j.S + seg) * K + 128 * h + 32 * wq));
+            tma_store_2d(&p.map_out, stg, v0 + c0,
+                         (int32_t)(((int64_t)chain * j.S + seg) * K + 128 * h + 32 * wq));
           else
-            tma_store_2d(&p.map_out, stg, 128 * h + 32 * wq, (int32_t)(((int64_t)chain * j.S + seg) * V + v0));
+            tma_store_2d(&p.map_out, stg, 128 * h + 32 * wq, (int32_t)(((int64_t)chain * j.S + seg) * V + v0 + c0));
         }
         bulk_commit();
       }
@@ -471,14 +508,13 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
 #pragma unroll
       for (int h = 0; h < C::HALVES; ++h) {
         const int k = t + 128 * h;
-        // byte offset of (n = c, k): kblock(k) + (c/8)*1024 + (c%8)*128 + ((piece ^ (c%8)) << 4) + (k%4)*4
-        const uint32_t kb = (uint32_t)(k >> 5) * (VT * 128) + (uint32_t)(k & 3) * 4;
+        const uint32_t kb = (uint32_t)(k >> 5) * (VT * 128) + (uint32_t)(k & 3) * 4 + (uint32_t)(c0 >> 3) * 1024;
         const uint32_t piece = (uint32_t)((k & 31) >> 2);
         uint32_t rowoff[8];
 #pragma unroll
         for (int m = 0; m < 8; ++m) rowoff[m] = kb + (uint32_t)m * 128 + ((piece ^ (uint32_t)m) << 4);
 #pragma unroll
-        for (int c = 0; c < VT; ++c) {
+        for (int c = 0; c < EC; ++c) {  // n = c0 + c; c0 is a multiple of 8
           const uint32_t off = rowoff[c & 7] + (uint32_t)(c >> 3) * 1024;
           uint32_t hb, lb;
           split_tf32(y[h][c], hb, lb);
@@ -489,17 +525,18 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       fence_proxy_async_smem();  // generic writes -> read by tcgen05.mma (async proxy)
     };
 
-    // acc += the accumulator chains of one 128-row block, in pairs, round-to-nearest.
-    auto drain_add = [&](int h, float (&acc)[VT]) {
-      float a[32], b[32];
-      const uint32_t base = tmem + lane_off + (uint32_t)(h * (C::NB + C::NS) * VT);
+    // acc += the accumulator chains of one 128-row block (this warpgroup's 16
+    // columns), in pairs, round-to-nearest: big chains first, then the small.
+    auto drain_add = [&](int h, float (&acc)[EC]) {
+      float a[16], b[16];
+      const uint32_t base = tmem + lane_off + (uint32_t)(h * C::NQ * VT + c0);
 #pragma unroll
-      for (int q = 0; q < C::NB + C::NS; q += 2) {  // big pairs first, then small pairs
-        tmem_ld32(base + q * VT, a);
-        tmem_ld32(base + (q + 1) * VT, b);
+      for (int q = 0; q < C::NQ; q += 2) {
+        tmem_ld16(base + q * VT, a);
+        tmem_ld16(base + (q + 1) * VT, b);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < VT; ++c) acc[c] += a[c] + b[c];
+        for (int c = 0; c < EC; ++c) acc[c] += a[c] + b[c];
       }
     };
 
@@ -522,17 +559,17 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
 #pragma unroll
         for (int h = 0; h < C::HALVES; ++h) {
           const int k = t + 128 * h;
-          if (j.layout == 0) {  // [K rows][32 floats], 128-byte swizzle
+          if (j.layout == 0) {  // [K rows][32 floats], 128-byte swizzle: pieces 4e..4e+3 of row k
             const uint8_t* row = ht + k * 128;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const float4 v = *reinterpret_cast<const float4*>(row + ((q ^ (k & 7)) << 4));
+            for (int q = 0; q < EC / 4; ++q) {
+              const float4 v = *reinterpret_cast<const float4*>(row + (((4 * e + q) ^ (k & 7)) << 4));
               y[h][4 * q] = v.x; y[h][4 * q + 1] = v.y; y[h][4 * q + 2] = v.z; y[h][4 * q + 3] = v.w;
             }
           } else {              // [VT rows][K floats]
             const float* f = reinterpret_cast<const float*>(ht) + k;
 #pragma unroll
-            for (int c = 0; c < VT; ++c) y[h][c] = f[c * K];
+            for (int c = 0; c < EC; ++c) y[h][c] = f[(c0 + c) * K];
           }
         }
         if (p.release != 2) {  // the h slot's last ordinary read is done: release it
@@ -544,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
 #pragma unroll
         for (int h = 0; h < C::HALVES; ++h)
 #pragma unroll
-          for (int c = 0; c < VT; ++c) y[h][c] = 0.f;
+          for (int c = 0; c < EC; ++c) y[h][c] = 0.f;
       }
       uint64_t* dbar = (p.stall_test && step == 0) ? &ctl->never : &ctl->d_full;
       if (!(ok = warp_wait(dbar, step & 1, wc))) break;
@@ -554,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       for (int h = 0; h < C::HALVES; ++h) drain_add(h, y[h]);
       if (step + 1 < nsteps) {  // X_{j+1} -> B operand: the critical path to the next step
         write_b();
-        tc_fence_before();  // the chains have been read (wait::ld in drain)
+        tc_fence_before();  // the chains have been read (wait::ld in drain_add)
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->x_ready);
         QLA_TR(3, step, 4, 0);
@@ -565,12 +602,12 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
           const int k = t + 128 * h;
           if (j.layout == 0) {
 #pragma unroll
-            for (int q = 0; q < VT / 4; ++q)
-              *reinterpret_cast<float4*>(F + (int64_t)k * V + v0 + 4 * q) =
+            for (int q = 0; q < EC / 4; ++q)
+              *reinterpret_cast<float4*>(F + (int64_t)k * V + v0 + c0 + 4 * q) =
                   make_float4(y[h][4 * q], y[h][4 * q + 1], y[h][4 * q + 2], y[h][4 * q + 3]);
           } else {
 #pragma unroll
-            for (int c = 0; c < VT; ++c) F[(int64_t)(v0 + c) * K + k] = y[h][c];
+            for (int c = 0; c < EC; ++c) F[(int64_t)(v0 + c0 + c) * K + k] = y[h][c];
           }
         }
       }
@@ -646,9 +683,10 @@ cudaError_t launch_k(const SeqJob& j, int release, unsigned int* status, uint64_
   const bool kv = j.layout == 0;
   const uint64_t rows = states * (kv ? (uint64_t)K : (uint64_t)j.V);
   const uint64_t cols = kv ? (uint64_t)j.V : (uint64_t)K;
-  // kv: box 32 columns x K rows (128-byte swizzle); vk: K columns x VT rows (TMA stores use 32-wide boxes)
+  // H: kv box 32 columns x K rows (128-byte swizzle); vk box K columns x VT rows
   if (p.has_h && !make_map(&p.map_h, j.H, rows, cols, kv ? 32 : K, kv ? K : VT, kv)) return cudaErrorInvalidValue;
-  if (j.out && !make_map(&p.map_out, j.out, rows, cols, 32, kv ? 32 : VT, kv)) return cudaErrorInvalidValue;
+  // out: per-warp stores of [32 rows][16 columns] (kv) or [16 rows][32 columns] (vk), no swizzle
+  if (j.out && !make_map(&p.map_out, j.out, rows, cols, kv ? EC : 32, kv ? 32 : EC, false)) return cudaErrorInvalidValue;
   const bool fwd = j.direction == 0;
   if (!make_map(&p.map_m, j.M, states * K, K, fwd ? 32 : 128, fwd ? 128 : 32, fwd)) return cudaErrorInvalidValue;
   auto kern = seq_tc_kernel<K>;
