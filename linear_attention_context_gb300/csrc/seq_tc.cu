@@ -30,7 +30,9 @@
 // an M=128, N=32, K=8 tf32 MMA keeps the tensor pipe busy for about 17, so
 // three threads issue: one the big terms, one A_hi X_lo, one A_lo X_hi, each
 // into its own accumulators (no two threads ever accumulate into the same
-// TMEM columns).
+// TMEM columns).  A barrier poll from an issuing thread waits until that
+// thread's queued MMAs have been dispatched (~110 cycles measured), so the
+// issuers poll once per pair of chunks, not per chunk.
 //
 // One CTA owns a VT-column tile of one unit (chain, group) for all of the
 // unit's segments.  Roles, storage, handoff and lifetime (the table the
@@ -54,7 +56,7 @@
 //  storage        written by           read by             reusable after
 //  m ring [s]     TMA (async)          splitter (generic)  splitter's last read: fence + m_empty arrive
 //  h slot [j&1]   TMA (async)          epilogue (generic)  epilogue's last read: fence + h_empty arrive
-//  A ring (TMEM)  splitter tcgen05.st  mma (async)         3 commits -> a_empty
+//  A ring (TMEM)  splitter tcgen05.st  mma (async)         3 commits -> a_empty (per group of 2 chunks)
 //  B hi/lo        epilogue st.shared   mma (async)         d_full (3 commits: all MMAs of the step done)
 //                 + fence.proxy.async
 //  chains (TMEM)  mma                  epilogue tcgen05.ld x_ready (epilogue's wait::ld done)
@@ -63,7 +65,8 @@
 //
 // Chunks go kc-major: chunk c = kc * HALVES + h is A[128h.., 32kc..], so the
 // two row blocks of K = 256 interleave.  Barriers: m_full/h_full count 1 +
-// transaction bytes; m_empty, a_full count 4 (the splitter warpgroup's warps);
+// transaction bytes; m_empty count 4 (the splitter warpgroup's warps); a_full
+// count 8 (a group of two A slots gets one chunk from each splitter warpgroup);
 // h_empty, x_ready count 8 (the epilogue warps); a_empty, d_full count 3 (one
 // tcgen05.commit per issuing thread).  Producers wait their empty barriers
 // with the parity of (use / slots) ^ 1, consumers their full barriers with
@@ -122,7 +125,10 @@ struct Cfg {
   static constexpr int NB = K == 128 ? 4 : 2;     // big-term chains per row block
   static constexpr int NQ = NB + 2;               // chains per row block (+ A_hi X_lo, A_lo X_hi)
   static constexpr uint32_t ACOL = HALVES * NQ * VT;  // first column of the A ring
-  static constexpr int NA = (int)((kTmemCols - ACOL) / 64);  // A ring slots (hi, lo: 64 columns)
+  static constexpr int NA = 4;                    // A ring slots (hi, lo: 64 columns each) ...
+  static constexpr int NAG = 2;                   // ... in two groups of two chunks, one barrier pair per group
+  static_assert(ACOL + NA * 64 <= kTmemCols, "TMEM columns");
+  static_assert(CPS % 4 == 0, "chunks per step");
   static constexpr int NM = K == 128 ? 6 : 4;     // m ring stages
   static constexpr int NOUT = K == 128 ? 2 : 1;   // out staging buffers
   static constexpr uint32_t TILE = (uint32_t)K * VT * 4;  // one state tile (bytes)
@@ -135,7 +141,6 @@ struct Cfg {
   static constexpr uint32_t CTRL_BYTES = 512;
   static constexpr uint32_t SMEM = OFF_CTRL + CTRL_BYTES + 1024;  // + alignment slack
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(NA >= 2 && NA <= 6, "A ring");
 };
 
 struct TcParams {
@@ -153,7 +158,7 @@ struct TcParams {
 
 struct Ctrl {
   uint64_t m_full[6], m_empty[6];
-  uint64_t a_full[6], a_empty[6];
+  uint64_t a_full[2], a_empty[2];
   uint64_t h_full[2], h_empty[2];
   uint64_t x_ready, d_full, never;
   uint64_t mma_done[3];
@@ -221,23 +226,26 @@ __device__ __forceinline__ void mma_role(const SeqJob& j, Ctrl* ctl, uint8_t* sm
   // compile-time byte offset (>> 4) to the start-address field.
   const uint64_t dh0 = smem_desc_sw128(smem_u32(smem + C::OFF_BHI), 1024);
   const uint64_t dl0 = smem_desc_sw128(smem_u32(smem + C::OFF_BLO), 1024);
-  int slot = 0;
+  int grp = 0;
   uint32_t phase = 0;
   bool ok = true;
   for (int step = 0; step < nsteps && ok; ++step) {
     if (!(ok = mbar_wait(&ctl->x_ready, step & 1, wc))) break;
     if (ROLE == 0) QLA_TR(1, step, 0, 0);
     tc_fence_after();
+    // One wait and one commit per pair of chunks: a barrier poll from this
+    // thread stalls until its queued MMAs have been dispatched.
 #pragma unroll
-    for (int c = 0; c < C::CPS; ++c) {
-      if (!(ok = mbar_wait(&ctl->a_full[slot], phase, wc))) break;
+    for (int c = 0; c < C::CPS; c += 2) {
+      if (!(ok = mbar_wait(&ctl->a_full[grp], phase, wc))) break;
       if (ROLE == 0) QLA_TR(1, step, 1, c);
       tc_fence_after();
-      mma_chunk<K, ROLE>(c, tmem, tmem + C::ACOL + slot * 64, dh0, dl0);
-      mma_commit(&ctl->a_empty[slot]);
+      mma_chunk<K, ROLE>(c, tmem, tmem + C::ACOL + (2 * grp) * 64, dh0, dl0);
+      mma_chunk<K, ROLE>(c + 1, tmem, tmem + C::ACOL + (2 * grp + 1) * 64, dh0, dl0);
+      mma_commit(&ctl->a_empty[grp]);
       if (ROLE == 0) QLA_TR(1, step, 3, c);
-      if (++slot == C::NA) {
-        slot = 0;
+      if (++grp == C::NAG) {
+        grp = 0;
         phase ^= 1;
       }
     }
@@ -277,9 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       mbar_init(&ctl->m_full[i], 1);
       mbar_init(&ctl->m_empty[i], 4);
     }
-    for (int i = 0; i < C::NA; ++i) {
-      mbar_init(&ctl->a_full[i], 4);
-      mbar_init(&ctl->a_empty[i], 3);
+    for (int i = 0; i < C::NAG; ++i) {
+      mbar_init(&ctl->a_full[i], 8);   // both splitter warpgroups fill one chunk of the group
+      mbar_init(&ctl->a_empty[i], 3);  // one commit per issuing thread
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->h_full[i], 1);
@@ -373,8 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
     const int t = 32 * (warp & 3) + lane;            // A row within the 128-row block = TMEM lane
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const int total = nsteps * C::CPS;
-    int stage = grp, aslot = grp;
-    uint32_t mphase = 0, aphase = 0;
+    int stage = grp;
+    uint32_t mphase = 0;
     bool ok = true;
     for (int mit = grp; mit < total && ok; mit += 2) {
       const int step = mit / C::CPS, c = mit % C::CPS;
@@ -401,7 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->m_empty[stage]);
       }
-      if (!(ok = warp_wait(&ctl->a_empty[aslot], aphase ^ 1, wc))) break;
+      const int aslot = mit % C::NA, agrp = aslot >> 1;
+      const uint32_t aphase = (uint32_t)(mit / C::NA) & 1;
+      if (!(ok = warp_wait(&ctl->a_empty[agrp], aphase ^ 1, wc))) break;
       QLA_TR(2, step, 1, c);
       tc_fence_after();
       const uint32_t a = tmem + lane_off + C::ACOL + aslot * 64;
@@ -416,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->a_full[aslot]);
+      if (lane == 0) mbar_arrive(&ctl->a_full[agrp]);
       QLA_TR(2, step, 2, c);
       if (p.release == 2) {
         __syncwarp();
@@ -425,10 +435,6 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       if ((stage += 2) >= C::NM) {
         stage -= C::NM;
         mphase ^= 1;
-      }
-      if ((aslot += 2) >= C::NA) {
-        aslot -= C::NA;
-        aphase ^= 1;
       }
     }
   } else {
@@ -589,8 +595,10 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       tc_fence_after();
 #pragma unroll
       for (int h = 0; h < C::HALVES; ++h) drain_add(h, y[h]);
+      QLA_TR(3, step, 5, 0);
       if (step + 1 < nsteps) {  // X_{j+1} -> B operand: the critical path to the next step
         write_b();
+        QLA_TR(3, step, 6, 0);
         tc_fence_before();  // the chains have been read (wait::ld in drain_add)
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->x_ready);
