@@ -122,13 +122,13 @@ struct Cfg {
   static constexpr int HALVES = K / 128;          // 128-row MMA blocks of the output
   static constexpr int KCH = K / 32;              // 32-wide k chunks per block
   static constexpr int CPS = HALVES * KCH;        // chunks per step
-  static constexpr int NB = K == 128 ? 4 : 2;     // big-term chains per row block
+  static constexpr int NB = 2;                    // big-term chains per row block
   static constexpr int NQ = NB + 2;               // chains per row block (+ A_hi X_lo, A_lo X_hi)
   static constexpr uint32_t ACOL = HALVES * NQ * VT;  // first column of the A ring
-  static constexpr int NA = 4;                    // A ring slots (hi, lo: 64 columns each) ...
-  static constexpr int NAG = 2;                   // ... in two groups of two chunks, one barrier pair per group
+  static constexpr int NA = (int)((kTmemCols - ACOL) / 128) * 2;  // A ring slots (hi, lo: 64 columns each) ...
+  static constexpr int NAG = NA / 2;              // ... in groups of two chunks, one barrier pair per group
   static_assert(ACOL + NA * 64 <= kTmemCols, "TMEM columns");
-  static_assert(CPS % 4 == 0, "chunks per step");
+  static_assert(CPS % 2 == 0 && NAG <= 4, "chunks per step, A groups");
   static constexpr int NM = K == 128 ? 6 : 4;     // m ring stages
   static constexpr int NOUT = K == 128 ? 2 : 1;   // out staging buffers
   static constexpr uint32_t TILE = (uint32_t)K * VT * 4;  // one state tile (bytes)
@@ -158,7 +158,7 @@ struct TcParams {
 
 struct Ctrl {
   uint64_t m_full[6], m_empty[6];
-  uint64_t a_full[2], a_empty[2];
+  uint64_t a_full[4], a_empty[4];
   uint64_t h_full[2], h_empty[2];
   uint64_t x_ready, d_full, never;
   uint64_t mma_done[3];
