@@ -122,7 +122,7 @@ struct Cfg {
   static constexpr int HALVES = K / 128;          // 128-row MMA blocks of the output
   static constexpr int KCH = K / 32;              // 32-wide k chunks per block
   static constexpr int CPS = HALVES * KCH;        // chunks per step
-  static constexpr int NB = 2;                    // big-term chains per row block
+  static constexpr int NB = K == 128 ? 4 : 2;     // big-term chains per row block
   static constexpr int NQ = NB + 2;               // chains per row block (+ A_hi X_lo, A_lo X_hi)
   static constexpr uint32_t ACOL = HALVES * NQ * VT;  // first column of the A ring
   static constexpr int NA = (int)((kTmemCols - ACOL) / 128) * 2;  // A ring slots (hi, lo: 64 columns each) ...
