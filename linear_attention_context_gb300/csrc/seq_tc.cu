@@ -481,10 +481,10 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
 #pragma unroll
       for (int h = 0; h < C::HALVES; ++h) {
         float* stg = reinterpret_cast<float*>(smem + C::OFF_OUT + b * C::TILE + ((h * 2 + e) * 4 + wq) * 2048);
-        if (j.layout == 0) {  // [32 rows][16 floats]: this lane's row
+        if (j.layout == 0) {  // [32 rows][16 floats], 64-byte swizzle: 16-byte piece q of row r at q ^ ((r/2)%4)
 #pragma unroll
           for (int q = 0; q < EC / 4; ++q)
-            *reinterpret_cast<float4*>(stg + lane * EC + 4 * q) =
+            *reinterpret_cast<float4*>(stg + lane * EC + 4 * (q ^ ((lane >> 1) & 3))) =
                 make_float4(y[h][4 * q], y[h][4 * q + 1], y[h][4 * q + 2], y[h][4 * q + 3]);
         } else {              // [16 rows][32 floats]: column `lane`
 #pragma unroll
@@ -658,19 +658,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D fp32 tensor map: `rows` x `cols` row-major at `base`, box box_cols x box_rows.
+// 2-D fp32 tensor map: `rows` x `cols` row-major at `base`, box box_cols x box_rows,
+// swizzle 0 (none), 64 or 128 (bytes).
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows,
-              bool swizzle128) {
+              int swizzle) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 4};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = swizzle == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                : CU_TENSOR_MAP_SWIZZLE_NONE;
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -692,11 +695,14 @@ cudaError_t launch_k(const SeqJob& j, int release, unsigned int* status, uint64_
   const uint64_t rows = states * (kv ? (uint64_t)K : (uint64_t)j.V);
   const uint64_t cols = kv ? (uint64_t)j.V : (uint64_t)K;
   // H: kv box 32 columns x K rows (128-byte swizzle); vk box K columns x VT rows
-  if (p.has_h && !make_map(&p.map_h, j.H, rows, cols, kv ? 32 : K, kv ? K : VT, kv)) return cudaErrorInvalidValue;
-  // out: per-warp stores of [32 rows][16 columns] (kv) or [16 rows][32 columns] (vk), no swizzle
-  if (j.out && !make_map(&p.map_out, j.out, rows, cols, kv ? EC : 32, kv ? 32 : EC, false)) return cudaErrorInvalidValue;
+  if (p.has_h && !make_map(&p.map_h, j.H, rows, cols, kv ? 32 : K, kv ? K : VT, kv ? 128 : 0))
+    return cudaErrorInvalidValue;
+  // out: per-warp stores of [32 rows][16 columns] (kv, 64-byte swizzle) or [16 rows][32 columns] (vk)
+  if (j.out && !make_map(&p.map_out, j.out, rows, cols, kv ? EC : 32, kv ? 32 : EC, kv ? 64 : 0))
+    return cudaErrorInvalidValue;
   const bool fwd = j.direction == 0;
-  if (!make_map(&p.map_m, j.M, states * K, K, fwd ? 32 : 128, fwd ? 128 : 32, fwd)) return cudaErrorInvalidValue;
+  if (!make_map(&p.map_m, j.M, states * K, K, fwd ? 32 : 128, fwd ? 128 : 32, fwd ? 128 : 0))
+    return cudaErrorInvalidValue;
   auto kern = seq_tc_kernel<K>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
