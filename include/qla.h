@@ -160,6 +160,40 @@ QLA_API int qla_device_status(int* flags);
 QLA_API int qla_selftest_stalled_wait(const float* H, const float* M, float* out, int S,
                               int wait_limit_us, void* stream);
 
+/*
+ * The scan variant without any allocation (this entry point has no
+ * counterpart on the pages; it exists for callers of this library).
+ *
+ * Some callers cannot call cudaMalloc or cudaMallocAsync: code that runs with
+ * a fixed device-memory budget handed out at start-up (an inference server's
+ * arena, an embedded or real-time host loop) must not grow the process's
+ * device footprint per call, and cudaMalloc can synchronise the device, which
+ * a latency-bound caller cannot afford.  This entry point runs the same scan
+ * as qla_cp_correct_ex(..., QLA_VARIANT_SCAN, ...) but keeps its scratch in a
+ * fixed device array inside the library (QLA_SCAN_STATIC_BYTES, allocated when
+ * the library is loaded and held by every GPU that loads it until the process
+ * exits), so it allocates nothing: no cudaMalloc, cudaMallocAsync, cudaFree or
+ * allocating library routine.  The caller still passes H, M, h_init, out and
+ * final_state as for qla_cp_correct_ex.
+ *
+ * - Scratch needed is qla_scan_workspace_bytes(B, heads, S, K, V, scan_group);
+ *   a shape that needs more than QLA_SCAN_STATIC_BYTES returns
+ *   QLA_ERR_UNSUPPORTED (qla_last_error() gives both sizes) and launches
+ *   nothing.
+ * - The first call on a device looks up that device's address of the array
+ *   (once per device, with that device current); make that first call before
+ *   any stream capture on the device.
+ * - Every call on a device shares the one array and it keeps the last call's
+ *   contents.  Nothing in it needs to start at zero: each scan phase writes
+ *   every scratch element it later reads.  Calls whose work overlaps on the
+ *   GPU (two streams, or two host threads without ordering) race on the
+ *   array; order them on one stream.
+ */
+#define QLA_SCAN_STATIC_BYTES (8u << 20)
+QLA_API int qla_cp_correct_scan_static(const float* H, const float* M, const float* h_init, float* out,
+                                       float* final_state, int B, int heads, int S, int K, int V, int layout,
+                                       int direction, int engine, int release, int scan_group, void* stream);
+
 /* ABI version of this header (major * 100 + minor). */
 QLA_API int qla_version(void);
 

@@ -33,7 +33,10 @@ STATUS = {0: "QLA_OK", -1: "QLA_ERR_INVALID_ARG", -2: "QLA_ERR_UNSUPPORTED", -3:
 # Every function include/qla.h declares.
 EXPORTS = ("qla_cp_correct", "qla_cp_correct_ex", "qla_scan_workspace_bytes", "qla_resolve",
            "qla_status_string", "qla_last_error", "qla_device_status", "qla_selftest_stalled_wait",
-           "qla_version")
+           "qla_cp_correct_scan_static", "qla_version")
+
+# Bytes of scratch the allocation-free scan entry point holds (QLA_SCAN_STATIC_BYTES).
+SCAN_STATIC_BYTES = 8 << 20
 
 
 class QlaError(RuntimeError):
@@ -75,6 +78,8 @@ def lib():
         L.qla_device_status.restype = ci
         L.qla_selftest_stalled_wait.argtypes = [vp, vp, vp, ci, ci, vp]
         L.qla_selftest_stalled_wait.restype = ci
+        L.qla_cp_correct_scan_static.argtypes = [vp, vp, vp, vp, vp] + [ci] * 10 + [vp]
+        L.qla_cp_correct_scan_static.restype = ci
         L.qla_version.argtypes = []
         L.qla_version.restype = ci
         _LIB = L

@@ -285,6 +285,95 @@ int run_scan(const float* H, const float* M, const float* h_init, float* out, fl
   return st;
 }
 
+// ---------------------------------------------------------------- allocation-free scan
+//
+// Scratch of qla_cp_correct_scan_static(): a fixed array of this file, one
+// per device that loads the library.  Host code must not use the symbol as
+// an address; it looks up each device's address once, with that device
+// current, and passes the result to the kernels.
+static __device__ __align__(256) float g_scan_static[QLA_SCAN_STATIC_BYTES / sizeof(float)];
+
+std::mutex g_static_mutex;
+float* g_static_ptr[kMaxDevices];
+
+int scan_static_pointer(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(QLA_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_static_mutex);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_scan_static)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(scan scratch)");
+    g_static_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_static_ptr[dev];
+  return QLA_OK;
+}
+
+// The four scan phases of run_scan(), on a caller-provided workspace.
+int run_scan_in(const float* H, const float* M, const float* h_init, float* out, float* fin, const Shape& s,
+                int engine, int release, int G, float* ws, const DeviceInfo* d, cudaStream_t stream) {
+  const int L = (s.S + G - 1) / G;
+  const int Gr = (s.S + L - 1) / L;
+  float* Aagg = ws;
+  float* bagg = Aagg + (size_t)s.chains() * Gr * s.K * s.K;
+  float* carry = bagg + (size_t)s.chains() * Gr * s.state();
+  const SeqJob base = plain_job(H, M, h_init, out, fin, s);
+  int st;
+  {  // 1a: group products of M, forward, kv view, from the identity
+    SeqJob j = base;
+    j.H = nullptr;
+    j.init = nullptr;
+    j.init_mode = kInitIdentity;
+    j.out = nullptr;
+    j.fin = Aagg;
+    j.fin_unit_stride = (int64_t)s.K * s.K;
+    j.L = L;
+    j.G = Gr;
+    j.V = s.K;
+    j.layout = QLA_LAYOUT_KV;
+    j.direction = QLA_FORWARD;
+    if ((st = launch_seq(j, engine_for(j, engine), release, d, stream)) != QLA_OK) return st;
+  }
+  {  // 1b: group recurrences from zero
+    SeqJob j = base;
+    j.init = nullptr;
+    j.init_mode = kInitZero;
+    j.out = nullptr;
+    j.fin = bagg;
+    j.fin_unit_stride = s.state();
+    j.L = L;
+    j.G = Gr;
+    if ((st = launch_seq(j, engine_for(j, engine), release, d, stream)) != QLA_OK) return st;
+  }
+  {  // 2: carries across the group aggregates
+    SeqJob j = base;
+    j.H = bagg;
+    j.M = Aagg;
+    j.h_chain_stride = (int64_t)Gr * s.state();
+    j.m_chain_stride = (int64_t)Gr * s.K * s.K;
+    j.out = carry;
+    j.fin = fin;
+    j.S = Gr;
+    j.L = Gr;
+    j.G = 1;
+    if ((st = launch_seq(j, engine_for(j, engine), release, d, stream)) != QLA_OK) return st;
+  }
+  if (out) {  // 3: re-run each group from its entering state
+    SeqJob j = base;
+    j.init = carry;
+    j.init_mode = kInitPointer;
+    j.init_unit_stride = s.state();
+    j.fin = nullptr;
+    j.L = L;
+    j.G = Gr;
+    if ((st = launch_seq(j, engine_for(j, engine), release, d, stream)) != QLA_OK) return st;
+  }
+  return QLA_OK;
+}
+
 }  // namespace
 }  // namespace qla
 
@@ -293,6 +382,35 @@ using namespace qla;
 extern "C" {
 
 int qla_version(void) { return 100; }
+
+int qla_cp_correct_scan_static(const float* H, const float* M, const float* h_init, float* out, float* final_state,
+                               int B, int heads, int S, int K, int V, int layout, int direction, int engine,
+                               int release, int scan_group, void* stream) {
+  t_last_error.clear();
+  Shape s{B, heads, S, K, V, layout, direction};
+  int st = check_args(H, M, h_init, out, final_state, s);
+  if (st != QLA_OK) return st;
+  if (engine < QLA_ENGINE_AUTO || engine > QLA_ENGINE_TC) return fail(QLA_ERR_INVALID_ARG, "unknown engine %d", engine);
+  if (release < QLA_RELEASE_MEMBAR || release > QLA_RELEASE_NONE)
+    return fail(QLA_ERR_INVALID_ARG, "unknown release mode %d", release);
+  if (scan_group < 0) return fail(QLA_ERR_INVALID_ARG, "scan_group must be >= 0");
+  const int G = scan_group > 0 ? std::min(scan_group, S) : auto_groups(S);
+  const int L = (S + G - 1) / G;
+  const size_t need = scan_bytes(s, (S + L - 1) / L);
+  if (need > QLA_SCAN_STATIC_BYTES)
+    return fail(QLA_ERR_UNSUPPORTED,
+                "this shape needs %zu bytes of scan scratch; the allocation-free scan holds %u bytes "
+                "(use qla_cp_correct_ex with QLA_VARIANT_SCAN instead)",
+                need, (unsigned)QLA_SCAN_STATIC_BYTES);
+  DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != QLA_OK) return st;
+  float* ws = nullptr;
+  if ((st = scan_static_pointer(&ws)) != QLA_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const int eng = resolve_engine(s, engine);
+  if (S == 1) return launch_seq(plain_job(H, M, h_init, out, final_state, s), eng, release, d, cs);
+  return run_scan_in(H, M, h_init, out, final_state, s, eng, release, G, ws, d, cs);
+}
 
 const char* qla_status_string(int status) {
   switch (status) {
