@@ -143,8 +143,7 @@ int auto_groups(int S) {
 }
 
 int resolve_engine(const Shape& s, int engine) {
-  (void)s;
-  if (engine == QLA_ENGINE_AUTO) return QLA_ENGINE_SIMT;
+  if (engine == QLA_ENGINE_AUTO) return tc_supports(s.K, s.V) ? QLA_ENGINE_TC : QLA_ENGINE_SIMT;
   return engine;
 }
 

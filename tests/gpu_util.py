@@ -9,7 +9,7 @@ import numpy as np
 # Engines under test.  The tensor-core engine takes the shapes listed in
 # tc_supports(); the others take every supported shape.
 ALL_ENGINES = ("simt", "ws_simt", "tc")
-BUILT_ENGINES = ("simt",)
+BUILT_ENGINES = ("simt", "tc")
 
 
 def engines_under_test():
