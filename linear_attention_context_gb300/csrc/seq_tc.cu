@@ -727,8 +727,10 @@ cudaError_t launch_seq_tc(const SeqJob& job, int release, unsigned int* status, 
                           cudaStream_t stream) {
   if (!tc_supports(job.K, job.V)) return cudaErrorInvalidValue;
   if ((int64_t)job.nchains * job.G > 65535) return cudaErrorInvalidValue;
-  if (job.h_chain_stride != (int64_t)job.S * job.K * job.V || job.m_chain_stride != (int64_t)job.S * job.K * job.K)
-    return cudaErrorInvalidValue;
+  // The tensor maps view H/out and M as 2-D arrays of all chains' states, so
+  // chains must be packed back to back (H and out are absent in scan phase 1a).
+  if ((job.H || job.out) && job.h_chain_stride != (int64_t)job.S * job.K * job.V) return cudaErrorInvalidValue;
+  if (job.m_chain_stride != (int64_t)job.S * job.K * job.K) return cudaErrorInvalidValue;
   return job.K == 128 ? launch_k<128>(job, release, status, limit_ns, stall_test, stream)
                       : launch_k<256>(job, release, status, limit_ns, stall_test, stream);
 }
