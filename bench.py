@@ -49,6 +49,25 @@ def algorithmic_flops(chains, S_, K_, V_):
     return 2 * chains * (S_ - 1) * K_ * K_ * V_
 
 
+def kernel_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    capture, or None when the kernel sources changed since it was taken."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    h = hashlib.sha256()
+    for s in d.get("sources", []):
+        fp = os.path.join(ROOT, s)
+        if not os.path.exists(fp):
+            return None
+        with open(fp, "rb") as f:
+            h.update(f.read())
+    return d["dram_bytes_per_launch"] if h.hexdigest() == d.get("sources_sha256") else None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -308,7 +327,8 @@ def run_ours(args):
                        "graph": "one CUDA graph per step (its 4 calls)",
                        "parallelism": f"replicas x{world} (no collective)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": args.traffic,
+                         "frac": round(achieved / peak, 4),
+                         "traffic": args.traffic if args.traffic is not None else (kernel_traffic() if eng == "tc" else None),
                          "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                                         if peak_kind == "measured" else "fallback 6.8 TB/s",
                          "algorithmic_bytes_per_launch": bytes_call, "launches_per_call": launches_per_call,
