@@ -56,6 +56,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep in hardware for up to `hint_ns`
+// until the phase completes; it resumes as soon as the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Shared abort state of one CTA plus the device-wide status word.
 struct WaitCtl {
   volatile int* abort;        // shared memory: non-zero once any role gave up
@@ -63,13 +79,18 @@ struct WaitCtl {
   uint64_t limit_ns;          // per-wait time limit
 };
 
+// Sleep granularity of the bounded waits: a hinted try_wait wakes as soon as
+// the phase completes, so this only sets how often the abort flag and the
+// time limit are looked at while a wait really stalls.
+constexpr uint32_t kWaitSleepNs = 200000;  // 0.2 ms
+
 // Bounded wait for the phase with the given parity.  Returns false (and raises
 // the abort flag) when the limit passes or another role has already aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& c) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if (*c.abort) return false;
     if (globaltimer() - t0 > c.limit_ns) {
       *c.abort = 1;
@@ -82,7 +103,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
 // Bounded wait used while draining after an abort: ignores the abort flag.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) {
     if (globaltimer() - t0 > limit_ns) return false;
   }
   return true;
