@@ -9,14 +9,15 @@
 // engine keeps that producer/consumer shape and moves the contraction onto
 // tcgen05 with fp32 accuracy from three TF32 products:
 //     A X ~= A_hi X_hi + A_hi X_lo + A_lo X_hi,
-// with hi = x rounded to the nearest TF32 value and lo = x - hi (exact in
-// fp32) rounded to the nearest TF32 value.  Both operands reach the tensor
-// core already exact in TF32, so it drops no bits of them.  Rounding to
-// nearest matters: the tensor core cuts the 13 low mantissa bits of an fp32
-// operand toward zero, and a lo taken by truncation carries x's sign, which
-// turned that cut into a coherent shrink of about 2^-20 per step.  The
-// remaining errors (the rounding of lo, the dropped A_lo X_lo term, both
-// below 2^-22 relative) are unbiased.
+// The tensor core reads an fp32 operand as TF32 by cutting its 13 low mantissa
+// bits toward zero (measured).  So every lo part is rounded to the nearest
+// TF32 value before the MMA sees it: a lo cut toward zero is biased (it keeps
+// x's sign), and that bias showed as a coherent shrink of about 2^-20 per
+// step.  A (the propagation matrix) splits as hi = RN_tf32(a),
+// lo = RN_tf32(a - hi); X (the state) uses hi = the raw value, which the
+// tensor core reads exactly as trunc_tf32(x), and lo = RN_tf32(x - trunc(x)).
+// With A's lo of random sign, the dropped A_lo X_lo term (below 2^-21
+// relative) is unbiased, as is the rounding of each lo (below 2^-21).
 //
 // Accumulation: the tensor core also rounds its fp32 accumulator toward zero,
 // so a long chain of MMAs into one accumulator shrinks the result coherently
@@ -522,10 +523,11 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
 #pragma unroll
         for (int c = 0; c < EC; ++c) {  // n = c0 + c; c0 is a multiple of 8
           const uint32_t off = rowoff[c & 7] + (uint32_t)(c >> 3) * 1024;
-          uint32_t hb, lb;
-          split_tf32(y[h][c], hb, lb);
-          *reinterpret_cast<uint32_t*>(bhi + off) = hb;
-          *reinterpret_cast<uint32_t*>(blo + off) = lb;
+          // hi: the raw value (the tensor core reads it as trunc_tf32(y), exactly);
+          // lo: y - trunc_tf32(y), rounded to the nearest TF32 value.
+          const float yv = y[h][c];
+          *reinterpret_cast<float*>(bhi + off) = yv;
+          *reinterpret_cast<uint32_t*>(blo + off) = tf32_rn_bits(yv - __uint_as_float(__float_as_uint(yv) & 0xFFFFE000u));
         }
       }
       fence_proxy_async_smem();  // generic writes -> read by tcgen05.mma (async proxy)
