@@ -112,36 +112,40 @@ namespace {
 
 using namespace ptx;
 
-constexpr int VT = 32;                          // state columns per CTA
+constexpr int VT = 32;                          // state columns per tile
 constexpr int EC = 16;                          // state columns per epilogue warpgroup
-constexpr int kThreads = 640;                   // 20 warps
 constexpr uint32_t kChunkBytes = 128 * 32 * 4;  // one A chunk: 128 rows x 32 columns fp32
 constexpr uint32_t kTmemCols = 512;
 
-template <int K>
+// TILES column tiles of VT columns share one CTA, one M stream and one A
+// split; with two, the issuers run all of tile 0's MMAs of a step before
+// tile 1's, so tile 0's epilogue overlaps tile 1's MMAs.
+template <int K, int TILES>
 struct Cfg {
   static constexpr int HALVES = K / 128;          // 128-row MMA blocks of the output
   static constexpr int KCH = K / 32;              // 32-wide k chunks per block
   static constexpr int CPS = HALVES * KCH;        // chunks per step
-  static constexpr int NB = K == 128 ? 4 : 2;     // big-term chains per row block
+  static constexpr int NB = (TILES == 1 && K == 128) ? 4 : 2;  // big-term chains per row block
   static constexpr int NQ = NB + 2;               // chains per row block (+ A_hi X_lo, A_lo X_hi)
-  static constexpr uint32_t ACOL = HALVES * NQ * VT;  // first column of the A ring
+  static constexpr uint32_t ACOL = TILES * HALVES * NQ * VT;  // first column of the A ring
   static constexpr int NA = (int)((kTmemCols - ACOL) / 128) * 2;  // A ring slots (hi, lo: 64 columns each) ...
   static constexpr int NAG = NA / 2;              // ... in groups of two chunks, one barrier pair per group
-  static_assert(ACOL + NA * 64 <= kTmemCols, "TMEM columns");
-  static_assert(CPS % 2 == 0 && NAG <= 4, "chunks per step, A groups");
-  static constexpr int NM = K == 128 ? 6 : 4;     // m ring stages
-  static constexpr int NOUT = K == 128 ? 2 : 1;   // out staging buffers
+  static constexpr int NM = TILES == 2 ? 4 : (K == 128 ? 6 : 4);  // m ring stages
+  static constexpr int NOUT = (TILES == 1 && K == 128) ? 2 : 1;    // out staging buffers per tile
+  static constexpr int WARPS = 12 + 8 * TILES;    // WG0 + 2 splitter WGs + 2 epilogue WGs per tile
   static constexpr uint32_t TILE = (uint32_t)K * VT * 4;  // one state tile (bytes)
   static constexpr uint32_t OFF_M = 0;
-  static constexpr uint32_t OFF_H = OFF_M + NM * kChunkBytes;
-  static constexpr uint32_t OFF_BHI = OFF_H + 2 * TILE;
-  static constexpr uint32_t OFF_BLO = OFF_BHI + TILE;
-  static constexpr uint32_t OFF_OUT = OFF_BLO + TILE;
-  static constexpr uint32_t OFF_CTRL = OFF_OUT + NOUT * TILE;
+  static constexpr uint32_t OFF_H = OFF_M + NM * kChunkBytes;       // [TILES][2 slots]
+  static constexpr uint32_t OFF_BHI = OFF_H + TILES * 2 * TILE;     // [TILES] (hi), then [TILES] (lo)
+  static constexpr uint32_t OFF_BLO = OFF_BHI + TILES * TILE;
+  static constexpr uint32_t OFF_OUT = OFF_BLO + TILES * TILE;       // [TILES][NOUT]
+  static constexpr uint32_t OFF_CTRL = OFF_OUT + TILES * NOUT * TILE;
   static constexpr uint32_t CTRL_BYTES = 512;
   static constexpr uint32_t SMEM = OFF_CTRL + CTRL_BYTES + 1024;  // + alignment slack
   static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(ACOL + NA * 64 <= kTmemCols, "TMEM columns");
+  static_assert(CPS % 2 == 0 && NAG >= 1 && NAG <= 4, "chunks per step, A groups");
+  static_assert(TILES == 1 || K == 128, "two tiles only for K = 128");
 };
 
 struct TcParams {
@@ -160,8 +164,9 @@ struct TcParams {
 struct Ctrl {
   uint64_t m_full[6], m_empty[6];
   uint64_t a_full[4], a_empty[4];
-  uint64_t h_full[2], h_empty[2];
-  uint64_t x_ready, d_full, never;
+  uint64_t h_full[2][2], h_empty[2][2];  // [tile][slot]
+  uint64_t x_ready[2], d_full[2];        // [tile]
+  uint64_t never;
   uint64_t mma_done[3];
   uint32_t tmem_base;
   int abort;
@@ -190,15 +195,16 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) 
 }
 
 // The MMAs one issuing thread owes chunk c (k-block kc = c / HALVES, row
-// block h = c % HALVES): role 0 the four A_hi X_hi k-steps, role 1 the A_hi X_lo
-// ones, role 2 the A_lo X_hi ones.  With c and the role compile-time
-// constants every chain index and accumulate flag folds to a constant.
-template <int K, int ROLE>
-__device__ __forceinline__ void mma_chunk(const int c, uint32_t tmem, uint32_t a_hi, uint64_t dh0, uint64_t dl0) {
-  using C = Cfg<K>;
+// block h = c % HALVES) of tile `tl`: role 0 the four A_hi X_hi k-steps, role
+// 1 the A_hi X_lo ones, role 2 the A_lo X_hi ones.  With c, tl and the role
+// compile-time constants every chain index and accumulate flag folds.
+template <int K, int TILES, int ROLE>
+__device__ __forceinline__ void mma_chunk(const int tl, const int c, uint32_t tmem, uint32_t a_hi, uint64_t dh0,
+                                          uint64_t dl0) {
+  using C = Cfg<K, TILES>;
   constexpr uint32_t idesc = idesc_tf32(128, VT);
   const int kc = c / C::HALVES, h = c % C::HALVES;
-  const int q0 = h * C::NQ;
+  const int q0 = (tl * C::HALVES + h) * C::NQ;
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const int ks = kc * 4 + s;  // k-step within the row block: B rows [8 ks, 8 ks + 8)
@@ -213,53 +219,67 @@ __device__ __forceinline__ void mma_chunk(const int c, uint32_t tmem, uint32_t a
   }
 }
 
-template <int K, int ROLE>
-__device__ __forceinline__ void mma_role(const SeqJob& j, Ctrl* ctl, uint8_t* smem, uint32_t tmem, int nsteps,
-                                         const WaitCtl& wc
+template <int K, int TILES, int ROLE>
+__device__ __forceinline__ void mma_role(Ctrl* ctl, uint8_t* smem, uint32_t tmem, int nsteps, const WaitCtl& wc
 #ifdef QLA_TRACE
                                          ,
                                          bool tr
 #endif
 ) {
-  using C = Cfg<K>;
-  (void)j;
-  // Descriptors of the k-block 0 rows of B hi / lo; every other k-step adds a
-  // compile-time byte offset (>> 4) to the start-address field.
-  const uint64_t dh0 = smem_desc_sw128(smem_u32(smem + C::OFF_BHI), 1024);
-  const uint64_t dl0 = smem_desc_sw128(smem_u32(smem + C::OFF_BLO), 1024);
-  int grp = 0;
-  uint32_t phase = 0;
+  using C = Cfg<K, TILES>;
+  // Descriptors of the k-block 0 rows of each tile's B hi / lo; every other
+  // k-step adds a compile-time byte offset (>> 4) to the start-address field.
+  uint64_t dh0[TILES], dl0[TILES];
+#pragma unroll
+  for (int tl = 0; tl < TILES; ++tl) {
+    dh0[tl] = smem_desc_sw128(smem_u32(smem + C::OFF_BHI + tl * C::TILE), 1024);
+    dl0[tl] = smem_desc_sw128(smem_u32(smem + C::OFF_BLO + tl * C::TILE), 1024);
+  }
+  int grp0 = 0;
+  uint32_t phase0 = 0;
   bool ok = true;
   for (int step = 0; step < nsteps && ok; ++step) {
-    if (!(ok = mbar_wait(&ctl->x_ready, step & 1, wc))) break;
-    if (ROLE == 0) QLA_TR(1, step, 0, 0);
-    tc_fence_after();
-    // One wait and one commit per pair of chunks: a barrier poll from this
-    // thread stalls until its queued MMAs have been dispatched.
 #pragma unroll
-    for (int c = 0; c < C::CPS; c += 2) {
-      if (!(ok = mbar_wait(&ctl->a_full[grp], phase, wc))) break;
-      if (ROLE == 0) QLA_TR(1, step, 1, c);
+    for (int tl = 0; tl < TILES && ok; ++tl) {
+      if (!(ok = mbar_wait(&ctl->x_ready[tl], step & 1, wc))) break;
+      if (ROLE == 0 && tl == 0) QLA_TR(1, step, 0, 0);
       tc_fence_after();
-      mma_chunk<K, ROLE>(c, tmem, tmem + C::ACOL + (2 * grp) * 64, dh0, dl0);
-      mma_chunk<K, ROLE>(c + 1, tmem, tmem + C::ACOL + (2 * grp + 1) * 64, dh0, dl0);
-      mma_commit(&ctl->a_empty[grp]);
-      if (ROLE == 0) QLA_TR(1, step, 3, c);
-      if (++grp == C::NAG) {
-        grp = 0;
-        phase ^= 1;
+      int grp = grp0;
+      uint32_t phase = phase0;
+      // One wait and one commit per pair of chunks: a barrier poll from this
+      // thread stalls until its queued MMAs have been dispatched.  The A
+      // pairs are waited for by tile 0 and released after the last tile.
+#pragma unroll
+      for (int c = 0; c < C::CPS; c += 2) {
+        if (tl == 0) {
+          if (!(ok = mbar_wait(&ctl->a_full[grp], phase, wc))) break;
+          if (ROLE == 0) QLA_TR(1, step, 1, c);
+          tc_fence_after();
+        }
+        mma_chunk<K, TILES, ROLE>(tl, c, tmem, tmem + C::ACOL + (2 * grp) * 64, dh0[tl], dl0[tl]);
+        mma_chunk<K, TILES, ROLE>(tl, c + 1, tmem, tmem + C::ACOL + (2 * grp + 1) * 64, dh0[tl], dl0[tl]);
+        if (tl == TILES - 1) mma_commit(&ctl->a_empty[grp]);
+        if (ROLE == 0 && tl == 0) QLA_TR(1, step, 3, c);
+        if (++grp == C::NAG) {
+          grp = 0;
+          phase ^= 1;
+        }
+      }
+      if (ok) mma_commit(&ctl->d_full[tl]);
+      if (tl == TILES - 1) {
+        grp0 = grp;
+        phase0 = phase;
       }
     }
-    if (ok) mma_commit(&ctl->d_full);
   }
   // All MMAs this thread issued must finish before TMEM is freed.
   mma_commit(&ctl->mma_done[ROLE]);
   mbar_wait_drain(&ctl->mma_done[ROLE], 0, 200000000ull);
 }
 
-template <int K>
-__global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_constant__ TcParams p) {
-  using C = Cfg<K>;
+template <int K, int TILES>
+__global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(const __grid_constant__ TcParams p) {
+  using C = Cfg<K, TILES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + C::OFF_CTRL);
@@ -273,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
   const int s_lo = g * j.L;
   const int n = min(j.L, j.S - s_lo);
   const int nsteps = n - 1 + (j.fin ? 1 : 0);
-  const int v0 = blockIdx.x * VT;
+  const int vbase = blockIdx.x * (TILES * VT);
   const bool fwd = j.direction == 0;
   auto seg_of = [&](int step) { return fwd ? s_lo + step : s_lo + n - 1 - step; };
 #ifdef QLA_TRACE
@@ -290,12 +310,14 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       mbar_init(&ctl->a_full[i], 8);   // both splitter warpgroups fill one chunk of the group
       mbar_init(&ctl->a_empty[i], 3);  // one commit per issuing thread
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&ctl->h_full[i], 1);
-      mbar_init(&ctl->h_empty[i], 8);
+    for (int tl = 0; tl < TILES; ++tl) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&ctl->h_full[tl][i], 1);
+        mbar_init(&ctl->h_empty[tl][i], 8);  // the tile's epilogue warps
+      }
+      mbar_init(&ctl->x_ready[tl], 8);
+      mbar_init(&ctl->d_full[tl], 3);
     }
-    mbar_init(&ctl->x_ready, 8);
-    mbar_init(&ctl->d_full, 3);
     mbar_init(&ctl->never, 1);
     for (int i = 0; i < 3; ++i) mbar_init(&ctl->mma_done[i], 1);
     ctl->abort = 0;
@@ -319,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       if (p.has_h) prefetch_tensormap(&p.map_h);
       if (j.out) prefetch_tensormap(&p.map_out);
       uint32_t mit = 0;
-      int hissued = 0;
+      int hissued[TILES] = {};
       bool ok = true;
       const int hrows = j.layout == 0 ? K : j.V;  // rows of one state in the 2-D view of H
       for (int step = 0; step < nsteps && ok; ++step) {
@@ -327,14 +349,19 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
         const int64_t mrow0 = ((int64_t)chain * j.S + seg) * K;
         if (p.has_h) {
           const int slot = step & 1;
-          if (!(ok = mbar_wait(&ctl->h_empty[slot], ((step >> 1) & 1) ^ 1, wc))) break;
-          mbar_arrive_expect_tx(&ctl->h_full[slot], C::TILE);
           const int64_t hrow0 = ((int64_t)chain * j.S + seg) * hrows;
-          if (j.layout == 0)
-            tma_load_2d(smem + C::OFF_H + slot * C::TILE, &p.map_h, v0, (int32_t)hrow0, &ctl->h_full[slot]);
-          else
-            tma_load_2d(smem + C::OFF_H + slot * C::TILE, &p.map_h, 0, (int32_t)(hrow0 + v0), &ctl->h_full[slot]);
-          ++hissued;
+          for (int tl = 0; tl < TILES && ok; ++tl) {
+            if (!(ok = mbar_wait(&ctl->h_empty[tl][slot], ((step >> 1) & 1) ^ 1, wc))) break;
+            mbar_arrive_expect_tx(&ctl->h_full[tl][slot], C::TILE);
+            uint8_t* dst = smem + C::OFF_H + (tl * 2 + slot) * C::TILE;
+            const int v0 = vbase + tl * VT;
+            if (j.layout == 0)
+              tma_load_2d(dst, &p.map_h, v0, (int32_t)hrow0, &ctl->h_full[tl][slot]);
+            else
+              tma_load_2d(dst, &p.map_h, 0, (int32_t)(hrow0 + v0), &ctl->h_full[tl][slot]);
+            ++hissued[tl];
+          }
+          if (!ok) break;
           QLA_TR(0, step, 0, 0);
         }
         for (int c = 0; c < C::CPS; ++c, ++mit) {
@@ -356,23 +383,24 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
         const uint32_t uses = mit > (uint32_t)s ? (mit - 1 - s) / C::NM + 1 : 0;
         if (uses) mbar_wait_drain(&ctl->m_full[s], (uses - 1) & 1, drain);
       }
-      for (int s = 0; s < 2; ++s) {
-        const int uses = hissued > s ? (hissued - 1 - s) / 2 + 1 : 0;
-        if (uses) mbar_wait_drain(&ctl->h_full[s], (uses - 1) & 1, drain);
-      }
+      for (int tl = 0; tl < TILES; ++tl)
+        for (int s = 0; s < 2; ++s) {
+          const int uses = hissued[tl] > s ? (hissued[tl] - 1 - s) / 2 + 1 : 0;
+          if (uses) mbar_wait_drain(&ctl->h_full[tl][s], (uses - 1) & 1, drain);
+        }
     }
     __syncwarp();
   } else if (warp <= 3) {
     // ------------------------------------------------------------ mma issuers
     if (lane == 0) {
 #ifdef QLA_TRACE
-      if (warp == 1) mma_role<K, 0>(j, ctl, smem, tmem, nsteps, wc, tr);
-      else if (warp == 2) mma_role<K, 1>(j, ctl, smem, tmem, nsteps, wc, tr);
-      else mma_role<K, 2>(j, ctl, smem, tmem, nsteps, wc, tr);
+      if (warp == 1) mma_role<K, TILES, 0>(ctl, smem, tmem, nsteps, wc, tr);
+      else if (warp == 2) mma_role<K, TILES, 1>(ctl, smem, tmem, nsteps, wc, tr);
+      else mma_role<K, TILES, 2>(ctl, smem, tmem, nsteps, wc, tr);
 #else
-      if (warp == 1) mma_role<K, 0>(j, ctl, smem, tmem, nsteps, wc);
-      else if (warp == 2) mma_role<K, 1>(j, ctl, smem, tmem, nsteps, wc);
-      else mma_role<K, 2>(j, ctl, smem, tmem, nsteps, wc);
+      if (warp == 1) mma_role<K, TILES, 0>(ctl, smem, tmem, nsteps, wc);
+      else if (warp == 2) mma_role<K, TILES, 1>(ctl, smem, tmem, nsteps, wc);
+      else mma_role<K, TILES, 2>(ctl, smem, tmem, nsteps, wc);
 #endif
     }
     __syncwarp();
@@ -392,38 +420,43 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       if (!(ok = warp_wait(&ctl->m_full[stage], mphase, wc))) break;
       QLA_TR(2, step, 0, c);
       const uint8_t* chunk = smem + C::OFF_M + stage * kChunkBytes;
-      float x[32];
-      if (fwd) {  // row t of a [128][32] tile, 16-byte pieces swizzled by (t & 7)
-        const uint8_t* row = chunk + t * 128;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 v = *reinterpret_cast<const float4*>(row + ((q ^ (t & 7)) << 4));
-          x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
-        }
-      } else {    // column t of a [32][128] tile
-        const float* col = reinterpret_cast<const float*>(chunk) + t;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) x[k] = col[k * 128];
-      }
-      if (p.release != 2) {  // the slot's last ordinary read is done: release it
-        release_fence(p.release);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->m_empty[stage]);
-      }
       const int aslot = mit % C::NA, agrp = aslot >> 1;
       const uint32_t aphase = (uint32_t)(mit / C::NA) & 1;
-      if (!(ok = warp_wait(&ctl->a_empty[agrp], aphase ^ 1, wc))) break;
-      QLA_TR(2, step, 1, c);
-      tc_fence_after();
       const uint32_t a = tmem + lane_off + C::ACOL + aslot * 64;
+      // Two 16-column halves: read (ordinary shared loads), then split and
+      // store to TMEM.  The slot is released after the second half's read.
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
+        float x[16];
+        if (fwd) {  // row t of a [128][32] tile, 16-byte pieces swizzled by (t & 7)
+          const uint8_t* row = chunk + t * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 v = *reinterpret_cast<const float4*>(row + (((4 * half + q) ^ (t & 7)) << 4));
+            x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
+          }
+        } else {    // column t of a [32][128] tile
+          const float* col = reinterpret_cast<const float*>(chunk) + t + 16 * half * 128;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) x[k] = col[k * 128];
+        }
+        if (half == 1 && p.release != 2) {  // the slot's last ordinary read is done: release it
+          release_fence(p.release);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->m_empty[stage]);
+        }
+        if (half == 0) {
+          if (!(ok = warp_wait(&ctl->a_empty[agrp], aphase ^ 1, wc))) break;
+          QLA_TR(2, step, 1, c);
+          tc_fence_after();
+        }
         uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) split_tf32(x[16 * half + k], hi[k], lo[k]);
+        for (int k = 0; k < 16; ++k) split_tf32(x[k], hi[k], lo[k]);
         tmem_st16(a + 16 * half, hi);
         tmem_st16(a + 32 + 16 * half, lo);
       }
+      if (!ok) break;
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -440,14 +473,19 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int e = (warp - 12) >> 2;                  // column half: columns [16e, 16e + 16) of the tile
+    const int ew = warp - 12;
+    const int tl = ew >> 3;                          // tile
+    const int e = (ew >> 2) & 1;                     // column half of the tile: [16e, 16e + 16)
     const int wq = warp & 3;
     const int t = 32 * wq + lane;                    // output row within a 128-row block = TMEM lane
     const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
     const int V = j.V;
     const int c0 = e * EC;
-    uint8_t* bhi = smem + C::OFF_BHI;
-    uint8_t* blo = smem + C::OFF_BLO;
+    const int v0 = vbase + tl * VT;
+    uint8_t* bhi = smem + C::OFF_BHI + tl * C::TILE;
+    uint8_t* blo = smem + C::OFF_BLO + tl * C::TILE;
+    uint64_t* x_ready = &ctl->x_ready[tl];
+    uint64_t* d_full = &ctl->d_full[tl];
     float y[C::HALVES][EC];
     int out_count = 0;
     bool ok = true;
@@ -479,9 +517,10 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       const int b = out_count % C::NOUT;
       if (lane == 0) bulk_wait_read<C::NOUT - 1>();
       __syncwarp();
+      uint8_t* stg_base = smem + C::OFF_OUT + (tl * C::NOUT + b) * C::TILE;
 #pragma unroll
       for (int h = 0; h < C::HALVES; ++h) {
-        float* stg = reinterpret_cast<float*>(smem + C::OFF_OUT + b * C::TILE + ((h * 2 + e) * 4 + wq) * 2048);
+        float* stg = reinterpret_cast<float*>(stg_base + ((h * 2 + e) * 4 + wq) * 2048);
         if (j.layout == 0) {  // [32 rows][16 floats], 64-byte swizzle: 16-byte piece q of row r at q ^ ((r/2)%4)
 #pragma unroll
           for (int q = 0; q < EC / 4; ++q)
@@ -497,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       if (lane == 0) {
 #pragma unroll
         for (int h = 0; h < C::HALVES; ++h) {
-          const uint8_t* stg = smem + C::OFF_OUT + b * C::TILE + ((h * 2 + e) * 4 + wq) * 2048;
+          const uint8_t* stg = stg_base + ((h * 2 + e) * 4 + wq) * 2048;
           if (j.layout == 0)
             tma_store_2d(&p.map_out, stg, v0 + c0,
                          (int32_t)(((int64_t)chain * j.S + seg) * K + 128 * h + 32 * wq));
@@ -537,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
     // columns), in pairs, round-to-nearest: big chains first, then the small.
     auto drain_add = [&](int h, float (&acc)[EC]) {
       float a[16], b[16];
-      const uint32_t base = tmem + lane_off + (uint32_t)(h * C::NQ * VT + c0);
+      const uint32_t base = tmem + lane_off + (uint32_t)((tl * C::HALVES + h) * C::NQ * VT + c0);
 #pragma unroll
       for (int q = 0; q < C::NQ; q += 2) {
         tmem_ld16(base + q * VT, a);
@@ -551,19 +590,19 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
     if (nsteps > 0) {  // X_0 -> B operand first: the first step's MMAs wait on it
       write_b();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->x_ready);
+      if (lane == 0) mbar_arrive(x_ready);
     }
     if (j.out) {
-      if (p.in_place && p.has_h && nsteps > 0) ok = warp_wait(&ctl->h_full[0], 0, wc);
+      if (p.in_place && p.has_h && nsteps > 0) ok = warp_wait(&ctl->h_full[tl][0], 0, wc);
       if (ok) store_out(seg_of(0));
     }
     for (int step = 0; step < nsteps && ok; ++step) {
       // H_j into the accumulator registers first: it does not depend on the MMAs
       const int slot = step & 1;
       if (p.has_h) {
-        if (!(ok = warp_wait(&ctl->h_full[slot], (step >> 1) & 1, wc))) break;
+        if (!(ok = warp_wait(&ctl->h_full[tl][slot], (step >> 1) & 1, wc))) break;
         QLA_TR(3, step, 2, 0);
-        const uint8_t* ht = smem + C::OFF_H + slot * C::TILE;
+        const uint8_t* ht = smem + C::OFF_H + (tl * 2 + slot) * C::TILE;
 #pragma unroll
         for (int h = 0; h < C::HALVES; ++h) {
           const int k = t + 128 * h;
@@ -583,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
         if (p.release != 2) {  // the h slot's last ordinary read is done: release it
           release_fence(p.release);
           __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl->h_empty[slot]);
+          if (lane == 0) mbar_arrive(&ctl->h_empty[tl][slot]);
         }
       } else {
 #pragma unroll
@@ -591,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
 #pragma unroll
           for (int c = 0; c < EC; ++c) y[h][c] = 0.f;
       }
-      uint64_t* dbar = (p.stall_test && step == 0) ? &ctl->never : &ctl->d_full;
+      uint64_t* dbar = (p.stall_test && step == 0) ? &ctl->never : d_full;
       if (!(ok = warp_wait(dbar, step & 1, wc))) break;
       QLA_TR(3, step, 1, 0);
       tc_fence_after();
@@ -603,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
         QLA_TR(3, step, 6, 0);
         tc_fence_before();  // the chains have been read (wait::ld in drain_add)
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->x_ready);
+        if (lane == 0) mbar_arrive(x_ready);
         QLA_TR(3, step, 4, 0);
       } else if (j.fin) {
         float* F = j.fin + u * j.fin_unit_stride;
@@ -623,13 +662,13 @@ __global__ void __launch_bounds__(kThreads, 1) seq_tc_kernel(const __grid_consta
       }
       if (step + 1 < n && j.out) {
         if (p.in_place && p.has_h && step + 1 < nsteps)
-          if (!(ok = warp_wait(&ctl->h_full[(step + 1) & 1], ((step + 1) >> 1) & 1, wc))) break;
+          if (!(ok = warp_wait(&ctl->h_full[tl][(step + 1) & 1], ((step + 1) >> 1) & 1, wc))) break;
         store_out(seg_of(step + 1));
         QLA_TR(3, step, 3, 0);
       }
       if (p.has_h && p.release == 2) {
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->h_empty[slot]);
+        if (lane == 0) mbar_arrive(&ctl->h_empty[tl][slot]);
       }
     }
     if (lane == 0) bulk_wait_all();
@@ -679,10 +718,10 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   return r == CUDA_SUCCESS;
 }
 
-template <int K>
+template <int K, int TILES>
 cudaError_t launch_k(const SeqJob& j, int release, unsigned int* status, uint64_t limit_ns, int stall_test,
                      cudaStream_t stream) {
-  using C = Cfg<K>;
+  using C = Cfg<K, TILES>;
   TcParams p;
   memset(&p, 0, sizeof p);
   p.job = j;
@@ -705,11 +744,11 @@ cudaError_t launch_k(const SeqJob& j, int release, unsigned int* status, uint64_
   const bool fwd = j.direction == 0;
   if (!make_map(&p.map_m, j.M, states * K, K, fwd ? 32 : 128, fwd ? 128 : 32, fwd ? 128 : 0))
     return cudaErrorInvalidValue;
-  auto kern = seq_tc_kernel<K>;
+  auto kern = seq_tc_kernel<K, TILES>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid(j.V / VT, j.nchains * j.G);
-  kern<<<grid, kThreads, C::SMEM, stream>>>(p);
+  dim3 grid(j.V / (TILES * VT), j.nchains * j.G);
+  kern<<<grid, 32 * C::WARPS, C::SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -733,8 +772,11 @@ cudaError_t launch_seq_tc(const SeqJob& job, int release, unsigned int* status, 
   // chains must be packed back to back (H and out are absent in scan phase 1a).
   if ((job.H || job.out) && job.h_chain_stride != (int64_t)job.S * job.K * job.V) return cudaErrorInvalidValue;
   if (job.m_chain_stride != (int64_t)job.S * job.K * job.K) return cudaErrorInvalidValue;
-  return job.K == 128 ? launch_k<128>(job, release, status, limit_ns, stall_test, stream)
-                      : launch_k<256>(job, release, status, limit_ns, stall_test, stream);
+  // One column tile per CTA.  (Two tiles per CTA, with tile 0's epilogue
+  // overlapping tile 1's MMAs, measured slower on the 32-head K=V=128 S=8
+  // workload: 27.6 us against 19.9 us per call.)
+  if (job.K == 256) return launch_k<256, 1>(job, release, status, limit_ns, stall_test, stream);
+  return launch_k<128, 1>(job, release, status, limit_ns, stall_test, stream);
 }
 
 }  // namespace qla
