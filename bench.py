@@ -406,6 +406,55 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args):
+    """Low batch*heads sweep (B=1, K=V=128, 0.99*orthogonal M): the sequential
+    kernel against the group scan, per (heads, S), forward kv and reverse vk.
+    One JSON line per point; not the headline metric."""
+    import torch
+
+    import linear_attention_context_gb300 as qla
+    import qla_inputs as qi
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream(dev)
+    for heads in qi.SWEEP_HEADS:
+        for S_ in qi.SWEEP_S:
+            c = qi.sweep_case(heads, S_)
+            for layout, direction in (("kv", "fwd"), ("vk", "rev")):
+                H, M, h0 = qi.make_inputs(c, layout)
+                Hd, Md, h0d = (torch.from_numpy(a).to(dev) for a in (H, M, h0))
+                out = torch.empty_like(Hd)
+                times = {}
+                for variant in ("seq", "scan"):
+                    def call():
+                        qla.cp_correct(Hd, Md, h0d, out, layout=layout, direction=direction, variant=variant,
+                                       stream=stream)
+                    with torch.cuda.stream(stream):
+                        for _ in range(3):
+                            call()
+                        g = torch.cuda.CUDAGraph()
+                        with torch.cuda.graph(g, stream=stream):
+                            for _ in range(10):
+                                call()
+                    stream.synchronize()
+                    for _ in range(3):
+                        g.replay()
+                    stream.synchronize()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    with torch.cuda.stream(stream):
+                        e0.record(stream)
+                        for _ in range(args.sweep_reps):
+                            g.replay()
+                        e1.record(stream)
+                    stream.synchronize()
+                    times[variant] = e0.elapsed_time(e1) * 1e3 / (10 * args.sweep_reps)
+                auto = qla.resolve(1, heads, S_, 128, 128, layout)[0]
+                print(json.dumps({"sweep": {"heads": heads, "S": S_, "layout": layout, "direction": direction},
+                                  "us_per_call": {k: round(v, 2) for k, v in times.items()},
+                                  "auto": auto, "bytes_per_call": algorithmic_bytes(heads, S_, 128, 128)}),
+                      flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -421,9 +470,13 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-check", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="time sequential vs scan over the low batch*heads sweep")
+    ap.add_argument("--sweep-reps", type=int, default=20)
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_ours(args)
 

@@ -132,7 +132,9 @@ struct Cfg {
   static constexpr int NAG = NA / 2;              // ... in groups of two chunks, one barrier pair per group
   static constexpr int NM = TILES == 2 ? 4 : (K == 128 ? 6 : 4);  // m ring stages
   static constexpr int NOUT = (TILES == 1 && K == 128) ? 2 : 1;    // out staging buffers per tile
-  static constexpr int WARPS = 12 + 8 * TILES;    // WG0 + 2 splitter WGs + 2 epilogue WGs per tile
+  static constexpr int NSG = 2;                   // splitter warpgroups (take chunks round-robin)
+  static constexpr int WARPS = 4 + 4 * NSG + 8 * TILES;  // WG0 + splitter WGs + 2 epilogue WGs per tile
+  static constexpr int EPI_WARP0 = 4 + 4 * NSG;   // first epilogue warp
   static constexpr uint32_t TILE = (uint32_t)K * VT * 4;  // one state tile (bytes)
   static constexpr uint32_t OFF_M = 0;
   static constexpr uint32_t OFF_H = OFF_M + NM * kChunkBytes;       // [TILES][2 slots]
@@ -146,6 +148,11 @@ struct Cfg {
   static_assert(ACOL + NA * 64 <= kTmemCols, "TMEM columns");
   static_assert(CPS % 2 == 0 && NAG >= 1 && NAG <= 4, "chunks per step, A groups");
   static_assert(TILES == 1 || K == 128, "two tiles only for K = 128");
+  // A splitter group may wait on a ring slot only for a use whose previous
+  // use was its own: otherwise, while another group's fill of the previous
+  // use is still in flight, the phase two uses back (same parity) would
+  // satisfy its parity wait.  So each ring depth is a multiple of NSG.
+  static_assert(NM % NSG == 0 && NA % NSG == 0, "ring depths must be multiples of the splitter groups");
 };
 
 struct TcParams {
@@ -162,7 +169,7 @@ struct TcParams {
 };
 
 struct Ctrl {
-  uint64_t m_full[6], m_empty[6];
+  uint64_t m_full[8], m_empty[8];
   uint64_t a_full[4], a_empty[4];
   uint64_t h_full[2][2], h_empty[2][2];  // [tile][slot]
   uint64_t x_ready[2], d_full[2];        // [tile]
@@ -307,7 +314,7 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
       mbar_init(&ctl->m_empty[i], 4);
     }
     for (int i = 0; i < C::NAG; ++i) {
-      mbar_init(&ctl->a_full[i], 8);   // both splitter warpgroups fill one chunk of the group
+      mbar_init(&ctl->a_full[i], 8);   // two splitter warpgroups fill one chunk each of the group
       mbar_init(&ctl->a_empty[i], 3);  // one commit per issuing thread
     }
     for (int tl = 0; tl < TILES; ++tl) {
@@ -332,6 +339,11 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   WaitCtl wc{&ctl->abort, p.status, p.limit_ns};
+  // Programmatic dependent launch: the set-up above may overlap the previous
+  // kernel's tail; every global access below comes after the wait (no
+  // non-coherent load is hoisted above it: none is used).
+  pdl_launch_dependents();
+  pdl_wait();
   QLA_TR(0, 0, 7, 0);
 
   if (warp == 0) {
@@ -404,16 +416,16 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
 #endif
     }
     __syncwarp();
-  } else if (warp < 12) {
+  } else if (warp < C::EPI_WARP0) {
     // ------------------------------------------------------------ A splitters
-    const int grp = (warp - 4) >> 2;                 // takes chunks grp, grp + 2, grp + 4, ...
+    const int grp = (warp - 4) >> 2;                 // takes chunks grp, grp + NSG, grp + 2 NSG, ...
     const int t = 32 * (warp & 3) + lane;            // A row within the 128-row block = TMEM lane
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const int total = nsteps * C::CPS;
     int stage = grp;
     uint32_t mphase = 0;
     bool ok = true;
-    for (int mit = grp; mit < total && ok; mit += 2) {
+    for (int mit = grp; mit < total && ok; mit += C::NSG) {
       const int step = mit / C::CPS, c = mit % C::CPS;
       (void)step;
       (void)c;
@@ -466,14 +478,14 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->m_empty[stage]);
       }
-      if ((stage += 2) >= C::NM) {
+      if ((stage += C::NSG) >= C::NM) {
         stage -= C::NM;
         mphase ^= 1;
       }
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - 12;
+    const int ew = warp - C::EPI_WARP0;
     const int tl = ew >> 3;                          // tile
     const int e = (ew >> 2) & 1;                     // column half of the tile: [16e, 16e + 16)
     const int wq = warp & 3;
@@ -671,7 +683,9 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
         if (lane == 0) mbar_arrive(&ctl->h_empty[tl][slot]);
       }
     }
-    if (lane == 0) bulk_wait_all();
+    // Shared memory may go once the stores have read it; the grid completes
+    // only after its global writes are performed.
+    if (lane == 0) bulk_wait_read<0>();
     __syncwarp();
   }
 
@@ -747,8 +761,21 @@ cudaError_t launch_k(const SeqJob& j, int release, unsigned int* status, uint64_
   auto kern = seq_tc_kernel<K, TILES>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid(j.V / (TILES * VT), j.nchains * j.G);
-  kern<<<grid, 32 * C::WARPS, C::SMEM, stream>>>(p);
+  // Programmatic stream serialisation: this launch may begin before the
+  // previous kernel on the stream finishes; the kernel waits for it
+  // (griddepcontrol.wait) before touching global memory.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(j.V / (TILES * VT), j.nchains * j.G);
+  cfg.blockDim = dim3(32 * C::WARPS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
