@@ -125,18 +125,6 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// ---------------------------------------------------------------- programmatic dependent launch
-
-// Lets the next kernel on the stream (launched with programmatic stream
-// serialisation) be scheduled before this grid completes.
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Waits until the prerequisite grids have completed and their memory
-// operations are visible; no global access of this grid may precede it.
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void prefetch_tensormap(const void* map) {

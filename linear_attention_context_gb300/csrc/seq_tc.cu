@@ -339,11 +339,6 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   WaitCtl wc{&ctl->abort, p.status, p.limit_ns};
-  // Programmatic dependent launch: the set-up above may overlap the previous
-  // kernel's tail; every global access below comes after the wait (no
-  // non-coherent load is hoisted above it: none is used).
-  pdl_launch_dependents();
-  pdl_wait();
   QLA_TR(0, 0, 7, 0);
 
   if (warp == 0) {
@@ -761,21 +756,10 @@ cudaError_t launch_k(const SeqJob& j, int release, unsigned int* status, uint64_
   auto kern = seq_tc_kernel<K, TILES>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
-  // Programmatic stream serialisation: this launch may begin before the
-  // previous kernel on the stream finishes; the kernel waits for it
-  // (griddepcontrol.wait) before touching global memory.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(j.V / (TILES * VT), j.nchains * j.G);
-  cfg.blockDim = dim3(32 * C::WARPS);
-  cfg.dynamicSmemBytes = C::SMEM;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, p);
-  if (e != cudaSuccess) return e;
+  // (Programmatic dependent launch, letting this set-up overlap the previous
+  // kernel's tail, measured about 1 us slower per call here; not used.)
+  dim3 grid(j.V / (TILES * VT), j.nchains * j.G);
+  kern<<<grid, 32 * C::WARPS, C::SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 
