@@ -455,6 +455,43 @@ def run_sweep(args):
                       flush=True)
 
 
+def run_large(args):
+    """The 4 x 64-head, K=V=256, S=32 workload (6.4 GB of states), forward
+    and reverse kv: one call at a time, CUDA events, after two warm-up calls.
+    Not the headline metric."""
+    import torch
+
+    import linear_attention_context_gb300 as qla
+    import qla_inputs as qi
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    c = qi.WORKLOADS["c3"]
+    H, M, h0 = qi.make_inputs(c, "kv")
+    Hd, Md, h0d = (torch.from_numpy(a).to(dev) for a in (H, M, h0))
+    del H, M
+    out = torch.empty_like(Hd)
+    peak, _ = load_peaks()
+    nbytes = algorithmic_bytes(c.chains, c.S, c.K, c.V)
+    for direction in ("fwd", "rev"):
+        for _ in range(2):
+            qla.cp_correct(Hd, Md, h0d, out, layout="kv", direction=direction)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 5
+        e0.record()
+        for _ in range(reps):
+            qla.cp_correct(Hd, Md, h0d, out, layout="kv", direction=direction)
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        print(json.dumps({"large": {"B": c.B, "heads": c.heads, "K": c.K, "V": c.V, "S": c.S, "layout": "kv",
+                                    "direction": direction},
+                          "us_per_call": round(us, 1), "gbs": round(nbytes / us / 1e3, 1),
+                          "frac_of_measured_hbm": round(nbytes / us / 1e3 / peak, 4),
+                          "algorithmic_bytes": nbytes, "variant_engine": qla.resolve(c.B, c.heads, c.S, c.K, c.V)}),
+              flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -472,11 +509,14 @@ def main():
     ap.add_argument("--skip-check", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="time sequential vs scan over the low batch*heads sweep")
     ap.add_argument("--sweep-reps", type=int, default=20)
+    ap.add_argument("--large", action="store_true", help="time the 4 x 64-head K=V=256 S=32 workload")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
     elif args.sweep:
         run_sweep(args)
+    elif args.large:
+        run_large(args)
     else:
         run_ours(args)
 

@@ -153,11 +153,15 @@ int engine_for(const SeqJob& j, int engine) {
   return engine;
 }
 
+// The scan trades a sequential chain of S-1 steps for about 2L + G steps in
+// three launches whose parallel phases hold tiles * G CTAs.  Measured on
+// GB300 (K = V = 128, tensor-core engine): it wins for S >= 32 with up to
+// 16 column tiles (1.25x - 2.9x) and loses for S <= 8 or 128 tiles.
 int resolve_variant(const Shape& s, int variant, const DeviceInfo* d) {
-  (void)s;
   (void)d;
-  if (variant == QLA_VARIANT_AUTO) return QLA_VARIANT_SEQ;
-  return variant;
+  if (variant != QLA_VARIANT_AUTO) return variant;
+  const int64_t tiles = s.chains() * ((s.V + 31) / 32);
+  return (s.S >= 24 && tiles <= 16) ? QLA_VARIANT_SCAN : QLA_VARIANT_SEQ;
 }
 
 int launch_seq(const SeqJob& j, int engine, int release, const DeviceInfo* d, cudaStream_t stream) {
