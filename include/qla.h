@@ -87,7 +87,7 @@ enum {
 enum {
   QLA_ENGINE_AUTO = 0,    /* tensor-core engine where the shape allows, else SIMT */
   QLA_ENGINE_SIMT = 1,    /* plain FFMA kernel, no TMA: any supported K, V */
-  QLA_ENGINE_WS_SIMT = 2, /* warp-specialised TMA/mbarrier pipeline, FFMA propagate */
+                          /* 2 is not assigned: an engine value of 2 is rejected */
   QLA_ENGINE_TC = 3       /* warp-specialised TMA/mbarrier pipeline, tcgen05 3xTF32 propagate */
 };
 

@@ -142,6 +142,10 @@ int auto_groups(int S) {
   return (S + L - 1) / L;
 }
 
+bool known_engine(int engine) {
+  return engine == QLA_ENGINE_AUTO || engine == QLA_ENGINE_SIMT || engine == QLA_ENGINE_TC;
+}
+
 int resolve_engine(const Shape& s, int engine) {
   if (engine == QLA_ENGINE_AUTO) return tc_supports(s.K, s.V) ? QLA_ENGINE_TC : QLA_ENGINE_SIMT;
   return engine;
@@ -393,7 +397,7 @@ int qla_cp_correct_scan_static(const float* H, const float* M, const float* h_in
   Shape s{B, heads, S, K, V, layout, direction};
   int st = check_args(H, M, h_init, out, final_state, s);
   if (st != QLA_OK) return st;
-  if (engine < QLA_ENGINE_AUTO || engine > QLA_ENGINE_TC) return fail(QLA_ERR_INVALID_ARG, "unknown engine %d", engine);
+  if (!known_engine(engine)) return fail(QLA_ERR_INVALID_ARG, "unknown engine %d", engine);
   if (release < QLA_RELEASE_MEMBAR || release > QLA_RELEASE_NONE)
     return fail(QLA_ERR_INVALID_ARG, "unknown release mode %d", release);
   if (scan_group < 0) return fail(QLA_ERR_INVALID_ARG, "scan_group must be >= 0");
@@ -459,7 +463,7 @@ int qla_cp_correct_ex(const float* H, const float* M, const float* h_init, float
   if (st != QLA_OK) return st;
   if (variant < QLA_VARIANT_AUTO || variant > QLA_VARIANT_SCAN)
     return fail(QLA_ERR_INVALID_ARG, "unknown variant %d", variant);
-  if (engine < QLA_ENGINE_AUTO || engine > QLA_ENGINE_TC) return fail(QLA_ERR_INVALID_ARG, "unknown engine %d", engine);
+  if (!known_engine(engine)) return fail(QLA_ERR_INVALID_ARG, "unknown engine %d", engine);
   if (release < QLA_RELEASE_MEMBAR || release > QLA_RELEASE_NONE)
     return fail(QLA_ERR_INVALID_ARG, "unknown release mode %d", release);
   if (scan_group < 0) return fail(QLA_ERR_INVALID_ARG, "scan_group must be >= 0");

@@ -8,7 +8,6 @@ import numpy as np
 
 # Engines under test.  The tensor-core engine takes the shapes listed in
 # tc_supports(); the others take every supported shape.
-ALL_ENGINES = ("simt", "ws_simt", "tc")
 BUILT_ENGINES = ("simt", "tc")
 
 
@@ -22,8 +21,6 @@ def engines_under_test():
 def engine_supports(engine, K, V):
     if engine == "tc":
         return K in (128, 256) and V % 32 == 0
-    if engine == "ws_simt":
-        return K % 32 == 0 and V % 32 == 0
     return True
 
 
