@@ -10,14 +10,13 @@
 // tcgen05 with fp32 accuracy from three TF32 products:
 //     A X ~= A_hi X_hi + A_hi X_lo + A_lo X_hi,
 // The tensor core reads an fp32 operand as TF32 by cutting its 13 low mantissa
-// bits toward zero (measured).  So every lo part is rounded to the nearest
-// TF32 value before the MMA sees it: a lo cut toward zero is biased (it keeps
-// x's sign), and that bias showed as a coherent shrink of about 2^-20 per
-// step.  A (the propagation matrix) splits as hi = RN_tf32(a),
-// lo = RN_tf32(a - hi); X (the state) uses hi = the raw value, which the
-// tensor core reads exactly as trunc_tf32(x), and lo = RN_tf32(x - trunc(x)).
-// With A's lo of random sign, the dropped A_lo X_lo term (below 2^-21
-// relative) is unbiased, as is the rounding of each lo (below 2^-21).
+// bits toward zero (measured).  Both operands split as hi = RN_tf32(x) and
+// lo = x - hi (exact in fp32), and the MMA reads lo cut toward zero.  With hi
+// rounded to nearest, lo's sign is that of x times an even coin (x rounded
+// down or up), so the cut of lo (below 2^-23 relative to x) and the dropped
+// A_lo X_lo term (below 2^-22) carry no bias.  (With hi = trunc(x) instead,
+// lo keeps x's sign and a cut lo shrank every state coherently, by about
+// 2^-20 per step: measured.)
 //
 // Accumulation: the tensor core also rounds its fp32 accumulator toward zero,
 // so a long chain of MMAs into one accumulator shrinks the result coherently
@@ -113,7 +112,6 @@ namespace {
 using namespace ptx;
 
 constexpr int VT = 32;                          // state columns per tile
-constexpr int EC = 16;                          // state columns per epilogue warpgroup
 constexpr uint32_t kChunkBytes = 128 * 32 * 4;  // one A chunk: 128 rows x 32 columns fp32
 constexpr uint32_t kTmemCols = 512;
 
@@ -125,6 +123,7 @@ struct Cfg {
   static constexpr int HALVES = K / 128;          // 128-row MMA blocks of the output
   static constexpr int KCH = K / 32;              // 32-wide k chunks per block
   static constexpr int CPS = HALVES * KCH;        // chunks per step
+  static constexpr int NI = 3;                    // MMA-issuing warps (one thread each)
   static constexpr int NB = (TILES == 1 && K == 128) ? 4 : 2;  // big-term chains per row block
   static constexpr int NQ = NB + 2;               // chains per row block (+ A_hi X_lo, A_lo X_hi)
   static constexpr uint32_t ACOL = TILES * HALVES * NQ * VT;  // first column of the A ring
@@ -133,8 +132,11 @@ struct Cfg {
   static constexpr int NM = TILES == 2 ? 4 : (K == 128 ? 6 : 4);  // m ring stages
   static constexpr int NOUT = (TILES == 1 && K == 128) ? 2 : 1;    // out staging buffers per tile
   static constexpr int NSG = 2;                   // splitter warpgroups (take chunks round-robin)
-  static constexpr int WARPS = 4 + 4 * NSG + 8 * TILES;  // WG0 + splitter WGs + 2 epilogue WGs per tile
-  static constexpr int EPI_WARP0 = 4 + 4 * NSG;   // first epilogue warp
+  static constexpr int NE = (TILES == 1 && K == 128) ? 4 : 2;  // epilogue warpgroups per tile ...
+  static constexpr int EC = VT / NE;              // ... each owning EC state columns
+  static constexpr int SPL_WARP0 = 1 + NI;        // first splitter warp (after producer + issuers)
+  static constexpr int EPI_WARP0 = SPL_WARP0 + 4 * NSG;  // first epilogue warp
+  static constexpr int WARPS = EPI_WARP0 + 4 * NE * TILES;
   static constexpr uint32_t TILE = (uint32_t)K * VT * 4;  // one state tile (bytes)
   static constexpr uint32_t OFF_M = 0;
   static constexpr uint32_t OFF_H = OFF_M + NM * kChunkBytes;       // [TILES][2 slots]
@@ -193,12 +195,19 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 
 // Nearest TF32 value (ties away from zero) as fp32 bits: add half of the
 // 13-bit tail, then clear the tail; a carry correctly bumps the exponent.
+// (cvt.rna.tf32.f32 gives bit-identical results on GB300 but made the kernel
+// slower: 21.5 against 19.1 us per call.)
 __device__ __forceinline__ uint32_t tf32_rn_bits(float x) { return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u; }
 
-// x = hi + lo + r with hi, lo exact TF32 values and |r| <= 2^-22 |x|.
-__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-  hi = tf32_rn_bits(x);
-  lo = tf32_rn_bits(x - __uint_as_float(hi));
+// Two values at once: hi = RN_tf32(x), lo = x - hi exactly (one packed fma).
+__device__ __forceinline__ void split_tf32x2(float x0, float x1, uint32_t& hi0, uint32_t& hi1, uint32_t& lo0,
+                                             uint32_t& lo1) {
+  hi0 = tf32_rn_bits(x0);
+  hi1 = tf32_rn_bits(x1);
+  const float2 d = __ffma2_rn(make_float2(__uint_as_float(hi0), __uint_as_float(hi1)), make_float2(-1.f, -1.f),
+                              make_float2(x0, x1));
+  lo0 = __float_as_uint(d.x);
+  lo1 = __float_as_uint(d.y);
 }
 
 // The MMAs one issuing thread owes chunk c (k-block kc = c / HALVES, row
@@ -249,8 +258,34 @@ __device__ __forceinline__ void mma_role(Ctrl* ctl, uint8_t* smem, uint32_t tmem
 #pragma unroll
     for (int tl = 0; tl < TILES && ok; ++tl) {
       if (!(ok = mbar_wait(&ctl->x_ready[tl], step & 1, wc))) break;
-      if (ROLE == 0 && tl == 0) QLA_TR(1, step, 0, 0);
+      if (tl == 0) QLA_TR(1, step, 0, ROLE);
       tc_fence_after();
+      if constexpr (TILES == 1 && C::CPS == 4 && C::NAG == 2) {
+        // The A ring holds exactly one step (two pairs).  Pair 1 is usually
+        // split before the step starts: test it without blocking, so that
+        // no poll (which would stall until this thread's queued MMAs have
+        // dispatched) sits between the step's MMAs unless it must.
+        if (!(ok = mbar_wait(&ctl->a_full[0], phase0, wc))) break;
+        const bool pair1_ready = mbar_test_wait(&ctl->a_full[1], phase0);
+        QLA_TR(1, step, 1, 4 * ROLE);
+        tc_fence_after();
+        mma_chunk<K, TILES, ROLE>(0, 0, tmem, tmem + C::ACOL + 0 * 64, dh0[0], dl0[0]);
+        mma_chunk<K, TILES, ROLE>(0, 1, tmem, tmem + C::ACOL + 1 * 64, dh0[0], dl0[0]);
+        mma_commit(&ctl->a_empty[0]);
+        QLA_TR(1, step, 3, 4 * ROLE);
+        if (!pair1_ready) {
+          if (!(ok = mbar_wait(&ctl->a_full[1], phase0, wc))) break;
+          tc_fence_after();
+        }
+        QLA_TR(1, step, 1, 2 + 4 * ROLE);
+        mma_chunk<K, TILES, ROLE>(0, 2, tmem, tmem + C::ACOL + 2 * 64, dh0[0], dl0[0]);
+        mma_chunk<K, TILES, ROLE>(0, 3, tmem, tmem + C::ACOL + 3 * 64, dh0[0], dl0[0]);
+        mma_commit(&ctl->a_empty[1]);
+        mma_commit(&ctl->d_full[0]);
+        QLA_TR(1, step, 3, 2 + 4 * ROLE);
+        phase0 ^= 1;
+        continue;
+      }
       int grp = grp0;
       uint32_t phase = phase0;
       // One wait and one commit per pair of chunks: a barrier poll from this
@@ -260,13 +295,15 @@ __device__ __forceinline__ void mma_role(Ctrl* ctl, uint8_t* smem, uint32_t tmem
       for (int c = 0; c < C::CPS; c += 2) {
         if (tl == 0) {
           if (!(ok = mbar_wait(&ctl->a_full[grp], phase, wc))) break;
-          if (ROLE == 0) QLA_TR(1, step, 1, c);
+          QLA_TR(1, step, 1, c + 4 * ROLE);
           tc_fence_after();
         }
         mma_chunk<K, TILES, ROLE>(tl, c, tmem, tmem + C::ACOL + (2 * grp) * 64, dh0[tl], dl0[tl]);
+        if (tl == 0) QLA_TR(1, step, 2, c + 4 * ROLE);
         mma_chunk<K, TILES, ROLE>(tl, c + 1, tmem, tmem + C::ACOL + (2 * grp + 1) * 64, dh0[tl], dl0[tl]);
+        if (tl == 0) QLA_TR(1, step, 2, c + 1 + 4 * ROLE);
         if (tl == TILES - 1) mma_commit(&ctl->a_empty[grp]);
-        if (ROLE == 0 && tl == 0) QLA_TR(1, step, 3, c);
+        if (tl == 0) QLA_TR(1, step, 3, c + 4 * ROLE);
         if (++grp == C::NAG) {
           grp = 0;
           phase ^= 1;
@@ -305,28 +342,68 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
   auto seg_of = [&](int step) { return fwd ? s_lo + step : s_lo + n - 1 - step; };
 #ifdef QLA_TRACE
   const bool tr = blockIdx.x == 0 && blockIdx.y == 0 &&
-                  (threadIdx.x == 0 || threadIdx.x == 32 || threadIdx.x == 128 || threadIdx.x == 384);
+                  ((threadIdx.x & 31) == 0 &&
+                   (warp <= C::NI || warp == C::SPL_WARP0 || warp == C::SPL_WARP0 + 4 || warp == C::EPI_WARP0 ||
+                    warp == C::WARPS - 1));
+  const int trc = warp == C::WARPS - 1 ? 1 : 0;  // second traced epilogue warp
+  (void)trc;
 #endif
 
+  // Epilogue warps load the initial state before set-up, so its global-memory
+  // latency overlaps barrier initialisation and the TMEM allocation.
+  constexpr int EC = C::EC;
+  float y[C::HALVES][EC];
+  if (warp >= C::EPI_WARP0) {
+    const int e = ((warp - C::EPI_WARP0) >> 2) % C::NE;
+    const int t = 32 * (warp & 3) + lane;
+    const int v0 = vbase + ((warp - C::EPI_WARP0) / (4 * C::NE)) * VT;
+    const int c0 = e * EC;
+    const int V = j.V;
+#pragma unroll
+    for (int h = 0; h < C::HALVES; ++h) {
+      const int k = t + 128 * h;
+      if (j.init_mode == kInitPointer) {
+        const float* src = j.init + u * j.init_unit_stride;
+        if (j.layout == 0) {
+#pragma unroll
+          for (int q = 0; q < EC / 4; ++q) {
+            const float4 v = *reinterpret_cast<const float4*>(src + (int64_t)k * V + v0 + c0 + 4 * q);
+            y[h][4 * q] = v.x; y[h][4 * q + 1] = v.y; y[h][4 * q + 2] = v.z; y[h][4 * q + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < EC; ++c) y[h][c] = src[(int64_t)(v0 + c0 + c) * K + k];
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < EC; ++c) y[h][c] = (j.init_mode == kInitIdentity && k == v0 + c0 + c) ? 1.f : 0.f;
+      }
+    }
+  }
+
   if (threadIdx.x == 0) {
+    // The first TMA of a map fetches its descriptor: start that before set-up.
+    prefetch_tensormap(&p.map_m);
+    if (p.has_h) prefetch_tensormap(&p.map_h);
+    if (j.out) prefetch_tensormap(&p.map_out);
     for (int i = 0; i < C::NM; ++i) {
       mbar_init(&ctl->m_full[i], 1);
       mbar_init(&ctl->m_empty[i], 4);
     }
     for (int i = 0; i < C::NAG; ++i) {
       mbar_init(&ctl->a_full[i], 8);   // two splitter warpgroups fill one chunk each of the group
-      mbar_init(&ctl->a_empty[i], 3);  // one commit per issuing thread
+      mbar_init(&ctl->a_empty[i], C::NI);  // one commit per issuing thread
     }
     for (int tl = 0; tl < TILES; ++tl) {
       for (int i = 0; i < 2; ++i) {
         mbar_init(&ctl->h_full[tl][i], 1);
-        mbar_init(&ctl->h_empty[tl][i], 8);  // the tile's epilogue warps
+        mbar_init(&ctl->h_empty[tl][i], 4 * C::NE);  // the tile's epilogue warps
       }
-      mbar_init(&ctl->x_ready[tl], 8);
-      mbar_init(&ctl->d_full[tl], 3);
+      mbar_init(&ctl->x_ready[tl], 4 * C::NE);
+      mbar_init(&ctl->d_full[tl], C::NI);
     }
     mbar_init(&ctl->never, 1);
-    for (int i = 0; i < 3; ++i) mbar_init(&ctl->mma_done[i], 1);
+    for (int i = 0; i < C::NI; ++i) mbar_init(&ctl->mma_done[i], 1);
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -344,9 +421,6 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      prefetch_tensormap(&p.map_m);
-      if (p.has_h) prefetch_tensormap(&p.map_h);
-      if (j.out) prefetch_tensormap(&p.map_out);
       uint32_t mit = 0;
       int hissued[TILES] = {};
       bool ok = true;
@@ -397,7 +471,7 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
         }
     }
     __syncwarp();
-  } else if (warp <= 3) {
+  } else if (warp <= C::NI) {
     // ------------------------------------------------------------ mma issuers
     if (lane == 0) {
 #ifdef QLA_TRACE
@@ -413,7 +487,7 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
     __syncwarp();
   } else if (warp < C::EPI_WARP0) {
     // ------------------------------------------------------------ A splitters
-    const int grp = (warp - 4) >> 2;                 // takes chunks grp, grp + NSG, grp + 2 NSG, ...
+    const int grp = (warp - C::SPL_WARP0) >> 2;      // takes chunks grp, grp + NSG, grp + 2 NSG, ...
     const int t = 32 * (warp & 3) + lane;            // A row within the 128-row block = TMEM lane
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const int total = nsteps * C::CPS;
@@ -459,7 +533,7 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
         }
         uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) split_tf32(x[k], hi[k], lo[k]);
+        for (int k = 0; k < 16; k += 2) split_tf32x2(x[k], x[k + 1], hi[k], hi[k + 1], lo[k], lo[k + 1]);
         tmem_st16(a + 16 * half, hi);
         tmem_st16(a + 32 + 16 * half, lo);
       }
@@ -481,8 +555,8 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
   } else {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - C::EPI_WARP0;
-    const int tl = ew >> 3;                          // tile
-    const int e = (ew >> 2) & 1;                     // column half of the tile: [16e, 16e + 16)
+    const int tl = ew / (4 * C::NE);                 // tile
+    const int e = (ew >> 2) % C::NE;                 // column group of the tile: [EC e, EC e + EC)
     const int wq = warp & 3;
     const int t = 32 * wq + lane;                    // output row within a 128-row block = TMEM lane
     const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
@@ -493,33 +567,13 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
     uint8_t* blo = smem + C::OFF_BLO + tl * C::TILE;
     uint64_t* x_ready = &ctl->x_ready[tl];
     uint64_t* d_full = &ctl->d_full[tl];
-    float y[C::HALVES][EC];
     int out_count = 0;
     bool ok = true;
+#ifdef QLA_TRACE
+    int step_tr = 0;
+#endif
 
-    // initial state
-#pragma unroll
-    for (int h = 0; h < C::HALVES; ++h) {
-      const int k = t + 128 * h;
-      if (j.init_mode == kInitPointer) {
-        const float* src = j.init + u * j.init_unit_stride;
-        if (j.layout == 0) {
-#pragma unroll
-          for (int q = 0; q < EC / 4; ++q) {
-            const float4 v = *reinterpret_cast<const float4*>(src + (int64_t)k * V + v0 + c0 + 4 * q);
-            y[h][4 * q] = v.x; y[h][4 * q + 1] = v.y; y[h][4 * q + 2] = v.z; y[h][4 * q + 3] = v.w;
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < EC; ++c) y[h][c] = src[(int64_t)(v0 + c0 + c) * K + k];
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < EC; ++c) y[h][c] = (j.init_mode == kInitIdentity && k == v0 + c0 + c) ? 1.f : 0.f;
-      }
-    }
-
-    // out[seg] <- y through per-warp staging (2 KB per row block) and TMA stores
+    // out[seg] <- y through per-warp staging (32 x EC floats per row block) and TMA stores
     auto store_out = [&](int seg) {
       const int b = out_count % C::NOUT;
       if (lane == 0) bulk_wait_read<C::NOUT - 1>();
@@ -527,13 +581,14 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
       uint8_t* stg_base = smem + C::OFF_OUT + (tl * C::NOUT + b) * C::TILE;
 #pragma unroll
       for (int h = 0; h < C::HALVES; ++h) {
-        float* stg = reinterpret_cast<float*>(stg_base + ((h * 2 + e) * 4 + wq) * 2048);
-        if (j.layout == 0) {  // [32 rows][16 floats], 64-byte swizzle: 16-byte piece q of row r at q ^ ((r/2)%4)
+        float* stg = reinterpret_cast<float*>(stg_base + ((h * C::NE + e) * 4 + wq) * (32 * EC * 4));
+        if (j.layout == 0) {  // [32 rows][EC floats], (4 EC)-byte swizzle: 16-byte piece q of row r at
+                              // q ^ ((r EC / 32) % (EC / 4))
 #pragma unroll
           for (int q = 0; q < EC / 4; ++q)
-            *reinterpret_cast<float4*>(stg + lane * EC + 4 * (q ^ ((lane >> 1) & 3))) =
+            *reinterpret_cast<float4*>(stg + lane * EC + 4 * (q ^ ((lane * EC / 32) & (EC / 4 - 1)))) =
                 make_float4(y[h][4 * q], y[h][4 * q + 1], y[h][4 * q + 2], y[h][4 * q + 3]);
-        } else {              // [16 rows][32 floats]: column `lane`
+        } else {              // [EC rows][32 floats]: column `lane`
 #pragma unroll
           for (int c = 0; c < EC; ++c) stg[c * 32 + lane] = y[h][c];
         }
@@ -543,7 +598,7 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
       if (lane == 0) {
 #pragma unroll
         for (int h = 0; h < C::HALVES; ++h) {
-          const uint8_t* stg = stg_base + ((h * 2 + e) * 4 + wq) * 2048;
+          const uint8_t* stg = stg_base + ((h * C::NE + e) * 4 + wq) * (32 * EC * 4);
           if (j.layout == 0)
             tma_store_2d(&p.map_out, stg, v0 + c0,
                          (int32_t)(((int64_t)chain * j.S + seg) * K + 128 * h + 32 * wq));
@@ -567,30 +622,49 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
 #pragma unroll
         for (int m = 0; m < 8; ++m) rowoff[m] = kb + (uint32_t)m * 128 + ((piece ^ (uint32_t)m) << 4);
 #pragma unroll
-        for (int c = 0; c < EC; ++c) {  // n = c0 + c; c0 is a multiple of 8
-          const uint32_t off = rowoff[c & 7] + (uint32_t)(c >> 3) * 1024;
-          // hi: the raw value (the tensor core reads it as trunc_tf32(y), exactly);
-          // lo: y - trunc_tf32(y), rounded to the nearest TF32 value.
-          const float yv = y[h][c];
-          *reinterpret_cast<float*>(bhi + off) = yv;
-          *reinterpret_cast<uint32_t*>(blo + off) = tf32_rn_bits(yv - __uint_as_float(__float_as_uint(yv) & 0xFFFFE000u));
+        for (int c = 0; c < EC; c += 2) {  // n = c0 + c; c0 is a multiple of 8
+          uint32_t h0, h1, l0, l1;
+          split_tf32x2(y[h][c], y[h][c + 1], h0, h1, l0, l1);
+          const uint32_t off0 = rowoff[c & 7] + (uint32_t)(c >> 3) * 1024;
+          const uint32_t off1 = rowoff[(c + 1) & 7] + (uint32_t)((c + 1) >> 3) * 1024;
+          *reinterpret_cast<uint32_t*>(bhi + off0) = h0;
+          *reinterpret_cast<uint32_t*>(blo + off0) = l0;
+          *reinterpret_cast<uint32_t*>(bhi + off1) = h1;
+          *reinterpret_cast<uint32_t*>(blo + off1) = l1;
         }
       }
+      QLA_TR(3, step_tr, 7, trc);
       fence_proxy_async_smem();  // generic writes -> read by tcgen05.mma (async proxy)
     };
 
-    // acc += the accumulator chains of one 128-row block (this warpgroup's 16
+    // acc += the accumulator chains of one 128-row block (this warpgroup's EC
     // columns), in pairs, round-to-nearest: big chains first, then the small.
+    // (Loading all chains before a single wait measured slower.)
     auto drain_add = [&](int h, float (&acc)[EC]) {
-      float a[16], b[16];
+      float a[EC], b[EC];
       const uint32_t base = tmem + lane_off + (uint32_t)((tl * C::HALVES + h) * C::NQ * VT + c0);
 #pragma unroll
-      for (int q = 0; q < C::NQ; q += 2) {
-        tmem_ld16(base + q * VT, a);
-        tmem_ld16(base + (q + 1) * VT, b);
+      for (int q = 0; q + 1 < C::NQ; q += 2) {
+        tmem_ld<EC>(base + q * VT, a);
+        tmem_ld<EC>(base + (q + 1) * VT, b);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < EC; ++c) acc[c] += a[c] + b[c];
+        for (int c = 0; c < EC; c += 2) {  // acc += a + b, two columns per packed add
+          const float2 sab = __fadd2_rn(make_float2(a[c], a[c + 1]), make_float2(b[c], b[c + 1]));
+          const float2 r = __fadd2_rn(make_float2(acc[c], acc[c + 1]), sab);
+          acc[c] = r.x;
+          acc[c + 1] = r.y;
+        }
+      }
+      if constexpr (C::NQ % 2 == 1) {  // the last (small) chain alone
+        tmem_ld<EC>(base + (C::NQ - 1) * VT, a);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < EC; c += 2) {
+          const float2 r = __fadd2_rn(make_float2(acc[c], acc[c + 1]), make_float2(a[c], a[c + 1]));
+          acc[c] = r.x;
+          acc[c + 1] = r.y;
+        }
       }
     };
 
@@ -604,20 +678,23 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
       if (ok) store_out(seg_of(0));
     }
     for (int step = 0; step < nsteps && ok; ++step) {
+#ifdef QLA_TRACE
+      step_tr = step + 1;
+#endif
       // H_j into the accumulator registers first: it does not depend on the MMAs
       const int slot = step & 1;
       if (p.has_h) {
         if (!(ok = warp_wait(&ctl->h_full[tl][slot], (step >> 1) & 1, wc))) break;
-        QLA_TR(3, step, 2, 0);
+        QLA_TR(3, step, 2, trc);
         const uint8_t* ht = smem + C::OFF_H + (tl * 2 + slot) * C::TILE;
 #pragma unroll
         for (int h = 0; h < C::HALVES; ++h) {
           const int k = t + 128 * h;
-          if (j.layout == 0) {  // [K rows][32 floats], 128-byte swizzle: pieces 4e..4e+3 of row k
+          if (j.layout == 0) {  // [K rows][32 floats], 128-byte swizzle: pieces c0/4 .. of row k
             const uint8_t* row = ht + k * 128;
 #pragma unroll
             for (int q = 0; q < EC / 4; ++q) {
-              const float4 v = *reinterpret_cast<const float4*>(row + (((4 * e + q) ^ (k & 7)) << 4));
+              const float4 v = *reinterpret_cast<const float4*>(row + (((c0 / 4 + q) ^ (k & 7)) << 4));
               y[h][4 * q] = v.x; y[h][4 * q + 1] = v.y; y[h][4 * q + 2] = v.z; y[h][4 * q + 3] = v.w;
             }
           } else {              // [VT rows][K floats]
@@ -639,18 +716,18 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
       }
       uint64_t* dbar = (p.stall_test && step == 0) ? &ctl->never : d_full;
       if (!(ok = warp_wait(dbar, step & 1, wc))) break;
-      QLA_TR(3, step, 1, 0);
+      QLA_TR(3, step, 1, trc);
       tc_fence_after();
 #pragma unroll
       for (int h = 0; h < C::HALVES; ++h) drain_add(h, y[h]);
-      QLA_TR(3, step, 5, 0);
+      QLA_TR(3, step, 5, trc);
       if (step + 1 < nsteps) {  // X_{j+1} -> B operand: the critical path to the next step
         write_b();
-        QLA_TR(3, step, 6, 0);
+        QLA_TR(3, step, 6, trc);
         tc_fence_before();  // the chains have been read (wait::ld in drain_add)
         __syncwarp();
         if (lane == 0) mbar_arrive(x_ready);
-        QLA_TR(3, step, 4, 0);
+        QLA_TR(3, step, 4, trc);
       } else if (j.fin) {
         float* F = j.fin + u * j.fin_unit_stride;
 #pragma unroll
@@ -671,7 +748,7 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
         if (p.in_place && p.has_h && step + 1 < nsteps)
           if (!(ok = warp_wait(&ctl->h_full[tl][(step + 1) & 1], ((step + 1) >> 1) & 1, wc))) break;
         store_out(seg_of(step + 1));
-        QLA_TR(3, step, 3, 0);
+        QLA_TR(3, step, 3, trc);
       }
       if (p.has_h && p.release == 2) {
         __syncwarp();
@@ -709,7 +786,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D fp32 tensor map: `rows` x `cols` row-major at `base`, box box_cols x box_rows,
-// swizzle 0 (none), 64 or 128 (bytes).
+// swizzle 0 (none), 32, 64 or 128 (bytes).
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows,
               int swizzle) {
   auto fn = encode_fn();
@@ -720,6 +797,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   cuuint32_t estr[2] = {1, 1};
   const CUtensorMapSwizzle sw = swizzle == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                 : swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                : swizzle == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
                                                 : CU_TENSOR_MAP_SWIZZLE_NONE;
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -747,8 +825,8 @@ cudaError_t launch_k(const SeqJob& j, int release, unsigned int* status, uint64_
   // H: kv box 32 columns x K rows (128-byte swizzle); vk box K columns x VT rows
   if (p.has_h && !make_map(&p.map_h, j.H, rows, cols, kv ? 32 : K, kv ? K : VT, kv ? 128 : 0))
     return cudaErrorInvalidValue;
-  // out: per-warp stores of [32 rows][16 columns] (kv, 64-byte swizzle) or [16 rows][32 columns] (vk)
-  if (j.out && !make_map(&p.map_out, j.out, rows, cols, kv ? EC : 32, kv ? 32 : EC, kv ? 64 : 0))
+  // out: per-warp stores of [32 rows][EC columns] (kv, (4 EC)-byte swizzle) or [EC rows][32 columns] (vk)
+  if (j.out && !make_map(&p.map_out, j.out, rows, cols, kv ? C::EC : 32, kv ? 32 : C::EC, kv ? 4 * C::EC : 0))
     return cudaErrorInvalidValue;
   const bool fwd = j.direction == 0;
   if (!make_map(&p.map_m, j.M, states * K, K, fwd ? 32 : 128, fwd ? 128 : 32, fwd ? 128 : 0))
