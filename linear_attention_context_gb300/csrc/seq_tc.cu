@@ -47,11 +47,12 @@
 //                     memory, D in the accumulator chains (TMEM).
 //  splitter  4..11    two warpgroups, alternate chunks: m chunk (ordinary
 //                     shared loads) -> hi/lo -> TMEM A ring (NA slots).
-//  epilogue  12..19   two warpgroups, 16 columns each: H_j (ordinary shared
-//                     loads, then the h-slot release) + the chains
-//                     (tcgen05.ld) = X_{j+1}; its hi/lo -> B operand first
-//                     (the next step waits on it), then out via per-warp
-//                     TMA stores.
+//  epilogue  12..      NE warpgroups (four of 8 columns at K = 128, two of 16
+//                     at K = 256): H_j (ordinary shared loads, then the h-slot
+//                     release) + the chains (tcgen05.ld) = X_{j+1}; its hi/lo
+//                     -> B operand first (the next step waits on it), then out
+//                     via per-warp TMA stores.  (Stores straight from
+//                     registers measured slower: 19.0 against 18.5 us.)
 //
 //  storage        written by           read by             reusable after
 //  m ring [s]     TMA (async)          splitter (generic)  splitter's last read: fence + m_empty arrive
@@ -67,7 +68,7 @@
 // two row blocks of K = 256 interleave.  Barriers: m_full/h_full count 1 +
 // transaction bytes; m_empty count 4 (the splitter warpgroup's warps); a_full
 // count 8 (a group of two A slots gets one chunk from each splitter warpgroup);
-// h_empty, x_ready count 8 (the epilogue warps); a_empty, d_full count 3 (one
+// h_empty, x_ready count 4 NE (the epilogue warps); a_empty, d_full count 3 (one
 // tcgen05.commit per issuing thread).  Producers wait their empty barriers
 // with the parity of (use / slots) ^ 1, consumers their full barriers with
 // (use / slots), so the first producer wait passes at once.
@@ -111,26 +112,26 @@ namespace {
 
 using namespace ptx;
 
-constexpr int VT = 32;                          // state columns per tile
+constexpr int kCtaCols = 32;                    // state columns per CTA (TILES x VT)
 constexpr uint32_t kChunkBytes = 128 * 32 * 4;  // one A chunk: 128 rows x 32 columns fp32
 constexpr uint32_t kTmemCols = 512;
 
 // TILES column tiles of VT columns share one CTA, one M stream and one A
 // split; with two, the issuers run all of tile 0's MMAs of a step before
 // tile 1's, so tile 0's epilogue overlaps tile 1's MMAs.
-template <int K, int TILES>
+template <int K, int TILES, int VT>
 struct Cfg {
   static constexpr int HALVES = K / 128;          // 128-row MMA blocks of the output
   static constexpr int KCH = K / 32;              // 32-wide k chunks per block
   static constexpr int CPS = HALVES * KCH;        // chunks per step
   static constexpr int NI = 3;                    // MMA-issuing warps (one thread each)
-  static constexpr int NB = (TILES == 1 && K == 128) ? 4 : 2;  // big-term chains per row block
+  static constexpr int NB = K == 128 ? 4 : 2;     // big-term chains per row block
   static constexpr int NQ = NB + 2;               // chains per row block (+ A_hi X_lo, A_lo X_hi)
   static constexpr uint32_t ACOL = TILES * HALVES * NQ * VT;  // first column of the A ring
   static constexpr int NA = (int)((kTmemCols - ACOL) / 128) * 2;  // A ring slots (hi, lo: 64 columns each) ...
   static constexpr int NAG = NA / 2;              // ... in groups of two chunks, one barrier pair per group
-  static constexpr int NM = TILES == 2 ? 4 : (K == 128 ? 6 : 4);  // m ring stages
-  static constexpr int NOUT = (TILES == 1 && K == 128) ? 2 : 1;    // out staging buffers per tile
+  static constexpr int NM = (TILES == 2 && VT == 32) ? 4 : (K == 128 ? 6 : 4);  // m ring stages
+  static constexpr int NOUT = K == 128 ? 2 : 1;   // out staging buffers per tile
   static constexpr int NSG = 2;                   // splitter warpgroups (take chunks round-robin)
   static constexpr int NE = (TILES == 1 && K == 128) ? 4 : 2;  // epilogue warpgroups per tile ...
   static constexpr int EC = VT / NE;              // ... each owning EC state columns
@@ -150,6 +151,7 @@ struct Cfg {
   static_assert(ACOL + NA * 64 <= kTmemCols, "TMEM columns");
   static_assert(CPS % 2 == 0 && NAG >= 1 && NAG <= 4, "chunks per step, A groups");
   static_assert(TILES == 1 || K == 128, "two tiles only for K = 128");
+  static_assert(TILES * VT == kCtaCols && EC % 8 == 0, "tile widths");
   // A splitter group may wait on a ring slot only for a use whose previous
   // use was its own: otherwise, while another group's fill of the previous
   // use is still in flight, the phase two uses back (same parity) would
@@ -214,10 +216,10 @@ __device__ __forceinline__ void split_tf32x2(float x0, float x1, uint32_t& hi0, 
 // block h = c % HALVES) of tile `tl`: role 0 the four A_hi X_hi k-steps, role
 // 1 the A_hi X_lo ones, role 2 the A_lo X_hi ones.  With c, tl and the role
 // compile-time constants every chain index and accumulate flag folds.
-template <int K, int TILES, int ROLE>
+template <int K, int TILES, int VT, int ROLE>
 __device__ __forceinline__ void mma_chunk(const int tl, const int c, uint32_t tmem, uint32_t a_hi, uint64_t dh0,
                                           uint64_t dl0) {
-  using C = Cfg<K, TILES>;
+  using C = Cfg<K, TILES, VT>;
   constexpr uint32_t idesc = idesc_tf32(128, VT);
   const int kc = c / C::HALVES, h = c % C::HALVES;
   const int q0 = (tl * C::HALVES + h) * C::NQ;
@@ -235,14 +237,14 @@ __device__ __forceinline__ void mma_chunk(const int tl, const int c, uint32_t tm
   }
 }
 
-template <int K, int TILES, int ROLE>
+template <int K, int TILES, int VT, int ROLE>
 __device__ __forceinline__ void mma_role(Ctrl* ctl, uint8_t* smem, uint32_t tmem, int nsteps, const WaitCtl& wc
 #ifdef QLA_TRACE
                                          ,
                                          bool tr
 #endif
 ) {
-  using C = Cfg<K, TILES>;
+  using C = Cfg<K, TILES, VT>;
   // Descriptors of the k-block 0 rows of each tile's B hi / lo; every other
   // k-step adds a compile-time byte offset (>> 4) to the start-address field.
   uint64_t dh0[TILES], dl0[TILES];
@@ -269,8 +271,8 @@ __device__ __forceinline__ void mma_role(Ctrl* ctl, uint8_t* smem, uint32_t tmem
         const bool pair1_ready = mbar_test_wait(&ctl->a_full[1], phase0);
         QLA_TR(1, step, 1, 4 * ROLE);
         tc_fence_after();
-        mma_chunk<K, TILES, ROLE>(0, 0, tmem, tmem + C::ACOL + 0 * 64, dh0[0], dl0[0]);
-        mma_chunk<K, TILES, ROLE>(0, 1, tmem, tmem + C::ACOL + 1 * 64, dh0[0], dl0[0]);
+        mma_chunk<K, TILES, VT, ROLE>(0, 0, tmem, tmem + C::ACOL + 0 * 64, dh0[0], dl0[0]);
+        mma_chunk<K, TILES, VT, ROLE>(0, 1, tmem, tmem + C::ACOL + 1 * 64, dh0[0], dl0[0]);
         mma_commit(&ctl->a_empty[0]);
         QLA_TR(1, step, 3, 4 * ROLE);
         if (!pair1_ready) {
@@ -278,8 +280,8 @@ __device__ __forceinline__ void mma_role(Ctrl* ctl, uint8_t* smem, uint32_t tmem
           tc_fence_after();
         }
         QLA_TR(1, step, 1, 2 + 4 * ROLE);
-        mma_chunk<K, TILES, ROLE>(0, 2, tmem, tmem + C::ACOL + 2 * 64, dh0[0], dl0[0]);
-        mma_chunk<K, TILES, ROLE>(0, 3, tmem, tmem + C::ACOL + 3 * 64, dh0[0], dl0[0]);
+        mma_chunk<K, TILES, VT, ROLE>(0, 2, tmem, tmem + C::ACOL + 2 * 64, dh0[0], dl0[0]);
+        mma_chunk<K, TILES, VT, ROLE>(0, 3, tmem, tmem + C::ACOL + 3 * 64, dh0[0], dl0[0]);
         mma_commit(&ctl->a_empty[1]);
         mma_commit(&ctl->d_full[0]);
         QLA_TR(1, step, 3, 2 + 4 * ROLE);
@@ -298,9 +300,9 @@ __device__ __forceinline__ void mma_role(Ctrl* ctl, uint8_t* smem, uint32_t tmem
           QLA_TR(1, step, 1, c + 4 * ROLE);
           tc_fence_after();
         }
-        mma_chunk<K, TILES, ROLE>(tl, c, tmem, tmem + C::ACOL + (2 * grp) * 64, dh0[tl], dl0[tl]);
+        mma_chunk<K, TILES, VT, ROLE>(tl, c, tmem, tmem + C::ACOL + (2 * grp) * 64, dh0[tl], dl0[tl]);
         if (tl == 0) QLA_TR(1, step, 2, c + 4 * ROLE);
-        mma_chunk<K, TILES, ROLE>(tl, c + 1, tmem, tmem + C::ACOL + (2 * grp + 1) * 64, dh0[tl], dl0[tl]);
+        mma_chunk<K, TILES, VT, ROLE>(tl, c + 1, tmem, tmem + C::ACOL + (2 * grp + 1) * 64, dh0[tl], dl0[tl]);
         if (tl == 0) QLA_TR(1, step, 2, c + 1 + 4 * ROLE);
         if (tl == TILES - 1) mma_commit(&ctl->a_empty[grp]);
         if (tl == 0) QLA_TR(1, step, 3, c + 4 * ROLE);
@@ -321,9 +323,9 @@ __device__ __forceinline__ void mma_role(Ctrl* ctl, uint8_t* smem, uint32_t tmem
   mbar_wait_drain(&ctl->mma_done[ROLE], 0, 200000000ull);
 }
 
-template <int K, int TILES>
-__global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(const __grid_constant__ TcParams p) {
-  using C = Cfg<K, TILES>;
+template <int K, int TILES, int VT>
+__global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kernel(const __grid_constant__ TcParams p) {
+  using C = Cfg<K, TILES, VT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + C::OFF_CTRL);
@@ -475,13 +477,13 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
     // ------------------------------------------------------------ mma issuers
     if (lane == 0) {
 #ifdef QLA_TRACE
-      if (warp == 1) mma_role<K, TILES, 0>(ctl, smem, tmem, nsteps, wc, tr);
-      else if (warp == 2) mma_role<K, TILES, 1>(ctl, smem, tmem, nsteps, wc, tr);
-      else mma_role<K, TILES, 2>(ctl, smem, tmem, nsteps, wc, tr);
+      if (warp == 1) mma_role<K, TILES, VT, 0>(ctl, smem, tmem, nsteps, wc, tr);
+      else if (warp == 2) mma_role<K, TILES, VT, 1>(ctl, smem, tmem, nsteps, wc, tr);
+      else mma_role<K, TILES, VT, 2>(ctl, smem, tmem, nsteps, wc, tr);
 #else
-      if (warp == 1) mma_role<K, TILES, 0>(ctl, smem, tmem, nsteps, wc);
-      else if (warp == 2) mma_role<K, TILES, 1>(ctl, smem, tmem, nsteps, wc);
-      else mma_role<K, TILES, 2>(ctl, smem, tmem, nsteps, wc);
+      if (warp == 1) mma_role<K, TILES, VT, 0>(ctl, smem, tmem, nsteps, wc);
+      else if (warp == 2) mma_role<K, TILES, VT, 1>(ctl, smem, tmem, nsteps, wc);
+      else mma_role<K, TILES, VT, 2>(ctl, smem, tmem, nsteps, wc);
 #endif
     }
     __syncwarp();
@@ -690,11 +692,12 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES>::WARPS, 1) seq_tc_kernel(co
 #pragma unroll
         for (int h = 0; h < C::HALVES; ++h) {
           const int k = t + 128 * h;
-          if (j.layout == 0) {  // [K rows][32 floats], 128-byte swizzle: pieces c0/4 .. of row k
-            const uint8_t* row = ht + k * 128;
+          if (j.layout == 0) {  // [K rows][VT floats], (4 VT)-byte swizzle: 16-byte piece p of row k
+                                // at p ^ ((k VT / 32) % (VT / 4)); this warp's pieces are c0/4 ..
+            const uint8_t* row = ht + k * (VT * 4);
 #pragma unroll
             for (int q = 0; q < EC / 4; ++q) {
-              const float4 v = *reinterpret_cast<const float4*>(row + (((c0 / 4 + q) ^ (k & 7)) << 4));
+              const float4 v = *reinterpret_cast<const float4*>(row + (((c0 / 4 + q) ^ ((k * VT / 32) & (VT / 4 - 1))) << 4));
               y[h][4 * q] = v.x; y[h][4 * q + 1] = v.y; y[h][4 * q + 2] = v.z; y[h][4 * q + 3] = v.w;
             }
           } else {              // [VT rows][K floats]
@@ -805,10 +808,10 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   return r == CUDA_SUCCESS;
 }
 
-template <int K, int TILES>
+template <int K, int TILES, int VT>
 cudaError_t launch_k(const SeqJob& j, int release, unsigned int* status, uint64_t limit_ns, int stall_test,
                      cudaStream_t stream) {
-  using C = Cfg<K, TILES>;
+  using C = Cfg<K, TILES, VT>;
   TcParams p;
   memset(&p, 0, sizeof p);
   p.job = j;
@@ -822,8 +825,8 @@ cudaError_t launch_k(const SeqJob& j, int release, unsigned int* status, uint64_
   const bool kv = j.layout == 0;
   const uint64_t rows = states * (kv ? (uint64_t)K : (uint64_t)j.V);
   const uint64_t cols = kv ? (uint64_t)j.V : (uint64_t)K;
-  // H: kv box 32 columns x K rows (128-byte swizzle); vk box K columns x VT rows
-  if (p.has_h && !make_map(&p.map_h, j.H, rows, cols, kv ? 32 : K, kv ? K : VT, kv ? 128 : 0))
+  // H: kv box VT columns x K rows ((4 VT)-byte swizzle); vk box K columns x VT rows
+  if (p.has_h && !make_map(&p.map_h, j.H, rows, cols, kv ? VT : K, kv ? K : VT, kv ? 4 * VT : 0))
     return cudaErrorInvalidValue;
   // out: per-warp stores of [32 rows][EC columns] (kv, (4 EC)-byte swizzle) or [EC rows][32 columns] (vk)
   if (j.out && !make_map(&p.map_out, j.out, rows, cols, kv ? C::EC : 32, kv ? 32 : C::EC, kv ? 4 * C::EC : 0))
@@ -831,7 +834,7 @@ cudaError_t launch_k(const SeqJob& j, int release, unsigned int* status, uint64_
   const bool fwd = j.direction == 0;
   if (!make_map(&p.map_m, j.M, states * K, K, fwd ? 32 : 128, fwd ? 128 : 32, fwd ? 128 : 0))
     return cudaErrorInvalidValue;
-  auto kern = seq_tc_kernel<K, TILES>;
+  auto kern = seq_tc_kernel<K, TILES, VT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   // (Programmatic dependent launch, letting this set-up overlap the previous
@@ -851,7 +854,7 @@ extern "C" __attribute__((visibility("default"))) int qla_debug_trace(long long*
 }
 #endif
 
-bool tc_supports(int K, int V) { return (K == 128 || K == 256) && V % VT == 0 && V >= VT; }
+bool tc_supports(int K, int V) { return (K == 128 || K == 256) && V % kCtaCols == 0 && V >= kCtaCols; }
 
 cudaError_t launch_seq_tc(const SeqJob& job, int release, unsigned int* status, uint64_t limit_ns, int stall_test,
                           cudaStream_t stream) {
@@ -864,8 +867,11 @@ cudaError_t launch_seq_tc(const SeqJob& job, int release, unsigned int* status, 
   // One column tile per CTA.  (Two tiles per CTA, with tile 0's epilogue
   // overlapping tile 1's MMAs, measured slower on the 32-head K=V=128 S=8
   // workload: 27.6 us against 19.9 us per call.)
-  if (job.K == 256) return launch_k<256, 1>(job, release, status, limit_ns, stall_test, stream);
-  return launch_k<128, 1>(job, release, status, limit_ns, stall_test, stream);
+  if (job.K == 256) return launch_k<256, 1, 32>(job, release, status, limit_ns, stall_test, stream);
+  // (Two independent 16-column halves per CTA, one's epilogue overlapping the
+  // other's MMAs, measured slower: 23.9 against 18.5 us; the A splitters could
+  // not keep up.)
+  return launch_k<128, 1, 32>(job, release, status, limit_ns, stall_test, stream);
 }
 
 }  // namespace qla
