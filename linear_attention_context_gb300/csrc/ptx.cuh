@@ -207,6 +207,23 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// As mma_tf32_ts with the descriptor in two 32-bit halves and the accumulate
+// flag a compile-time constant (a constant predicate costs no instruction).
+template <bool ACC>
+__device__ __forceinline__ void mma_tf32_ts_c(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                              uint32_t idesc) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " .reg .b64 bd;\n"
+      " setp.ne.b32 p, %5, 0;\n"
+      " mov.b64 bd, {%2, %3};\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], bd, %4, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(ACC ? 1 : 0)
+      : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05 operation this thread issued before it completes.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))

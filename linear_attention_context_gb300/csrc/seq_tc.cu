@@ -237,6 +237,43 @@ __device__ __forceinline__ void mma_chunk(const int tl, const int c, uint32_t tm
   }
 }
 
+// The operands of one issuer's 16 MMAs of a step (K = 128, one tile), the
+// same every step: D chain, A slot column, B descriptor low word.  Computed
+// once, so a step's issue is the MMA instructions alone.
+template <int VT, int ROLE>
+struct MmaOps {
+  uint32_t d[16], a[16], b[16];
+};
+
+template <int K, int TILES, int VT, int ROLE>
+__device__ __forceinline__ MmaOps<VT, ROLE> mma_ops(uint32_t tmem, uint64_t dh0, uint64_t dl0) {
+  using C = Cfg<K, TILES, VT>;
+  MmaOps<VT, ROLE> o;
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {
+    const int c = m / 4, s = m % 4, ks = m;
+    const uint32_t off = ((uint32_t)c * (VT * 128) + (uint32_t)s * 32) >> 4;
+    o.d[m] = tmem + (uint32_t)(ROLE == 0 ? ks % C::NB : ROLE == 1 ? C::NB : C::NB + 1) * VT;
+    o.a[m] = tmem + C::ACOL + (uint32_t)c * 64 + (ROLE == 2 ? 32u : 0u) + (uint32_t)s * 8;
+    o.b[m] = (uint32_t)(ROLE == 1 ? dl0 : dh0) + off;
+  }
+  return o;
+}
+
+// Chunks C0..C1 of a step from precomputed operands.
+template <int K, int TILES, int VT, int ROLE, int C0, int C1>
+__device__ __forceinline__ void mma_issue(const MmaOps<VT, ROLE>& o, uint32_t bhi) {
+  using C = Cfg<K, TILES, VT>;
+  constexpr uint32_t idesc = idesc_tf32(128, VT);
+#pragma unroll
+  for (int m = 4 * C0; m < 4 * C1 + 4; ++m) {
+    if ((ROLE == 0 && m < C::NB) || (ROLE != 0 && m == 0))
+      mma_tf32_ts_c<false>(o.d[m], o.a[m], o.b[m], bhi, idesc);
+    else
+      mma_tf32_ts_c<true>(o.d[m], o.a[m], o.b[m], bhi, idesc);
+  }
+}
+
 template <int K, int TILES, int VT, int ROLE>
 __device__ __forceinline__ void mma_role(Ctrl* ctl, uint8_t* smem, uint32_t tmem, int nsteps, const WaitCtl& wc
 #ifdef QLA_TRACE
@@ -256,6 +293,9 @@ __device__ __forceinline__ void mma_role(Ctrl* ctl, uint8_t* smem, uint32_t tmem
   int grp0 = 0;
   uint32_t phase0 = 0;
   bool ok = true;
+  [[maybe_unused]] MmaOps<VT, ROLE> ops;
+  [[maybe_unused]] uint32_t bhi = (uint32_t)(dh0[0] >> 32);  // the same for the hi and lo descriptors
+  if constexpr (TILES == 1 && C::CPS == 4 && C::NAG == 2) ops = mma_ops<K, TILES, VT, ROLE>(tmem, dh0[0], dl0[0]);
   for (int step = 0; step < nsteps && ok; ++step) {
 #pragma unroll
     for (int tl = 0; tl < TILES && ok; ++tl) {
@@ -271,8 +311,7 @@ __device__ __forceinline__ void mma_role(Ctrl* ctl, uint8_t* smem, uint32_t tmem
         const bool pair1_ready = mbar_test_wait(&ctl->a_full[1], phase0);
         QLA_TR(1, step, 1, 4 * ROLE);
         tc_fence_after();
-        mma_chunk<K, TILES, VT, ROLE>(0, 0, tmem, tmem + C::ACOL + 0 * 64, dh0[0], dl0[0]);
-        mma_chunk<K, TILES, VT, ROLE>(0, 1, tmem, tmem + C::ACOL + 1 * 64, dh0[0], dl0[0]);
+        mma_issue<K, TILES, VT, ROLE, 0, 1>(ops, bhi);
         mma_commit(&ctl->a_empty[0]);
         QLA_TR(1, step, 3, 4 * ROLE);
         if (!pair1_ready) {
@@ -280,8 +319,7 @@ __device__ __forceinline__ void mma_role(Ctrl* ctl, uint8_t* smem, uint32_t tmem
           tc_fence_after();
         }
         QLA_TR(1, step, 1, 2 + 4 * ROLE);
-        mma_chunk<K, TILES, VT, ROLE>(0, 2, tmem, tmem + C::ACOL + 2 * 64, dh0[0], dl0[0]);
-        mma_chunk<K, TILES, VT, ROLE>(0, 3, tmem, tmem + C::ACOL + 3 * 64, dh0[0], dl0[0]);
+        mma_issue<K, TILES, VT, ROLE, 2, 3>(ops, bhi);
         mma_commit(&ctl->a_empty[1]);
         mma_commit(&ctl->d_full[0]);
         QLA_TR(1, step, 3, 2 + 4 * ROLE);
