@@ -224,6 +224,12 @@ __device__ __forceinline__ void mma_tf32_ts_c(uint32_t d_tmem, uint32_t a_tmem, 
       : "memory");
 }
 
+// 4-byte shared store at a 32-bit shared address plus a compile-time offset.
+template <uint32_t OFF>
+__device__ __forceinline__ void sts32(uint32_t saddr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0+%2], %1;" ::"r"(saddr), "r"(v), "n"(OFF) : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05 operation this thread issued before it completes.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))

@@ -604,7 +604,6 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
     const int c0 = e * EC;
     const int v0 = vbase + tl * VT;
     uint8_t* bhi = smem + C::OFF_BHI + tl * C::TILE;
-    uint8_t* blo = smem + C::OFF_BLO + tl * C::TILE;
     uint64_t* x_ready = &ctl->x_ready[tl];
     uint64_t* d_full = &ctl->d_full[tl];
     int out_count = 0;
@@ -651,26 +650,39 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
     };
 
     // X -> B operand (hi and lo), K-major, 128-byte swizzle: element (n, k) of
-    // B^T sits in k-block k/32, row n, 16-byte piece ((k%32)/4) ^ (n%8).
+    // B^T sits in k-block k/32, row n, 16-byte piece ((k%32)/4) ^ (n%8).  The
+    // shared addresses of this thread's elements (row k = t, its EC columns)
+    // are fixed: computed once; row k + 128 is 4 k-blocks further, B_lo one
+    // tile-set further.
+    uint32_t baddr[EC];
+    {
+      const uint32_t kb = (uint32_t)(t >> 5) * (VT * 128) + (uint32_t)(t & 3) * 4 + (uint32_t)(c0 >> 3) * 1024;
+      const uint32_t piece = (uint32_t)((t & 31) >> 2);
+#pragma unroll
+      for (int c = 0; c < EC; ++c)
+        baddr[c] = smem_u32(bhi) + kb + (uint32_t)(c & 7) * 128 + ((piece ^ (uint32_t)(c & 7)) << 4) +
+                   (uint32_t)(c >> 3) * 1024;
+    }
     auto write_b = [&]() {
+      constexpr uint32_t kLo = C::OFF_BLO - C::OFF_BHI;
+      constexpr uint32_t kHalf = 4 * VT * 128;  // row k + 128
 #pragma unroll
       for (int h = 0; h < C::HALVES; ++h) {
-        const int k = t + 128 * h;
-        const uint32_t kb = (uint32_t)(k >> 5) * (VT * 128) + (uint32_t)(k & 3) * 4 + (uint32_t)(c0 >> 3) * 1024;
-        const uint32_t piece = (uint32_t)((k & 31) >> 2);
-        uint32_t rowoff[8];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) rowoff[m] = kb + (uint32_t)m * 128 + ((piece ^ (uint32_t)m) << 4);
-#pragma unroll
-        for (int c = 0; c < EC; c += 2) {  // n = c0 + c; c0 is a multiple of 8
+        for (int c = 0; c < EC; c += 2) {
           uint32_t h0, h1, l0, l1;
           split_tf32x2(y[h][c], y[h][c + 1], h0, h1, l0, l1);
-          const uint32_t off0 = rowoff[c & 7] + (uint32_t)(c >> 3) * 1024;
-          const uint32_t off1 = rowoff[(c + 1) & 7] + (uint32_t)((c + 1) >> 3) * 1024;
-          *reinterpret_cast<uint32_t*>(bhi + off0) = h0;
-          *reinterpret_cast<uint32_t*>(blo + off0) = l0;
-          *reinterpret_cast<uint32_t*>(bhi + off1) = h1;
-          *reinterpret_cast<uint32_t*>(blo + off1) = l1;
+          if (h == 0) {
+            sts32<0>(baddr[c], h0);
+            sts32<kLo>(baddr[c], l0);
+            sts32<0>(baddr[c + 1], h1);
+            sts32<kLo>(baddr[c + 1], l1);
+          } else {
+            sts32<kHalf>(baddr[c], h0);
+            sts32<kLo + kHalf>(baddr[c], l0);
+            sts32<kHalf>(baddr[c + 1], h1);
+            sts32<kLo + kHalf>(baddr[c + 1], l1);
+          }
         }
       }
       QLA_TR(3, step_tr, 7, trc);
