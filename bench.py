@@ -139,16 +139,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def dist_setup(n_gpus):
+def dist_setup(n_gpus, backend="nccl"):
+    """Rank, world size and local rank from the launcher's environment; one
+    process per GPU over NCCL (gloo, on the host, for the multi-rank tests)."""
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
+    elif backend == "nccl":
         torch.cuda.set_device(0)
     return rank, world, local
 
@@ -159,22 +164,34 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world):
+def max_over_ranks(x, world, device="cuda"):
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
 
-def make_problem_set():
-    """The four calls' seeded inputs (numpy, host)."""
+def job_us_per_call(ms_slowest, calls_per_rank, world):
+    """Whole-job figure: every rank's calls over the slowest rank's time (each
+    rank processes its own shard, so the job's calls are world x calls_per_rank)."""
+    return ms_slowest * 1e3 / (calls_per_rank * world)
+
+
+def shard_unit0(rank):
+    """First chain of this rank's shard: rank r processes batch element r of a
+    job with B = world (the same shapes on every rank, disjoint inputs)."""
+    return rank * HEADS
+
+
+def make_problem_set(rank=0):
+    """The four calls' seeded inputs (numpy, host), this rank's shard."""
     import qla_inputs as qi
     probs = []
     for name, layout, direction in CALLS:
-        H, M, h0 = qi.make_inputs(qi.WORKLOADS[name], layout)
+        H, M, h0 = qi.make_inputs(qi.WORKLOADS[name], layout, unit0=shard_unit0(rank))
         probs.append(dict(name=name, layout=layout, direction=direction, H=H, M=M, h0=h0))
     return probs
 
@@ -187,7 +204,7 @@ def run_ours(args):
 
     rank, world, local = dist_setup(args.gpus)
     dev = torch.device("cuda", torch.cuda.current_device())
-    probs = make_problem_set()
+    probs = make_problem_set(rank)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     per_call = sum(p["H"].nbytes * 2 + p["M"].nbytes + p["h0"].nbytes for p in probs) / len(probs)
     reps = max(2, math.ceil(3 * l2 / (per_call * len(probs))))
@@ -263,7 +280,7 @@ def run_ours(args):
 
     n_calls = args.steps * len(CALLS)
     us_per_call_rank = ms * 1e3 / n_calls
-    value = ms * 1e3 / (n_calls * world)  # whole job: all ranks' calls over the slowest rank's time
+    value = job_us_per_call(ms, n_calls, world)
     var, eng = qla.resolve(1, HEADS, S, K, V, "kv")
     if args.engine != "auto":
         eng = args.engine
@@ -307,7 +324,7 @@ def run_ours(args):
         ems = max_over_ranks(a0.elapsed_time(a1), world)
         h2d = sum(h["H"].nbytes + h["M"].nbytes + h["h0"].nbytes for h in hin)
         d2h = sum(h["out"].nbytes for h in hin)
-        e2e = {"value": round(ems * 1e3 / (e2e_steps * len(CALLS) * world), 3), "unit": "us",
+        e2e = {"value": round(job_us_per_call(ems, e2e_steps * len(CALLS), world), 3), "unit": "us",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     cpu = None

@@ -120,27 +120,32 @@ class Case:
         return replace(self, **kw)
 
 
-def make_inputs(c: Case, layout: str = "kv"):
+def make_inputs(c: Case, layout: str = "kv", unit0: int = 0):
     """Returns (H, M, h_init) as numpy fp32 arrays shaped for ``layout``.
 
-    h_init is None when ``c.init_kind == "none"`` (zero initial state)."""
+    h_init is None when ``c.init_kind == "none"`` (zero initial state).
+    ``unit0`` is the index of this problem's first chain within a larger job
+    of the same Case: the arrays are then exactly chains unit0 .. unit0 +
+    B*heads - 1 of that job (the generator streams are keyed by block index),
+    which is how a job is sharded across ranks."""
     n = c.chains
     KV = c.K * c.V
+    b0 = unit0 * c.S
     if c.h_kind == "gaussian":
-        H = gaussian(n * c.S, KV, c.seed, TENSOR_H, c.h_scale)
+        H = gaussian(n * c.S, KV, c.seed, TENSOR_H, c.h_scale, block0=b0)
     elif c.h_kind == "small_int":
-        H = small_int(n * c.S, KV, c.seed, TENSOR_H, c.int_max)
+        H = small_int(n * c.S, KV, c.seed, TENSOR_H, c.int_max, block0=b0)
     elif c.h_kind == "zero":
         H = np.zeros(n * c.S * KV, np.float32)
     else:
         raise ValueError(c.h_kind)
     nm = n * c.S
     if c.m_kind == "householder":
-        M = householder(nm, c.K, c.seed, TENSOR_M, c.gmin, c.gmax)
+        M = householder(nm, c.K, c.seed, TENSOR_M, c.gmin, c.gmax, block0=b0)
     elif c.m_kind == "orthogonal":
-        M = orthogonal(nm, c.K, c.seed, TENSOR_M, c.m_scale)
+        M = orthogonal(nm, c.K, c.seed, TENSOR_M, c.m_scale, block0=b0)
     elif c.m_kind == "signed_perm":
-        M = signed_perm(nm, c.K, c.seed, TENSOR_M)
+        M = signed_perm(nm, c.K, c.seed, TENSOR_M, block0=b0)
     elif c.m_kind == "identity":
         M = np.broadcast_to(np.eye(c.K, dtype=np.float32), (nm, c.K, c.K)).copy()
     elif c.m_kind == "zero":
@@ -148,9 +153,9 @@ def make_inputs(c: Case, layout: str = "kv"):
     else:
         raise ValueError(c.m_kind)
     if c.init_kind == "gaussian":
-        h0 = gaussian(n, KV, c.seed, TENSOR_INIT, c.init_scale)
+        h0 = gaussian(n, KV, c.seed, TENSOR_INIT, c.init_scale, block0=unit0)
     elif c.init_kind == "small_int":
-        h0 = small_int(n, KV, c.seed, TENSOR_INIT, c.int_max)
+        h0 = small_int(n, KV, c.seed, TENSOR_INIT, c.int_max, block0=unit0)
     elif c.init_kind == "none":
         h0 = None
     else:
