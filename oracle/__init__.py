@@ -76,3 +76,41 @@ def cp_correct(H, M, h_init, layout="kv", direction="fwd", want_out=True, want_f
     if return_threads:
         return out, fin, used
     return out, fin
+
+
+def cp_correct_varlen(H, M, h_init, cu_seg, layout="kv", direction="fwd"):
+    """Variable-length form: sequences of different segment counts packed
+    along the segment axis.
+
+    H: [heads, T, K, V] (kv) or [heads, T, V, K] (vk); M: [heads, T, K, K];
+    cu_seg: N + 1 non-decreasing offsets with cu_seg[0] = 0 and cu_seg[N] = T,
+    sequence n owning segments cu_seg[n] .. cu_seg[n+1] - 1; h_init: [N, heads,
+    state] or None (zeros).  Each (sequence, head) chain is the fixed-length
+    recurrence over its own segments, so this is cp_correct applied to each
+    sequence's slice.  A sequence with no segment has no outputs and its final
+    state is its initial state.  Returns (out shaped like H, final [N, heads,
+    state]) in fp64."""
+    H = _f32(H)
+    M = _f32(M)
+    h_init = _f32(h_init)
+    cu = [int(x) for x in np.asarray(cu_seg).reshape(-1)]
+    heads, T = H.shape[:2]
+    state = H.shape[2:]
+    N = len(cu) - 1
+    assert N >= 0 and cu[0] == 0 and cu[-1] == T and all(a <= b for a, b in zip(cu, cu[1:])), cu
+    assert M.shape[:2] == (heads, T)
+    if h_init is not None:
+        assert h_init.shape == (N, heads) + state, (h_init.shape, H.shape)
+    out = np.zeros(H.shape, np.float64)
+    fin = np.zeros((N, heads) + state, np.float64)
+    for n in range(N):
+        s0, s1 = cu[n], cu[n + 1]
+        init = None if h_init is None else h_init[n:n + 1]
+        if s1 == s0:
+            if init is not None:
+                fin[n] = init[0]
+            continue
+        o, f = cp_correct(H[None, :, s0:s1], M[None, :, s0:s1], init, layout, direction, want_final=True)
+        out[:, s0:s1] = o[0]
+        fin[n] = f[0]
+    return out, fin

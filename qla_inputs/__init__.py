@@ -193,3 +193,35 @@ def sweep_case(heads: int, S: int) -> Case:
 
 SWEEP_HEADS = (1, 4, 32)
 SWEEP_S = (2, 8, 32, 128)
+
+
+def make_varlen_inputs(lengths, heads, K, V, seed, layout="kv", m_kind="householder", gmin=0.9, gmax=1.0,
+                       m_scale=0.99, h_scale=1.0, init_scale=1.0, with_init=True):
+    """Packed variable-length inputs: sequence n has lengths[n] segments.
+
+    Returns (H [heads, T, state], M [heads, T, K, K], h_init [N, heads, state]
+    or None, cu_seg int32 [N + 1]) as numpy arrays, state = (K, V) for kv and
+    (V, K) for vk.  Blocks are keyed (seed, tensor, block index) like the
+    fixed-length inputs; H and M blocks are numbered head-major (h * T + t)."""
+    lengths = [int(x) for x in lengths]
+    cu = np.zeros(len(lengths) + 1, np.int32)
+    cu[1:] = np.cumsum(lengths)
+    T = int(cu[-1])
+    N = len(lengths)
+    KV = K * V
+    H = gaussian(heads * T, KV, seed, TENSOR_H, h_scale)
+    if m_kind == "householder":
+        M = householder(heads * T, K, seed, TENSOR_M, gmin, gmax)
+    elif m_kind == "orthogonal":
+        M = orthogonal(heads * T, K, seed, TENSOR_M, m_scale)
+    elif m_kind == "signed_perm":
+        M = signed_perm(heads * T, K, seed, TENSOR_M)
+    elif m_kind == "identity":
+        M = np.broadcast_to(np.eye(K, dtype=np.float32), (heads * T, K, K)).copy()
+    else:
+        raise ValueError(m_kind)
+    st = (K, V) if layout == "kv" else (V, K)
+    H = H.reshape((heads, T) + st)
+    M = M.reshape(heads, T, K, K)
+    h0 = gaussian(N * heads, KV, seed, TENSOR_INIT, init_scale).reshape((N, heads) + st) if with_init else None
+    return H, M, h0, cu
