@@ -126,6 +126,33 @@ QLA_API int qla_cp_correct_ex(const float* H, const float* M, const float* h_ini
                       int direction, int variant, int engine, int release, int scan_group,
                       void* stream);
 
+/*
+ * Variable-length form.  Antarx Memos, "一次 TileLang Warp Specialization 数值
+ * 错误的定位与修复", sections "验证分别回答了什么问题" and "性能结果", list
+ * variable-length inputs among the configurations the full operator is
+ * checked and timed on, without fixing a layout; here the offsets follow the
+ * cu_seqlens convention of varlen attention kernels.  N sequences share the
+ * segment axis: sequence n owns segments cu_seg[n] .. cu_seg[n+1] - 1, so it
+ * has cu_seg[n+1] - cu_seg[n] >= 0 segments, and each (sequence, head) chain
+ * is the fixed-length recurrence over its own segments.
+ *   H, out       [heads][T][state]: head h's segments of all sequences, packed;
+ *                out may equal H (in place) or be NULL when final_state is not.
+ *   M            [heads][T][K][K].
+ *   h_init       [N][heads][state] or NULL (zero initial states).
+ *   final_state  [N][heads][state] or NULL; a sequence without segments gets
+ *                its initial state.
+ *   cu_seg       DEVICE pointer to N + 1 int32 offsets, cu_seg[0] = 0,
+ *                non-decreasing, cu_seg[N] = T (4-byte aligned).
+ * Sequential variant only; engine QLA_ENGINE_*.  The host checks everything
+ * but the offsets' values; a kernel that finds a chain's offsets outside
+ * [0, T] or decreasing skips that chain (reads and writes nothing for it) and
+ * sets bit 1 (value 2) of the device status word (qla_device_status).
+ * Requires N * heads <= 65535.
+ */
+QLA_API int qla_cp_correct_varlen(const float* H, const float* M, const float* h_init, float* out,
+                          float* final_state, const int* cu_seg, int N, int T, int heads, int K,
+                          int V, int layout, int direction, int engine, void* stream);
+
 /* Bytes of device scratch the scan variant uses for this shape and group
  * size (0 = automatic); 0 when the scan does not apply. */
 QLA_API size_t qla_scan_workspace_bytes(int B, int heads, int S, int K, int V, int scan_group);
@@ -141,11 +168,13 @@ QLA_API const char* qla_status_string(int status);
 QLA_API const char* qla_last_error(void);
 
 /*
- * Reads and clears the device-side status word of the current device, which
- * a kernel sets when one of its bounded waits gives up (the kernel then drains
- * its copies in flight and returns early, leaving its outputs incomplete).
- * Synchronises the device.  *flags receives the word (0 = no event); returns
- * QLA_ERR_TIMEOUT if it was non-zero, QLA_OK otherwise, QLA_ERR_CUDA on error.
+ * Reads and clears the device-side status word of the current device.  Bit 0
+ * (value 1): one of a kernel's bounded waits gave up (the kernel then drained
+ * its copies in flight and returned early, leaving its outputs incomplete).
+ * Bit 1 (value 2): a variable-length call met invalid offsets and skipped
+ * those chains.  Synchronises the device.  *flags receives the word (0 = no
+ * event); returns QLA_ERR_TIMEOUT if bit 0 was set, else QLA_ERR_INVALID_ARG
+ * if the word was non-zero, QLA_OK otherwise, QLA_ERR_CUDA on error.
  */
 QLA_API int qla_device_status(int* flags);
 

@@ -31,8 +31,8 @@ STATUS = {0: "QLA_OK", -1: "QLA_ERR_INVALID_ARG", -2: "QLA_ERR_UNSUPPORTED", -3:
           -4: "QLA_ERR_ALIAS", -5: "QLA_ERR_CUDA", -6: "QLA_ERR_ARCH", -7: "QLA_ERR_TIMEOUT"}
 
 # Every function include/qla.h declares.
-EXPORTS = ("qla_cp_correct", "qla_cp_correct_ex", "qla_scan_workspace_bytes", "qla_resolve",
-           "qla_status_string", "qla_last_error", "qla_device_status", "qla_selftest_stalled_wait",
+EXPORTS = ("qla_cp_correct", "qla_cp_correct_ex", "qla_cp_correct_varlen", "qla_scan_workspace_bytes",
+           "qla_resolve", "qla_status_string", "qla_last_error", "qla_device_status", "qla_selftest_stalled_wait",
            "qla_cp_correct_scan_static", "qla_version")
 
 # Bytes of scratch the allocation-free scan entry point holds (QLA_SCAN_STATIC_BYTES).
@@ -66,6 +66,8 @@ def lib():
         L.qla_cp_correct.restype = ci
         L.qla_cp_correct_ex.argtypes = [vp, vp, vp, vp, vp] + [ci] * 11 + [vp]
         L.qla_cp_correct_ex.restype = ci
+        L.qla_cp_correct_varlen.argtypes = [vp, vp, vp, vp, vp, vp] + [ci] * 8 + [vp]
+        L.qla_cp_correct_varlen.restype = ci
         L.qla_scan_workspace_bytes.argtypes = [ci] * 6
         L.qla_scan_workspace_bytes.restype = cz
         L.qla_resolve.argtypes = [ci] * 6 + [ctypes.POINTER(ci), ctypes.POINTER(ci)]
@@ -166,6 +168,49 @@ def cp_correct(H, M, h_init=None, out=None, *, layout="kv", direction="fwd", fin
     return out
 
 
+def cp_correct_varlen(H, M, cu_seg, h_init=None, out=None, *, layout="kv", direction="fwd", final_state=None,
+                      engine="auto", stream=None, want_out=True):
+    """Variable-length form: N sequences packed along the segment axis.
+
+    H: [heads, T, K, V] (kv) or [heads, T, V, K] (vk) float32 CUDA tensor;
+    M: [heads, T, K, K]; cu_seg: int32 CUDA tensor of N + 1 offsets
+    (sequence n owns segments cu_seg[n] .. cu_seg[n+1] - 1); h_init and
+    final_state: [N, heads, state] or None; out like H (may be H), or None to
+    allocate.  Returns ``out`` (None when ``want_out`` is False).  Offsets are
+    checked on the device: invalid ones skip their chains and set bit 1 of the
+    status word (``device_status()``)."""
+    import torch
+    if layout not in LAYOUTS or direction not in DIRECTIONS:
+        raise ValueError(f"layout {layout!r} / direction {direction!r}")
+    if H.dim() != 4:
+        raise ValueError(f"H must be [heads, T, rows, cols], got {tuple(H.shape)}")
+    heads, T, r, c = H.shape
+    K, V = (r, c) if layout == "kv" else (c, r)
+    if tuple(M.shape) != (heads, T, K, K):
+        raise ValueError(f"M must be {(heads, T, K, K)}, got {tuple(M.shape)}")
+    dev = H.device
+    if dev.type != "cuda":
+        raise ValueError("H must be a CUDA tensor")
+    if cu_seg.dtype != torch.int32 or cu_seg.dim() != 1 or cu_seg.device != dev or not cu_seg.is_contiguous():
+        raise ValueError("cu_seg must be a contiguous 1-D int32 tensor on H's device")
+    N = cu_seg.numel() - 1
+    st = tuple(H.shape[2:])
+    _check_tensor("H", H, dev)
+    _check_tensor("M", M, dev)
+    _check_tensor("h_init", h_init, dev, (N, heads) + st)
+    _check_tensor("final_state", final_state, dev, (N, heads) + st)
+    if want_out and out is None:
+        out = torch.empty_like(H)
+    if out is not None:
+        _check_tensor("out", out, dev, H.shape)
+    with torch.cuda.device(dev):
+        rc = lib().qla_cp_correct_varlen(_ptr(H), _ptr(M), _ptr(h_init), _ptr(out), _ptr(final_state),
+                                         _ptr(cu_seg), N, T, heads, K, V, LAYOUTS[layout], DIRECTIONS[direction],
+                                         ENGINES[engine], _stream_handle(stream))
+    check(rc)
+    return out
+
+
 def scan_workspace_bytes(B, heads, S, K, V, scan_group=0) -> int:
     return int(lib().qla_scan_workspace_bytes(B, heads, S, K, V, scan_group))
 
@@ -180,9 +225,10 @@ def resolve(B, heads, S, K, V, layout="kv"):
 
 
 def device_status() -> int:
-    """Reads and clears the device status word (synchronises); 0 = no event."""
+    """Reads and clears the device status word (synchronises); 0 = no event,
+    bit 0 a bounded wait gave up, bit 1 invalid variable-length offsets."""
     f = ctypes.c_int()
     rc = lib().qla_device_status(ctypes.byref(f))
-    if rc not in (QLA_OK, -7):
+    if rc not in (QLA_OK, -7, -1):
         check(rc)
     return f.value

@@ -134,6 +134,46 @@ int check_args(const float* H, const float* M, const float* h_init, const float*
   return QLA_OK;
 }
 
+// Host-side checks of a variable-length call (the offsets themselves live in
+// device memory and are checked by the kernels).
+int check_varlen_args(const float* H, const float* M, const float* h_init, const float* out, const float* fin,
+                      const int* cu_seg, int N, int T, int heads, int K, int V, int layout, int direction) {
+  if (N < 1 || T < 0 || heads < 1 || K < 1 || V < 1)
+    return fail(QLA_ERR_INVALID_ARG, "N, heads, K, V must be >= 1 and T >= 0 (got %d, %d, %d, %d, %d)", N, heads, K,
+                V, T);
+  if (layout != QLA_LAYOUT_KV && layout != QLA_LAYOUT_VK)
+    return fail(QLA_ERR_INVALID_ARG, "layout must be QLA_LAYOUT_KV or QLA_LAYOUT_VK (got %d)", layout);
+  if (direction != QLA_FORWARD && direction != QLA_REVERSE)
+    return fail(QLA_ERR_INVALID_ARG, "direction must be QLA_FORWARD or QLA_REVERSE (got %d)", direction);
+  if (!H || !M || !cu_seg) return fail(QLA_ERR_INVALID_ARG, "H, M and cu_seg must not be NULL");
+  if (!out && !fin) return fail(QLA_ERR_INVALID_ARG, "out and final_state are both NULL: nothing to compute");
+  if (K % 32 || K > 256 || V % 32 || V > 256)
+    return fail(QLA_ERR_UNSUPPORTED, "K and V must be multiples of 32 in [32, 256] (got K=%d, V=%d)", K, V);
+  if ((int64_t)N * heads > 65535) return fail(QLA_ERR_UNSUPPORTED, "N*heads must be at most 65535");
+  if ((int64_t)heads * T >= (int64_t)1 << 31) return fail(QLA_ERR_UNSUPPORTED, "heads*T must be below 2^31");
+  const void* ptrs[] = {H, M, h_init, out, fin};
+  const char* names[] = {"H", "M", "h_init", "out", "final_state"};
+  for (int i = 0; i < 5; ++i)
+    if (ptrs[i] && (reinterpret_cast<uintptr_t>(ptrs[i]) & 15))
+      return fail(QLA_ERR_ALIGNMENT, "%s is not 16-byte aligned", names[i]);
+  if (reinterpret_cast<uintptr_t>(cu_seg) & 3) return fail(QLA_ERR_ALIGNMENT, "cu_seg is not 4-byte aligned");
+  const uintptr_t state = (uintptr_t)K * V * 4;
+  const uintptr_t sb = (uintptr_t)heads * T * state;
+  Range r[6];
+  int n = 0;
+  r[n++] = {(uintptr_t)H, (uintptr_t)H + sb, "H"};
+  r[n++] = {(uintptr_t)M, (uintptr_t)M + (uintptr_t)heads * T * K * K * 4, "M"};
+  r[n++] = {(uintptr_t)cu_seg, (uintptr_t)cu_seg + (uintptr_t)(N + 1) * 4, "cu_seg"};
+  if (h_init) r[n++] = {(uintptr_t)h_init, (uintptr_t)h_init + (uintptr_t)N * heads * state, "h_init"};
+  if (fin) r[n++] = {(uintptr_t)fin, (uintptr_t)fin + (uintptr_t)N * heads * state, "final_state"};
+  if (out && out != H) r[n++] = {(uintptr_t)out, (uintptr_t)out + sb, "out"};
+  for (int a = 0; a < n; ++a)
+    for (int b = a + 1; b < n; ++b)
+      if (overlap(r[a], r[b]))
+        return fail(QLA_ERR_ALIAS, "%s and %s overlap (only out == H is allowed)", r[a].name, r[b].name);
+  return QLA_OK;
+}
+
 // Scan group count for S segments: the critical path is about 2L + G steps
 // with G*L >= S, smallest near G = sqrt(2S).
 int auto_groups(int S) {
@@ -168,7 +208,9 @@ int resolve_variant(const Shape& s, int variant, const DeviceInfo* d) {
   return (s.S >= 24 && tiles <= 16) ? QLA_VARIANT_SCAN : QLA_VARIANT_SEQ;
 }
 
-int launch_seq(const SeqJob& j, int engine, int release, const DeviceInfo* d, cudaStream_t stream) {
+int launch_seq(const SeqJob& job, int engine, int release, const DeviceInfo* d, cudaStream_t stream) {
+  SeqJob j = job;
+  j.status = d->status_word;
   cudaError_t e;
   switch (engine) {
     case QLA_ENGINE_SIMT:
@@ -483,6 +525,40 @@ int qla_cp_correct(const float* H, const float* M, const float* h_init, float* o
                            QLA_ENGINE_AUTO, QLA_RELEASE_MEMBAR, 0, stream);
 }
 
+int qla_cp_correct_varlen(const float* H, const float* M, const float* h_init, float* out, float* final_state,
+                          const int* cu_seg, int N, int T, int heads, int K, int V, int layout, int direction,
+                          int engine, void* stream) {
+  t_last_error.clear();
+  int st = check_varlen_args(H, M, h_init, out, final_state, cu_seg, N, T, heads, K, V, layout, direction);
+  if (st != QLA_OK) return st;
+  if (!known_engine(engine)) return fail(QLA_ERR_INVALID_ARG, "unknown engine %d", engine);
+  DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != QLA_OK) return st;
+  SeqJob j{};
+  j.H = H;
+  j.M = M;
+  j.init = h_init;
+  j.out = out;
+  j.fin = final_state;
+  j.init_unit_stride = (int64_t)K * V;
+  j.fin_unit_stride = (int64_t)K * V;
+  j.nchains = N * heads;
+  j.S = 0;
+  j.L = 1 << 30;
+  j.G = 1;
+  j.K = K;
+  j.V = V;
+  j.layout = layout;
+  j.direction = direction;
+  j.init_mode = h_init ? kInitPointer : kInitZero;
+  j.cu_seg = cu_seg;
+  j.heads = heads;
+  j.T = T;
+  j.nstates = (int64_t)heads * T;
+  Shape s{N, heads, 1, K, V, layout, direction};
+  return launch_seq(j, resolve_engine(s, engine), QLA_RELEASE_MEMBAR, d, static_cast<cudaStream_t>(stream));
+}
+
 int qla_device_status(int* flags) {
   t_last_error.clear();
   DeviceInfo* d = nullptr;
@@ -497,7 +573,8 @@ int qla_device_status(int* flags) {
   if ((e = cudaMemcpy(d->status_word, &zero, sizeof zero, cudaMemcpyHostToDevice)) != cudaSuccess)
     return cuda_fail(e, "clear status word");
   if (flags) *flags = (int)w;
-  return w ? QLA_ERR_TIMEOUT : QLA_OK;
+  if (w & kStatusTimeout) return QLA_ERR_TIMEOUT;
+  return w ? QLA_ERR_INVALID_ARG : QLA_OK;
 }
 
 int qla_selftest_stalled_wait(const float* H, const float* M, float* out, int S, int wait_limit_us, void* stream) {

@@ -48,13 +48,16 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
   const int u = blockIdx.y;
   const int chain = u / j.G;
   const int g = u - chain * j.G;
+  int64_t cbase;  // the chain's first segment in the packed arrays
+  int S;
+  if (!chain_span(j, chain, cbase, S)) return;
   const int s_lo = g * j.L;
-  const int n = min(j.L, j.S - s_lo);
+  const int n = min(j.L, S - s_lo);
   const int64_t st = (int64_t)K * V;
 
-  const float* Hc = j.H ? j.H + chain * j.h_chain_stride : nullptr;
-  float* Oc = j.out ? j.out + chain * j.h_chain_stride : nullptr;
-  const float* Mc = j.M + chain * j.m_chain_stride;
+  const float* Hc = j.H ? j.H + cbase * st : nullptr;
+  float* Oc = j.out ? j.out + cbase * st : nullptr;
+  const float* Mc = j.M + cbase * K * K;
 
   float x[R][4];
 #pragma unroll

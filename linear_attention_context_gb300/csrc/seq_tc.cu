@@ -374,10 +374,25 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
   const int u = blockIdx.y;
   const int chain = u / j.G;
   const int g = u - chain * j.G;
+  int64_t cbase;  // the chain's first segment in the packed arrays
+  int S;
+  if (!chain_span(j, chain, cbase, S)) return;  // invalid offsets: recorded, nothing touched
   const int s_lo = g * j.L;
-  const int n = min(j.L, j.S - s_lo);
+  const int n = min(j.L, S - s_lo);
   const int nsteps = n - 1 + (j.fin ? 1 : 0);
   const int vbase = blockIdx.x * (TILES * VT);
+  if (n <= 0) {  // a sequence without segments: its final state is its initial state
+    if (j.fin) {
+      float* F = j.fin + u * j.fin_unit_stride;
+      const float* I = j.init_mode == kInitPointer ? j.init + u * j.init_unit_stride : nullptr;
+      for (int e = threadIdx.x; e < K * TILES * VT; e += blockDim.x) {
+        const int k = e / (TILES * VT), v = vbase + e % (TILES * VT);
+        const int64_t idx = j.layout == 0 ? (int64_t)k * j.V + v : (int64_t)v * K + k;
+        F[idx] = I ? I[idx] : (j.init_mode == kInitIdentity && k == v ? 1.f : 0.f);
+      }
+    }
+    return;
+  }
   const bool fwd = j.direction == 0;
   auto seg_of = [&](int step) { return fwd ? s_lo + step : s_lo + n - 1 - step; };
 #ifdef QLA_TRACE
@@ -467,10 +482,10 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
       const int hrows = j.layout == 0 ? K : j.V;  // rows of one state in the 2-D view of H
       for (int step = 0; step < nsteps && ok; ++step) {
         const int seg = seg_of(step);
-        const int64_t mrow0 = ((int64_t)chain * j.S + seg) * K;
+        const int64_t mrow0 = (cbase + seg) * K;
         if (p.has_h) {
           const int slot = step & 1;
-          const int64_t hrow0 = ((int64_t)chain * j.S + seg) * hrows;
+          const int64_t hrow0 = (cbase + seg) * hrows;
           for (int tl = 0; tl < TILES && ok; ++tl) {
             if (!(ok = mbar_wait(&ctl->h_empty[tl][slot], ((step >> 1) & 1) ^ 1, wc))) break;
             mbar_arrive_expect_tx(&ctl->h_full[tl][slot], C::TILE);
@@ -640,9 +655,9 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
           const uint8_t* stg = stg_base + ((h * C::NE + e) * 4 + wq) * (32 * EC * 4);
           if (j.layout == 0)
             tma_store_2d(&p.map_out, stg, v0 + c0,
-                         (int32_t)(((int64_t)chain * j.S + seg) * K + 128 * h + 32 * wq));
+                         (int32_t)((cbase + seg) * K + 128 * h + 32 * wq));
           else
-            tma_store_2d(&p.map_out, stg, 128 * h + 32 * wq, (int32_t)(((int64_t)chain * j.S + seg) * V + v0 + c0));
+            tma_store_2d(&p.map_out, stg, 128 * h + 32 * wq, (int32_t)((cbase + seg) * V + v0 + c0));
         }
         bulk_commit();
       }
@@ -871,7 +886,7 @@ cudaError_t launch_k(const SeqJob& j, int release, unsigned int* status, uint64_
   p.in_place = j.out != nullptr && (const void*)j.out == (const void*)j.H;
   p.release = release;
   p.stall_test = stall_test;
-  const uint64_t states = (uint64_t)j.nchains * j.S;
+  const uint64_t states = j.cu_seg ? (uint64_t)j.nstates : (uint64_t)j.nchains * j.S;
   const bool kv = j.layout == 0;
   const uint64_t rows = states * (kv ? (uint64_t)K : (uint64_t)j.V);
   const uint64_t cols = kv ? (uint64_t)j.V : (uint64_t)K;
@@ -911,9 +926,14 @@ cudaError_t launch_seq_tc(const SeqJob& job, int release, unsigned int* status, 
   if (!tc_supports(job.K, job.V)) return cudaErrorInvalidValue;
   if ((int64_t)job.nchains * job.G > 65535) return cudaErrorInvalidValue;
   // The tensor maps view H/out and M as 2-D arrays of all chains' states, so
-  // chains must be packed back to back (H and out are absent in scan phase 1a).
-  if ((job.H || job.out) && job.h_chain_stride != (int64_t)job.S * job.K * job.V) return cudaErrorInvalidValue;
-  if (job.m_chain_stride != (int64_t)job.S * job.K * job.K) return cudaErrorInvalidValue;
+  // chains must be packed back to back (H and out are absent in scan phase 1a;
+  // variable-length jobs locate every chain through its offsets).
+  if (!job.cu_seg) {
+    if ((job.H || job.out) && job.h_chain_stride != (int64_t)job.S * job.K * job.V) return cudaErrorInvalidValue;
+    if (job.m_chain_stride != (int64_t)job.S * job.K * job.K) return cudaErrorInvalidValue;
+  } else if (job.G != 1) {
+    return cudaErrorInvalidValue;
+  }
   // One column tile per CTA.  (Two tiles per CTA, with tile 0's epilogue
   // overlapping tile 1's MMAs, measured slower on the 32-head K=V=128 S=8
   // workload: 27.6 us against 19.9 us per call.)

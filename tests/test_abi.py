@@ -119,3 +119,21 @@ def _has_gpu():
         return torch.cuda.is_available()
     except Exception:
         return False
+
+
+def call_varlen(L, H=FAKE, M=FAKE + (1 << 32), h0=None, out=FAKE + (2 << 32), fin=None, cu=FAKE + (5 << 32), N=3,
+                T=10, heads=2, K=64, V=64, layout=0, direction=0, engine=0):
+    vp = ctypes.c_void_p
+    return L.qla_cp_correct_varlen(vp(H), vp(M), vp(h0), vp(out), vp(fin), vp(cu), N, T, heads, K, V, layout,
+                                   direction, engine, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(cu=None), -1), (dict(H=None), -1), (dict(M=None), -1), (dict(out=None), -1),
+    (dict(N=0), -1), (dict(T=-1), -1), (dict(heads=0), -1), (dict(layout=3), -1), (dict(direction=2), -1),
+    (dict(engine=2), -1), (dict(K=48), -2), (dict(V=300), -2), (dict(N=70000, heads=1), -2),
+    (dict(cu=FAKE + (5 << 32) + 2), -3), (dict(H=FAKE + 8), -3),
+    (dict(cu=FAKE + 64), -4), (dict(out=FAKE + 4096), -4), (dict(h0=FAKE + (1 << 32) + 16), -4),
+])
+def test_varlen_argument_checks(L, kw, status):
+    assert call_varlen(L, **kw) == status
