@@ -139,6 +139,11 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# Steps captured per CUDA graph in the timed region (rounded to a multiple of
+# the replica count).
+STEPS_PER_GRAPH = 16
+
+
 def dist_setup(n_gpus, backend="nccl"):
     """Rank, world size and local rank from the launcher's environment; one
     process per GPU over NCCL (gloo, on the host, for the multi-rank tests)."""
@@ -241,23 +246,34 @@ def run_ours(args):
             if not err <= 1e-5:
                 raise SystemExit(f"bench pre-check failed for {p['name']} {p['layout']} {p['direction']}: {err}")
 
-    # one CUDA graph per replica: the step's four calls
-    graphs = []
-    with torch.cuda.stream(stream):
-        for row in bufs:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for b in row:
+    # CUDA graphs of G consecutive steps (G a multiple of the replica count,
+    # so every graph runs the replicas in the same rotation): a graph
+    # boundary costs a few microseconds that a long captured sequence does
+    # not.  The timed region runs exactly K steps: K // G replays of the
+    # G-step graph, then a graph of the K % G remaining steps.
+    G = reps * max(1, STEPS_PER_GRAPH // reps)
+
+    def capture(nsteps):
+        if nsteps == 0:
+            return None
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for s in range(nsteps):
+                for b in bufs[s % reps]:
                     call(b, stream)
-            graphs.append(g)
+        return g
+
+    with torch.cuda.stream(stream):
+        g_full = capture(G)
+        g_rest = capture(args.steps % G)
     stream.synchronize()
 
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
     with torch.cuda.stream(stream):
-        for w in range(args.warmup):
-            graphs[w % reps].replay()
+        for w in range((args.warmup + G - 1) // G):  # at least W warm-up steps
+            g_full.replay()
     stream.synchronize()
     barrier(world)
     torch.cuda.synchronize()
@@ -266,8 +282,10 @@ def run_ours(args):
         sampler.mark("start")
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for s in range(args.steps):
-            graphs[s % reps].replay()
+        for _ in range(args.steps // G):
+            g_full.replay()
+        if g_rest is not None:
+            g_rest.replay()
         e1.record(stream)
     stream.synchronize()
     if sampler:
@@ -341,7 +359,7 @@ def run_ours(args):
                        "calls_per_step": len(CALLS), "variant": var, "engine": eng, "release": args.release,
                        "l2_defeat": f"inputs larger than L2: {reps} rotating replicas x {len(CALLS)} calls "
                                     f"({reps * len(CALLS) * per_call / 1e6:.0f} MB) vs L2 {l2 / 1e6:.0f} MB",
-                       "graph": "one CUDA graph per step (its 4 calls)",
+                       "graph": f"CUDA graphs of {G} steps ({G * len(CALLS)} calls) replayed back to back",
                        "parallelism": f"replicas x{world} (no collective)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4),

@@ -97,6 +97,11 @@
 // [role][step][event][chunk]; roles 0 producer, 1 mma, 2 splitter, 3 epilogue.
 #ifdef QLA_TRACE
 __device__ long long g_qla_trace[4 * 8 * 8 * 16];
+// Wall-clock (%globaltimer) entry and exit of every CTA of the last 64 calls:
+// [call % 64][CTA slot][entry, exit]; CTAs of consecutive calls are told apart
+// by the order of an atomic counter (the calls are stream-ordered).
+__device__ unsigned long long g_qla_gt[64 * 256 * 2];
+__device__ unsigned int g_qla_gt_count;
 #define QLA_TR(role, step, ev, ch)                                                                        \
   do {                                                                                                    \
     if (tr && (step) < 8 && (ch) < 16) g_qla_trace[(((role) * 8 + (step)) * 8 + (ev)) * 16 + (ch)] = clock64(); \
@@ -371,6 +376,16 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const SeqJob& j = p.job;
+#ifdef QLA_TRACE
+  __shared__ unsigned int gt_slot;
+  if (threadIdx.x == 0) {
+    const unsigned long long now = globaltimer();
+    const unsigned int idx = atomicAdd(&g_qla_gt_count, 1u);
+    const unsigned int nb = gridDim.x * gridDim.y;
+    gt_slot = ((idx / nb) % 64) * 256 + (idx % nb) % 256;
+    g_qla_gt[gt_slot * 2] = now;
+  }
+#endif
   const int u = blockIdx.y;
   const int chain = u / j.G;
   const int g = u - chain * j.G;
@@ -835,6 +850,10 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+#ifdef QLA_TRACE
+  __syncthreads();
+  if (threadIdx.x == 0) g_qla_gt[gt_slot * 2 + 1] = globaltimer();
+#endif
 }
 
 // ---------------------------------------------------------------- host side
@@ -912,6 +931,12 @@ cudaError_t launch_k(const SeqJob& j, int release, unsigned int* status, uint64_
 }  // namespace
 
 #ifdef QLA_TRACE
+extern "C" __attribute__((visibility("default"))) int qla_debug_walltimes(unsigned long long* out, int n) {
+  const int total = 64 * 256 * 2;
+  if (n > total) n = total;
+  return cudaMemcpyFromSymbol(out, g_qla_gt, sizeof(unsigned long long) * n) == cudaSuccess ? n : -1;
+}
+
 extern "C" __attribute__((visibility("default"))) int qla_debug_trace(long long* out, int n) {
   const int total = 4 * 8 * 8 * 16;
   if (n > total) n = total;
