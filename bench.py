@@ -316,29 +316,53 @@ def run_ours(args):
         hin = [dict(H=torch.from_numpy(p["H"]).pin_memory(), M=torch.from_numpy(p["M"]).pin_memory(),
                     h0=torch.from_numpy(p["h0"]).pin_memory(), out=torch.empty(p["H"].shape).pin_memory())
                for p in probs]
-        row = bufs[0]
         e2e_steps = max(3, min(args.steps, 50))
+        # Copies overlap compute as a user would pipeline them: inputs of a
+        # call go up on one stream, calls run on another, results come down on
+        # a third; each call's device buffers are reused two steps later (the
+        # replicas), once that earlier call's kernel and result copy are done.
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        nb = 2
 
-        def e2e_step():
-            for h, b in zip(hin, row):
-                b["H"].copy_(h["H"], non_blocking=True)
-                b["M"].copy_(h["M"], non_blocking=True)
-                b["h0"].copy_(h["h0"], non_blocking=True)
-                call(b, stream)
-                h["out"].copy_(b["out"], non_blocking=True)
+        def e2e_run(nsteps):
+            ev = lambda: torch.cuda.Event()  # noqa: E731
+            comp_done, out_done = {}, {}
+            for n in range(nsteps * len(CALLS)):
+                st, kind = divmod(n, len(CALLS))
+                b, h = bufs[st % nb][kind], hin[kind]
+                with torch.cuda.stream(s_in):
+                    if n - nb * len(CALLS) in comp_done:
+                        s_in.wait_event(comp_done[n - nb * len(CALLS)])
+                    b["H"].copy_(h["H"], non_blocking=True)
+                    b["M"].copy_(h["M"], non_blocking=True)
+                    b["h0"].copy_(h["h0"], non_blocking=True)
+                    e_in = ev()
+                    e_in.record(s_in)
+                with torch.cuda.stream(stream):
+                    stream.wait_event(e_in)
+                    if n - nb * len(CALLS) in out_done:
+                        stream.wait_event(out_done[n - nb * len(CALLS)])
+                    call(b, stream)
+                    comp_done[n] = ev()
+                    comp_done[n].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(comp_done[n])
+                    h["out"].copy_(b["out"], non_blocking=True)
+                    out_done[n] = ev()
+                    out_done[n].record(s_out)
+            return out_done[nsteps * len(CALLS) - 1]
 
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                e2e_step()
-        stream.synchronize()
+        last = e2e_run(3)
+        torch.cuda.synchronize()
         barrier(world)
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            a0.record(stream)
-            for _ in range(e2e_steps):
-                e2e_step()
-            a1.record(stream)
-        stream.synchronize()
+        a0.record(stream)
+        for si in (s_in, s_out):
+            si.wait_event(a0)
+        last = e2e_run(e2e_steps)
+        stream.wait_event(last)
+        a1.record(stream)
+        torch.cuda.synchronize()
         ems = max_over_ranks(a0.elapsed_time(a1), world)
         h2d = sum(h["H"].nbytes + h["M"].nbytes + h["h0"].nbytes for h in hin)
         d2h = sum(h["out"].nbytes for h in hin)
