@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
     const unsigned long long now = globaltimer();
     const unsigned int idx = atomicAdd(&g_qla_gt_count, 1u);
     const unsigned int nb = gridDim.x * gridDim.y;
-    gt_slot = ((idx / nb) % 64) * 256 + (idx % nb) % 256;
+    gt_slot = ((idx / nb) % 64) * 256 + (blockIdx.y * gridDim.x + blockIdx.x) % 256;
     g_qla_gt[gt_slot * 2] = now;
   }
 #endif
