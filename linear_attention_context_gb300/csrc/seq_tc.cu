@@ -123,7 +123,9 @@ constexpr uint32_t kTmemCols = 512;
 
 // TILES column tiles of VT columns share one CTA, one M stream and one A
 // split; with two, the issuers run all of tile 0's MMAs of a step before
-// tile 1's, so tile 0's epilogue overlaps tile 1's MMAs.
+// tile 1's, so tile 0's epilogue overlaps tile 1's MMAs.  (Two tiles, as
+// 2 x 32 or 2 x 16 columns, measured slower than one 32-column tile and are
+// not launched; the configuration stays generic.)
 template <int K, int TILES, int VT>
 struct Cfg {
   static constexpr int HALVES = K / 128;          // 128-row MMA blocks of the output
@@ -726,7 +728,8 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
       float a[EC], b[EC];
       const uint32_t base = tmem + lane_off + (uint32_t)((tl * C::HALVES + h) * C::NQ * VT + c0);
 #pragma unroll
-      for (int q = 0; q + 1 < C::NQ; q += 2) {
+      static_assert(C::NQ % 2 == 0, "chains are drained in pairs");
+      for (int q = 0; q < C::NQ; q += 2) {
         tmem_ld<EC>(base + q * VT, a);
         tmem_ld<EC>(base + (q + 1) * VT, b);
         tmem_wait_ld();
@@ -734,16 +737,6 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
         for (int c = 0; c < EC; c += 2) {  // acc += a + b, two columns per packed add
           const float2 sab = __fadd2_rn(make_float2(a[c], a[c + 1]), make_float2(b[c], b[c + 1]));
           const float2 r = __fadd2_rn(make_float2(acc[c], acc[c + 1]), sab);
-          acc[c] = r.x;
-          acc[c + 1] = r.y;
-        }
-      }
-      if constexpr (C::NQ % 2 == 1) {  // the last (small) chain alone
-        tmem_ld<EC>(base + (C::NQ - 1) * VT, a);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < EC; c += 2) {
-          const float2 r = __fadd2_rn(make_float2(acc[c], acc[c + 1]), make_float2(a[c], a[c + 1]));
           acc[c] = r.x;
           acc[c + 1] = r.y;
         }
