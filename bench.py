@@ -45,6 +45,14 @@ def algorithmic_bytes(chains, S_, K_, V_, with_init=True):
     return 4 * chains * ((S_ - 1) * K_ * V_ + (S_ - 1) * K_ * K_ + S_ * K_ * V_ + (K_ * V_ if with_init else 0))
 
 
+def scan_groups(S_):
+    """The scan's automatic group count for S segments (G ~ sqrt(2 S), as the
+    library chooses it)."""
+    G = max(1, round(math.sqrt(2.0 * S_)))
+    L = (S_ + G - 1) // G
+    return (S_ + L - 1) // L
+
+
 def algorithmic_flops(chains, S_, K_, V_):
     return 2 * chains * (S_ - 1) * K_ * K_ * V_
 
@@ -75,6 +83,46 @@ def load_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def compute_peaks(dev):
+    """The two compute ceilings the path could be bound by, on this device:
+    dense TF32 tensor throughput, measured (cuBLAS fp32 matmul with TF32
+    allowed, 8192^3, best of 5, CUDA events), and the FFMA ceiling computed
+    from the SM count (128 fp32 FMA lanes per SM per clock) at the maximum SM
+    clock.  Reported beside the HBM roofline."""
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    n = 8192
+    a = torch.randn(n, n, device=dev)
+    b = torch.randn(n, n, device=dev)
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        for _ in range(2):
+            torch.matmul(a, b)
+        best = float("inf")
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    del a, b
+    max_mhz = 2070.0
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            max_mhz = float(json.load(f).get("sm_max_mhz", max_mhz))
+    return {"tf32_tflops": round(2 * n ** 3 / (best * 1e-3) / 1e12, 1),
+            "tf32_how": "torch.matmul fp32 8192^3, TF32 allowed, best of 5",
+            "ffma_tflops": round(sms * 128 * 2 * max_mhz * 1e6 / 1e12, 1),
+            "ffma_how": f"{sms} SMs x 128 FMA/clk x 2 flop x {max_mhz:.0f} MHz",
+            "sms": sms, "l2_bytes": props.L2_cache_size}
 
 
 class ClockSampler:
@@ -369,6 +417,7 @@ def run_ours(args):
         e2e = {"value": round(job_us_per_call(ems, e2e_steps * len(CALLS), world), 3), "unit": "us",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
+    peaks = compute_peaks(dev) if rank == 0 and not args.skip_peaks else None
     cpu = None
     if rank == 0 and not args.skip_cpu:
         cpu = cpu_baseline(probs, budget_s=args.cpu_budget)
@@ -395,6 +444,15 @@ def run_ours(args):
                          "flops_per_call": algorithmic_flops(HEADS, S, K, V)},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_calls * launches_per_call, "clocks": clocks,
         }
+        if peaks:
+            # the tensor-pipe view of the same calls: 3xTF32 executes 3x the algorithmic flops
+            executed = 3 * algorithmic_flops(HEADS, S, K, V) if eng == "tc" else algorithmic_flops(HEADS, S, K, V)
+            rate = executed / (us_per_call_rank * 1e-6) / 1e12
+            ceiling = peaks["tf32_tflops"] if eng == "tc" else peaks["ffma_tflops"]
+            line["compute"] = {"executed_tflops": round(rate, 1),
+                               "ceiling_tflops": ceiling,
+                               "ceiling": "tf32 tensor (measured)" if eng == "tc" else "ffma (computed)",
+                               "frac": round(rate / ceiling, 4), "peaks": peaks}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -476,6 +534,7 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(0)
     stream = torch.cuda.Stream(dev)
+    lines = []
     for heads in qi.SWEEP_HEADS:
         for S_ in qi.SWEEP_S:
             c = qi.sweep_case(heads, S_)
@@ -508,10 +567,23 @@ def run_sweep(args):
                     stream.synchronize()
                     times[variant] = e0.elapsed_time(e1) * 1e3 / (10 * args.sweep_reps)
                 auto = qla.resolve(1, heads, S_, 128, 128, layout)[0]
-                print(json.dumps({"sweep": {"heads": heads, "S": S_, "layout": layout, "direction": direction},
-                                  "us_per_call": {k: round(v, 2) for k, v in times.items()},
-                                  "auto": auto, "bytes_per_call": algorithmic_bytes(heads, S_, 128, 128)}),
-                      flush=True)
+                # the scan's executed tensor work (3xTF32: 3x) per chain: group
+                # products of M, S steps of K^3; group recurrences (S steps),
+                # carries (G) and re-runs (S - G), K^2 V each
+                Kk = Vv = 128
+                G = scan_groups(S_)
+                flops = 3 * 2 * heads * (S_ * Kk ** 3 + 2 * S_ * Kk * Kk * Vv)
+                rate = flops / (times["scan"] * 1e-6) / 1e12
+                lines.append({"sweep": {"heads": heads, "S": S_, "layout": layout, "direction": direction},
+                              "us_per_call": {k: round(v, 2) for k, v in times.items()},
+                              "auto": auto, "bytes_per_call": algorithmic_bytes(heads, S_, 128, 128),
+                              "scan_tensor": {"groups": G, "executed_tflops": round(rate, 1)}})
+    # the matmul peak last: its power draw would lower the clocks of the timings
+    peaks = compute_peaks(dev)
+    print(json.dumps({"compute_peaks": peaks}), flush=True)
+    for ln in lines:
+        ln["scan_tensor"]["frac_of_tf32"] = round(ln["scan_tensor"]["executed_tflops"] / peaks["tf32_tflops"], 4)
+        print(json.dumps(ln), flush=True)
 
 
 def run_large(args):
@@ -566,6 +638,7 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-check", action="store_true")
+    ap.add_argument("--skip-peaks", action="store_true", help="skip the TF32 matmul peak measurement")
     ap.add_argument("--sweep", action="store_true", help="time sequential vs scan over the low batch*heads sweep")
     ap.add_argument("--sweep-reps", type=int, default=20)
     ap.add_argument("--large", action="store_true", help="time the 4 x 64-head K=V=256 S=32 workload")
