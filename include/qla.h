@@ -87,7 +87,8 @@ enum {
 enum {
   QLA_ENGINE_AUTO = 0,    /* tensor-core engine where the shape allows, else SIMT */
   QLA_ENGINE_SIMT = 1,    /* plain FFMA kernel, no TMA: any supported K, V */
-                          /* 2 is not assigned: an engine value of 2 is rejected */
+  QLA_ENGINE_TC_F16 = 2,  /* the same pipeline with tcgen05 kind::f16 MMAs on power-of-two-scaled
+                             fp16 hi/lo operand pairs (22 significant bits, as 3xTF32): K = 128 only */
   QLA_ENGINE_TC = 3       /* warp-specialised TMA/mbarrier pipeline, tcgen05 3xTF32 propagate */
 };
 

@@ -183,7 +183,8 @@ int auto_groups(int S) {
 }
 
 bool known_engine(int engine) {
-  return engine == QLA_ENGINE_AUTO || engine == QLA_ENGINE_SIMT || engine == QLA_ENGINE_TC;
+  return engine == QLA_ENGINE_AUTO || engine == QLA_ENGINE_SIMT || engine == QLA_ENGINE_TC ||
+         engine == QLA_ENGINE_TC_F16;
 }
 
 int resolve_engine(const Shape& s, int engine) {
@@ -193,6 +194,7 @@ int resolve_engine(const Shape& s, int engine) {
 
 // The engine a scan phase runs on: phase 1a's V' = K may differ from V.
 int engine_for(const SeqJob& j, int engine) {
+  if (engine == QLA_ENGINE_TC_F16 && !tc_f16_supports(j.K, j.V)) engine = QLA_ENGINE_TC;
   if (engine == QLA_ENGINE_TC && !tc_supports(j.K, j.V)) return QLA_ENGINE_SIMT;
   return engine;
 }
@@ -220,6 +222,11 @@ int launch_seq(const SeqJob& job, int engine, int release, const DeviceInfo* d, 
       if (!tc_supports(j.K, j.V))
         return fail(QLA_ERR_UNSUPPORTED, "the tensor-core engine takes K in {128, 256} (got K=%d, V=%d)", j.K, j.V);
       e = launch_seq_tc(j, release, d->status_word, kWaitLimitNs, 0, stream);
+      break;
+    case QLA_ENGINE_TC_F16:
+      if (!tc_f16_supports(j.K, j.V))
+        return fail(QLA_ERR_UNSUPPORTED, "the fp16-pair tensor-core engine takes K = 128 (got K=%d, V=%d)", j.K, j.V);
+      e = launch_seq_tc_f16(j, release, d->status_word, kWaitLimitNs, 0, stream);
       break;
     default:
       return fail(QLA_ERR_UNSUPPORTED, "engine %d is not available in this build", engine);

@@ -78,6 +78,13 @@ bool tc_supports(int K, int V);
 cudaError_t launch_seq_tc(const SeqJob& job, int release, unsigned int* status, uint64_t limit_ns,
                           int stall_test, cudaStream_t stream);
 
+// seq_tc_f16.cu: the same pipeline with kind::f16 MMAs on power-of-two-scaled
+// fp16 hi/lo operand pairs.  K = 128, V a multiple of 32; other arguments as
+// launch_seq_tc.
+bool tc_f16_supports(int K, int V);
+cudaError_t launch_seq_tc_f16(const SeqJob& job, int release, unsigned int* status, uint64_t limit_ns,
+                              int stall_test, cudaStream_t stream);
+
 // Bound on every device-side wait of the pipelined engines.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 

@@ -68,7 +68,7 @@ def call(L, H=FAKE, M=FAKE + (1 << 32), h0=None, out=FAKE + (2 << 32), fin=None,
     (dict(H=None), -1), (dict(M=None), -1), (dict(out=None), -1),
     (dict(B=0), -1), (dict(heads=-1), -1), (dict(S=0), -1), (dict(K=0), -1),
     (dict(layout=2), -1), (dict(direction=-1), -1),
-    (dict(variant=3), -1), (dict(engine=9), -1), (dict(engine=2), -1), (dict(release=7), -1), (dict(group=-1), -1),
+    (dict(variant=3), -1), (dict(engine=9), -1), (dict(engine=4), -1), (dict(release=7), -1), (dict(group=-1), -1),
     (dict(K=48), -2), (dict(V=288), -2), (dict(K=16), -2), (dict(V=100), -2),
     (dict(H=FAKE + 4), -3), (dict(M=FAKE + (1 << 32) + 8), -3), (dict(out=FAKE + (2 << 32) + 12), -3),
     (dict(h0=FAKE + (3 << 32) + 2), -3), (dict(fin=FAKE + (4 << 32) + 1), -3),
@@ -131,7 +131,7 @@ def call_varlen(L, H=FAKE, M=FAKE + (1 << 32), h0=None, out=FAKE + (2 << 32), fi
 @pytest.mark.parametrize("kw,status", [
     (dict(cu=None), -1), (dict(H=None), -1), (dict(M=None), -1), (dict(out=None), -1),
     (dict(N=0), -1), (dict(T=-1), -1), (dict(heads=0), -1), (dict(layout=3), -1), (dict(direction=2), -1),
-    (dict(engine=2), -1), (dict(K=48), -2), (dict(V=300), -2), (dict(N=70000, heads=1), -2),
+    (dict(engine=4), -1), (dict(K=48), -2), (dict(V=300), -2), (dict(N=70000, heads=1), -2),
     (dict(cu=FAKE + (5 << 32) + 2), -3), (dict(H=FAKE + 8), -3),
     (dict(cu=FAKE + 64), -4), (dict(out=FAKE + 4096), -4), (dict(h0=FAKE + (1 << 32) + 16), -4),
 ])

@@ -101,6 +101,52 @@ def test_edge_shapes(shape, layout, direction, engine):
     assert_parity(fin2, rfin, what="edge final only")
 
 
+# Magnitudes far from 1: the fp16-pair engine scales its operands by powers of
+# two (fp16 alone holds 6e-8 .. 65504); the other engines compute in fp32.
+RANGES = [
+    # (m_scale, h_scale, init_scale): M = m_scale * orthogonal
+    (0.99, 1e-20, 1e-20),  # tiny states
+    (0.99, 1e12, 1e12),    # states far above fp16's range
+    (1e-9, 1.0, 1.0),      # tiny propagation matrices
+    (3e5, 1.0, 1.0),       # propagation entries above fp16's range
+    (0.99, 0.0, 1.0),      # no local states: pure propagation of h_init
+]
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+@pytest.mark.parametrize("direction", DIRS)
+@pytest.mark.parametrize("rng", RANGES, ids=lambda r: "m{:g}_h{:g}_i{:g}".format(*r))
+def test_dynamic_range(rng, direction, engine):
+    m_scale, h_scale, init_scale = rng
+    c = qi.Case(B=1, heads=2, S=4, K=128, V=64, seed=91, m_kind="orthogonal", m_scale=m_scale,
+                h_scale=h_scale, init_kind="gaussian", init_scale=init_scale)
+    for layout in LAYOUTS:
+        H, M, h0 = qi.make_inputs(c, layout)
+        ref, rfin = oracle.cp_correct(H, M, h0, layout, direction, want_final=True)
+        got, fin = run(H, M, h0, layout, direction, engine=engine, final=True)
+        assert np.isfinite(got).all() and np.isfinite(fin).all()
+        assert_parity(got, ref, what=f"range {rng} {layout} {direction} {engine}")
+        assert_parity(fin, rfin, what=f"range {rng} final")
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+@pytest.mark.parametrize("direction", DIRS)
+def test_rows_of_different_magnitude(direction, engine):
+    """M = diag(d) Q with d spanning 10^-6 .. 10^6 (and rows of zeros): one
+    scale per matrix must serve rows twelve decades apart."""
+    c = qi.Case(B=1, heads=2, S=5, K=128, V=64, seed=92, m_kind="orthogonal", m_scale=1.0, h_scale=1.0,
+                init_kind="gaussian")
+    d = np.logspace(-6, 6, 128)
+    d[::17] = 0.0
+    for layout in LAYOUTS:
+        H, M, h0 = qi.make_inputs(c, layout)
+        M = np.ascontiguousarray(M * d[:, None]).astype(np.float32)
+        ref, rfin = oracle.cp_correct(H, M, h0, layout, direction, want_final=True)
+        got, fin = run(H, M, h0, layout, direction, engine=engine, final=True)
+        assert_parity(got, ref, what=f"row magnitudes {layout} {direction} {engine}")
+        assert_parity(fin, rfin, what="row magnitudes final")
+
+
 @pytest.mark.parametrize("engine", ENGINES)
 @pytest.mark.parametrize("direction", DIRS)
 @pytest.mark.parametrize("layout", LAYOUTS)
