@@ -180,15 +180,17 @@ QLA_API const char* qla_last_error(void);
 QLA_API int qla_device_status(int* flags);
 
 /*
- * Self-test of the bounded waits: launches the warp-specialised pipeline on a
- * tiny problem in a mode where one consumer waits on a barrier that nothing
- * arrives on.  The wait gives up after `wait_limit_us` microseconds, the kernel
- * records QLA_ERR_TIMEOUT in the device status word, drains and returns.  The
- * buffers are as for qla_cp_correct with K = V = 128; returns the launch
- * status.  Used by the tests to show that a stalled pipeline ends on its own.
+ * Self-test of the bounded waits: launches a warp-specialised pipeline
+ * (engine QLA_ENGINE_TC or QLA_ENGINE_TC_F16; any other value is
+ * QLA_ERR_INVALID_ARG) on a tiny problem in a mode where one consumer waits
+ * on a barrier that nothing arrives on.  The wait gives up after
+ * `wait_limit_us` microseconds, the kernel records QLA_ERR_TIMEOUT in the
+ * device status word, drains and returns.  The buffers are as for
+ * qla_cp_correct with K = V = 128; returns the launch status.  Used by the
+ * tests to show that a stalled pipeline ends on its own.
  */
 QLA_API int qla_selftest_stalled_wait(const float* H, const float* M, float* out, int S,
-                              int wait_limit_us, void* stream);
+                              int wait_limit_us, int engine, void* stream);
 
 /*
  * The scan variant without any allocation (this entry point has no

@@ -78,7 +78,7 @@ def lib():
         L.qla_last_error.restype = ctypes.c_char_p
         L.qla_device_status.argtypes = [ctypes.POINTER(ci)]
         L.qla_device_status.restype = ci
-        L.qla_selftest_stalled_wait.argtypes = [vp, vp, vp, ci, ci, vp]
+        L.qla_selftest_stalled_wait.argtypes = [vp, vp, vp, ci, ci, ci, vp]
         L.qla_selftest_stalled_wait.restype = ci
         L.qla_cp_correct_scan_static.argtypes = [vp, vp, vp, vp, vp] + [ci] * 10 + [vp]
         L.qla_cp_correct_scan_static.restype = ci

@@ -584,7 +584,8 @@ int qla_device_status(int* flags) {
   return w ? QLA_ERR_INVALID_ARG : QLA_OK;
 }
 
-int qla_selftest_stalled_wait(const float* H, const float* M, float* out, int S, int wait_limit_us, void* stream) {
+int qla_selftest_stalled_wait(const float* H, const float* M, float* out, int S, int wait_limit_us, int engine,
+                              void* stream) {
   t_last_error.clear();
   Shape s{1, 1, S, 128, 128, QLA_LAYOUT_KV, QLA_FORWARD};
   int st = check_args(H, M, nullptr, out, nullptr, s);
@@ -592,10 +593,16 @@ int qla_selftest_stalled_wait(const float* H, const float* M, float* out, int S,
   if (S < 2) return fail(QLA_ERR_INVALID_ARG, "the stalled-wait self-test needs S >= 2");
   if (wait_limit_us < 1 || wait_limit_us > 10000000)
     return fail(QLA_ERR_INVALID_ARG, "wait_limit_us must be in [1, 10^7]");
+  if (engine != QLA_ENGINE_TC && engine != QLA_ENGINE_TC_F16)
+    return fail(QLA_ERR_INVALID_ARG, "the stalled-wait self-test takes a pipelined engine (got %d)", engine);
   DeviceInfo* d = nullptr;
   if ((st = current_device(&d)) != QLA_OK) return st;
-  cudaError_t e = launch_seq_tc(plain_job(H, M, nullptr, out, nullptr, s), QLA_RELEASE_MEMBAR, d->status_word,
-                                (uint64_t)wait_limit_us * 1000ull, 1, static_cast<cudaStream_t>(stream));
+  const uint64_t limit = (uint64_t)wait_limit_us * 1000ull;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  SeqJob j = plain_job(H, M, nullptr, out, nullptr, s);
+  j.status = d->status_word;
+  cudaError_t e = engine == QLA_ENGINE_TC ? launch_seq_tc(j, QLA_RELEASE_MEMBAR, d->status_word, limit, 1, cs)
+                                          : launch_seq_tc_f16(j, QLA_RELEASE_MEMBAR, d->status_word, limit, 1, cs);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return QLA_OK;
 }

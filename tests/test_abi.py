@@ -137,3 +137,12 @@ def call_varlen(L, H=FAKE, M=FAKE + (1 << 32), h0=None, out=FAKE + (2 << 32), fi
 ])
 def test_varlen_argument_checks(L, kw, status):
     assert call_varlen(L, **kw) == status
+
+
+def test_stalled_wait_selftest_argument_checks(L):
+    vp = ctypes.c_void_p
+    H, M, out = vp(FAKE), vp(FAKE + (1 << 32)), vp(FAKE + (2 << 32))
+    assert L.qla_selftest_stalled_wait(H, M, out, 3, 1000, 1, None) == -1    # FFMA engine has no pipeline
+    assert L.qla_selftest_stalled_wait(H, M, out, 3, 1000, 0, None) == -1    # automatic choice is not an engine
+    assert L.qla_selftest_stalled_wait(H, M, out, 1, 1000, 3, None) == -1    # needs S >= 2
+    assert L.qla_selftest_stalled_wait(H, M, out, 3, 0, 3, None) == -1       # limit outside [1, 10^7]
