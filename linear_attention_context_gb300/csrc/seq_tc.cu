@@ -501,7 +501,8 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
       for (int step = 0; step < nsteps && ok; ++step) {
         const int seg = seg_of(step);
         const int64_t mrow0 = (cbase + seg) * K;
-        if (p.has_h) {
+        auto load_h = [&]() {
+          if (!p.has_h) return;
           const int slot = step & 1;
           const int64_t hrow0 = (cbase + seg) * hrows;
           for (int tl = 0; tl < TILES && ok; ++tl) {
@@ -515,20 +516,31 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
               tma_load_2d(dst, &p.map_h, 0, (int32_t)(hrow0 + v0), &ctl->h_full[tl][slot]);
             ++hissued[tl];
           }
-          if (!ok) break;
           QLA_TR(0, step, 0, 0);
-        }
-        for (int c = 0; c < C::CPS; ++c, ++mit) {
-          const int stage = mit % C::NM;
-          if (!(ok = mbar_wait(&ctl->m_empty[stage], ((mit / C::NM) & 1) ^ 1, wc))) break;
-          QLA_TR(0, step, 1, c);
-          mbar_arrive_expect_tx(&ctl->m_full[stage], kChunkBytes);
-          const int kc = c / C::HALVES, h = c % C::HALVES;
-          uint8_t* dst = smem + C::OFF_M + stage * kChunkBytes;
-          if (fwd)  // A = M: rows 128h.., columns 32kc..  (128-byte swizzle, box 32 x 128)
-            tma_load_2d(dst, &p.map_m, 32 * kc, (int32_t)(mrow0 + 128 * h), &ctl->m_full[stage]);
-          else      // A = M^T: M rows 32kc.., columns 128h..  (box 128 x 32)
-            tma_load_2d(dst, &p.map_m, 128 * h, (int32_t)(mrow0 + 32 * kc), &ctl->m_full[stage]);
+        };
+        auto load_m = [&]() {
+          for (int c = 0; c < C::CPS && ok; ++c, ++mit) {
+            const int stage = mit % C::NM;
+            if (!(ok = mbar_wait(&ctl->m_empty[stage], ((mit / C::NM) & 1) ^ 1, wc))) break;
+            QLA_TR(0, step, 1, c);
+            mbar_arrive_expect_tx(&ctl->m_full[stage], kChunkBytes);
+            const int kc = c / C::HALVES, h = c % C::HALVES;
+            uint8_t* dst = smem + C::OFF_M + stage * kChunkBytes;
+            if (fwd)  // A = M: rows 128h.., columns 32kc..  (128-byte swizzle, box 32 x 128)
+              tma_load_2d(dst, &p.map_m, 32 * kc, (int32_t)(mrow0 + 128 * h), &ctl->m_full[stage]);
+            else      // A = M^T: M rows 32kc.., columns 128h..  (box 128 x 32)
+              tma_load_2d(dst, &p.map_m, 128 * h, (int32_t)(mrow0 + 32 * kc), &ctl->m_full[stage]);
+          }
+        };
+        // The first step needs its M chunks before its H tile (the split and
+        // the MMAs come before the drain); later steps' M chunks wait for ring
+        // slots, so their H tile goes first.
+        if (step == 0) {
+          load_m();
+          if (ok) load_h();
+        } else {
+          load_h();
+          if (ok) load_m();
         }
       }
       // Drain: every issued load must land before shared memory goes away.
