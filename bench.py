@@ -586,6 +586,60 @@ def run_sweep(args):
         print(json.dumps(ln), flush=True)
 
 
+def run_varlen(args):
+    """Variable-length calls (K=V=128, Householder M): sequences of different
+    segment counts packed along the segment axis, the sequential variant
+    against the group scan.  One JSON line per case; not the headline metric."""
+    import numpy as np
+    import torch
+
+    import linear_attention_context_gb300 as qla
+    import qla_inputs as qi
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream(dev)
+    cases = [  # (lengths, heads)
+        ([128, 37, 0, 90], 1),
+        ([64, 64], 2),
+        ([200, 3, 17, 41, 9, 0, 120, 8], 1),
+        ([8] * 32, 32),
+    ]
+    for lengths, heads in cases:
+        H, M, h0, cu = qi.make_varlen_inputs(lengths, heads, 128, 128, seed=51, m_kind="householder",
+                                             h_scale=0.1, init_scale=0.1)
+        Hd, Md, h0d = (torch.from_numpy(np.ascontiguousarray(a)).to(dev) for a in (H, M, h0))
+        cud = torch.from_numpy(cu.astype(np.int32)).to(dev)
+        out = torch.empty_like(Hd)
+        bound = max(lengths)
+        times = {}
+        for variant in ("seq", "scan"):
+            def call():
+                qla.cp_correct_varlen(Hd, Md, cud, h0d, out, variant=variant, max_segments=bound, stream=stream)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    call()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for _ in range(10):
+                        call()
+            stream.synchronize()
+            for _ in range(3):
+                g.replay()
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(args.sweep_reps):
+                    g.replay()
+                e1.record(stream)
+            stream.synchronize()
+            times[variant] = e0.elapsed_time(e1) * 1e3 / (10 * args.sweep_reps)
+        print(json.dumps({"varlen": {"lengths": lengths, "heads": heads, "K": 128, "V": 128},
+                          "us_per_call": {k: round(v, 2) for k, v in times.items()}}), flush=True)
+    if qla.device_status() != 0:
+        raise SystemExit("device status word set during the varlen timings")
+
+
 def run_large(args):
     """The 4 x 64-head, K=V=256, S=32 workload (6.4 GB of states), forward
     and reverse kv: one call at a time, CUDA events, after two warm-up calls.
@@ -642,6 +696,7 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="time sequential vs scan over the low batch*heads sweep")
     ap.add_argument("--sweep-reps", type=int, default=20)
     ap.add_argument("--large", action="store_true", help="time the 4 x 64-head K=V=256 S=32 workload")
+    ap.add_argument("--varlen", action="store_true", help="time variable-length calls, sequential vs scan")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -649,6 +704,8 @@ def main():
         run_sweep(args)
     elif args.large:
         run_large(args)
+    elif args.varlen:
+        run_varlen(args)
     else:
         run_ours(args)
 

@@ -117,7 +117,8 @@ QLA_API int qla_cp_correct(const float* H, const float* M, const float* h_init, 
  *                visited as well).  out may be NULL when final_state is not.
  *   variant      QLA_VARIANT_*;  engine QLA_ENGINE_*;  release QLA_RELEASE_*
  *                (ignored by engines without a TMA producer).
- *   scan_group   segments per scan group (QLA_VARIANT_SCAN), 0 = automatic.
+ *   scan_group   number of scan groups G (QLA_VARIANT_SCAN), 0 = automatic;
+ *                each group covers ceil(S / G) consecutive segments.
  * The scan variant needs qla_scan_workspace_bytes() of device scratch, which
  * it takes from the stream-ordered allocator (cudaMallocAsync on `stream`) and
  * returns on the same stream.
@@ -144,15 +145,35 @@ QLA_API int qla_cp_correct_ex(const float* H, const float* M, const float* h_ini
  *                its initial state.
  *   cu_seg       DEVICE pointer to N + 1 int32 offsets, cu_seg[0] = 0,
  *                non-decreasing, cu_seg[N] = T (4-byte aligned).
- * Sequential variant only; engine QLA_ENGINE_*.  The host checks everything
- * but the offsets' values; a kernel that finds a chain's offsets outside
- * [0, T] or decreasing skips that chain (reads and writes nothing for it) and
- * sets bit 1 (value 2) of the device status word (qla_device_status).
+ * Sequential variant; engine QLA_ENGINE_*.  The host checks everything but
+ * the offsets' values; a kernel that finds a chain's offsets outside [0, T]
+ * or decreasing skips that chain (reads and writes nothing for it) and sets
+ * bit 1 (value 2) of the device status word (qla_device_status).
  * Requires N * heads <= 65535.
  */
 QLA_API int qla_cp_correct_varlen(const float* H, const float* M, const float* h_init, float* out,
                           float* final_state, const int* cu_seg, int N, int T, int heads, int K,
                           int V, int layout, int direction, int engine, void* stream);
+
+/*
+ * qla_cp_correct_varlen with a variant choice.  The scan variant needs the
+ * groups' size on the host without reading the device offsets, so the caller
+ * passes `max_segments`, an upper bound on every sequence's segment count
+ * (1 .. T; 0 means T; ignored by the sequential variant).  Every chain is cut
+ * into G groups of L consecutive segments, G = scan_group (0: automatic from
+ * max_segments) and L = ceil(max_segments / G); groups past a sequence's end
+ * are empty (their aggregates are the identity and zero).  A sequence longer
+ * than max_segments is treated like invalid offsets: bit 1 of the device
+ * status word is set and that chain's outputs are left unspecified.
+ * variant QLA_VARIANT_AUTO picks the scan when max_segments >= 24 and
+ * N * heads * ceil(V / 32) <= 16 (as qla_resolve for fixed lengths).  The scan
+ * allocates its workspace with cudaMallocAsync on `stream`
+ * (N * heads * G * (K*K + 2*K*V) * 4 bytes) and frees it the same way.
+ */
+QLA_API int qla_cp_correct_varlen_ex(const float* H, const float* M, const float* h_init, float* out,
+                          float* final_state, const int* cu_seg, int N, int T, int heads, int K,
+                          int V, int layout, int direction, int variant, int engine,
+                          int max_segments, int scan_group, void* stream);
 
 /* Bytes of device scratch the scan variant uses for this shape and group
  * size (0 = automatic); 0 when the scan does not apply. */

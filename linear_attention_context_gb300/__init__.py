@@ -31,7 +31,8 @@ STATUS = {0: "QLA_OK", -1: "QLA_ERR_INVALID_ARG", -2: "QLA_ERR_UNSUPPORTED", -3:
           -4: "QLA_ERR_ALIAS", -5: "QLA_ERR_CUDA", -6: "QLA_ERR_ARCH", -7: "QLA_ERR_TIMEOUT"}
 
 # Every function include/qla.h declares.
-EXPORTS = ("qla_cp_correct", "qla_cp_correct_ex", "qla_cp_correct_varlen", "qla_scan_workspace_bytes",
+EXPORTS = ("qla_cp_correct", "qla_cp_correct_ex", "qla_cp_correct_varlen", "qla_cp_correct_varlen_ex",
+           "qla_scan_workspace_bytes",
            "qla_resolve", "qla_status_string", "qla_last_error", "qla_device_status", "qla_selftest_stalled_wait",
            "qla_cp_correct_scan_static", "qla_version")
 
@@ -68,6 +69,8 @@ def lib():
         L.qla_cp_correct_ex.restype = ci
         L.qla_cp_correct_varlen.argtypes = [vp, vp, vp, vp, vp, vp] + [ci] * 8 + [vp]
         L.qla_cp_correct_varlen.restype = ci
+        L.qla_cp_correct_varlen_ex.argtypes = [vp, vp, vp, vp, vp, vp] + [ci] * 11 + [vp]
+        L.qla_cp_correct_varlen_ex.restype = ci
         L.qla_scan_workspace_bytes.argtypes = [ci] * 6
         L.qla_scan_workspace_bytes.restype = cz
         L.qla_resolve.argtypes = [ci] * 6 + [ctypes.POINTER(ci), ctypes.POINTER(ci)]
@@ -169,7 +172,7 @@ def cp_correct(H, M, h_init=None, out=None, *, layout="kv", direction="fwd", fin
 
 
 def cp_correct_varlen(H, M, cu_seg, h_init=None, out=None, *, layout="kv", direction="fwd", final_state=None,
-                      engine="auto", stream=None, want_out=True):
+                      engine="auto", stream=None, want_out=True, variant="seq", max_segments=0, scan_group=0):
     """Variable-length form: N sequences packed along the segment axis.
 
     H: [heads, T, K, V] (kv) or [heads, T, V, K] (vk) float32 CUDA tensor;
@@ -178,7 +181,10 @@ def cp_correct_varlen(H, M, cu_seg, h_init=None, out=None, *, layout="kv", direc
     final_state: [N, heads, state] or None; out like H (may be H), or None to
     allocate.  Returns ``out`` (None when ``want_out`` is False).  Offsets are
     checked on the device: invalid ones skip their chains and set bit 1 of the
-    status word (``device_status()``)."""
+    status word (``device_status()``).  ``variant`` "seq", "scan" or "auto";
+    the scan sizes its groups from ``max_segments`` (an upper bound on every
+    sequence's segment count, 0 = T) and ``scan_group`` (group count, 0 =
+    automatic); a longer sequence is flagged like invalid offsets."""
     import torch
     if layout not in LAYOUTS or direction not in DIRECTIONS:
         raise ValueError(f"layout {layout!r} / direction {direction!r}")
@@ -204,9 +210,10 @@ def cp_correct_varlen(H, M, cu_seg, h_init=None, out=None, *, layout="kv", direc
     if out is not None:
         _check_tensor("out", out, dev, H.shape)
     with torch.cuda.device(dev):
-        rc = lib().qla_cp_correct_varlen(_ptr(H), _ptr(M), _ptr(h_init), _ptr(out), _ptr(final_state),
-                                         _ptr(cu_seg), N, T, heads, K, V, LAYOUTS[layout], DIRECTIONS[direction],
-                                         ENGINES[engine], _stream_handle(stream))
+        rc = lib().qla_cp_correct_varlen_ex(_ptr(H), _ptr(M), _ptr(h_init), _ptr(out), _ptr(final_state),
+                                            _ptr(cu_seg), N, T, heads, K, V, LAYOUTS[layout],
+                                            DIRECTIONS[direction], VARIANTS[variant], ENGINES[engine],
+                                            int(max_segments), int(scan_group), _stream_handle(stream))
     check(rc)
     return out
 

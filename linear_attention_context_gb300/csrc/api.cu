@@ -430,6 +430,82 @@ int run_scan_in(const float* H, const float* M, const float* h_init, float* out,
   return QLA_OK;
 }
 
+// The scan variant for variable-length calls.  Every chain gets G groups of
+// L segments, L = ceil(Smax / G) from the caller's bound Smax on any
+// sequence's length; groups past a sequence's end are empty, so their
+// aggregates are the identity (1a) and zero (1b), and phase 2 steps through
+// them unchanged (in either direction).  Phases 1a, 1b and 3 locate each
+// (chain, group) through the offsets; phase 2 is a fixed-length recurrence
+// over the G aggregates of each chain.
+int run_scan_varlen(const SeqJob& vj, const Shape& s, int engine, int group, const DeviceInfo* d,
+                    cudaStream_t stream) {
+  const int G = group > 0 ? std::min(group, s.S) : auto_groups(s.S);
+  const int L = (s.S + G - 1) / G;
+  const int Gr = (s.S + L - 1) / L;  // groups actually formed
+  const int64_t chains = vj.nchains;
+  const size_t bytes = (size_t)chains * Gr * ((size_t)s.K * s.K + 2 * (size_t)s.state()) * sizeof(float);
+  float* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), bytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(scan workspace)");
+  float* Aagg = ws;
+  float* bagg = Aagg + (size_t)chains * Gr * s.K * s.K;
+  float* carry = bagg + (size_t)chains * Gr * s.state();
+  int st = QLA_OK;
+  {  // 1a: group products of M, forward, kv view, from the identity
+    SeqJob j = vj;
+    j.H = nullptr;
+    j.init = nullptr;
+    j.init_mode = kInitIdentity;
+    j.out = nullptr;
+    j.fin = Aagg;
+    j.fin_unit_stride = (int64_t)s.K * s.K;
+    j.L = L;
+    j.G = Gr;
+    j.V = s.K;
+    j.layout = QLA_LAYOUT_KV;
+    j.direction = QLA_FORWARD;
+    st = launch_seq(j, engine_for(j, engine), QLA_RELEASE_MEMBAR, d, stream);
+  }
+  if (st == QLA_OK) {  // 1b: group recurrences from zero
+    SeqJob j = vj;
+    j.init = nullptr;
+    j.init_mode = kInitZero;
+    j.out = nullptr;
+    j.fin = bagg;
+    j.fin_unit_stride = s.state();
+    j.L = L;
+    j.G = Gr;
+    st = launch_seq(j, engine_for(j, engine), QLA_RELEASE_MEMBAR, d, stream);
+  }
+  if (st == QLA_OK) {  // 2: carries across the group aggregates (fixed length Gr per chain)
+    SeqJob j = vj;
+    j.cu_seg = nullptr;
+    j.H = bagg;
+    j.M = Aagg;
+    j.h_chain_stride = (int64_t)Gr * s.state();
+    j.m_chain_stride = (int64_t)Gr * s.K * s.K;
+    j.out = carry;
+    j.S = Gr;
+    j.L = Gr;
+    j.G = 1;
+    j.nstates = chains * Gr;
+    st = launch_seq(j, engine_for(j, engine), QLA_RELEASE_MEMBAR, d, stream);
+  }
+  if (st == QLA_OK && vj.out) {  // 3: re-run each group from its entering state
+    SeqJob j = vj;
+    j.init = carry;
+    j.init_mode = kInitPointer;
+    j.init_unit_stride = s.state();
+    j.fin = nullptr;
+    j.L = L;
+    j.G = Gr;
+    st = launch_seq(j, engine_for(j, engine), QLA_RELEASE_MEMBAR, d, stream);
+  }
+  e = cudaFreeAsync(ws, stream);
+  if (st == QLA_OK && e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(scan workspace)");
+  return st;
+}
+
 }  // namespace
 }  // namespace qla
 
@@ -535,12 +611,29 @@ int qla_cp_correct(const float* H, const float* M, const float* h_init, float* o
 int qla_cp_correct_varlen(const float* H, const float* M, const float* h_init, float* out, float* final_state,
                           const int* cu_seg, int N, int T, int heads, int K, int V, int layout, int direction,
                           int engine, void* stream) {
+  return qla_cp_correct_varlen_ex(H, M, h_init, out, final_state, cu_seg, N, T, heads, K, V, layout, direction,
+                                  QLA_VARIANT_SEQ, engine, 0, 0, stream);
+}
+
+int qla_cp_correct_varlen_ex(const float* H, const float* M, const float* h_init, float* out, float* final_state,
+                             const int* cu_seg, int N, int T, int heads, int K, int V, int layout, int direction,
+                             int variant, int engine, int max_segments, int scan_group, void* stream) {
   t_last_error.clear();
   int st = check_varlen_args(H, M, h_init, out, final_state, cu_seg, N, T, heads, K, V, layout, direction);
   if (st != QLA_OK) return st;
   if (!known_engine(engine)) return fail(QLA_ERR_INVALID_ARG, "unknown engine %d", engine);
+  if (variant != QLA_VARIANT_AUTO && variant != QLA_VARIANT_SEQ && variant != QLA_VARIANT_SCAN)
+    return fail(QLA_ERR_INVALID_ARG, "unknown variant %d", variant);
+  if (max_segments < 0 || max_segments > T)
+    return fail(QLA_ERR_INVALID_ARG, "max_segments must be in [0, T] (got %d, T=%d)", max_segments, T);
+  if (scan_group < 0) return fail(QLA_ERR_INVALID_ARG, "scan_group must be >= 0 (got %d)", scan_group);
   DeviceInfo* d = nullptr;
   if ((st = current_device(&d)) != QLA_OK) return st;
+  const int Smax = max_segments > 0 ? max_segments : T;
+  Shape s{N, heads, std::max(1, Smax), K, V, layout, direction};
+  const int eng = resolve_engine(s, engine);
+  const int var = variant == QLA_VARIANT_AUTO ? resolve_variant(s, QLA_VARIANT_AUTO, d) : variant;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
   SeqJob j{};
   j.H = H;
   j.M = M;
@@ -562,8 +655,8 @@ int qla_cp_correct_varlen(const float* H, const float* M, const float* h_init, f
   j.heads = heads;
   j.T = T;
   j.nstates = (int64_t)heads * T;
-  Shape s{N, heads, 1, K, V, layout, direction};
-  return launch_seq(j, resolve_engine(s, engine), QLA_RELEASE_MEMBAR, d, static_cast<cudaStream_t>(stream));
+  if (var == QLA_VARIANT_SEQ || Smax < 2) return launch_seq(j, eng, QLA_RELEASE_MEMBAR, d, cs);
+  return run_scan_varlen(j, s, eng, scan_group, d, cs);
 }
 
 int qla_device_status(int* flags) {

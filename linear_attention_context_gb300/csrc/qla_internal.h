@@ -28,7 +28,7 @@ struct SeqJob {
   int nchains, S, L, G;
   int K, V, layout, direction;
   int init_mode;  // 0 zeros, 1 pointer, 2 identity (K == V)
-  // Variable length (cu_seg != nullptr, G = 1): H, out are [heads][T][state],
+  // Variable length (cu_seg != nullptr): H, out are [heads][T][state],
   // M [heads][T][K][K]; chain c = n * heads + h covers head h's segments
   // cu_seg[n] .. cu_seg[n+1] - 1 (device memory, N + 1 offsets).
   const int* cu_seg;
@@ -41,13 +41,15 @@ enum InitMode { kInitZero = 0, kInitPointer = 1, kInitIdentity = 2 };
 
 // Device status word bits.
 constexpr unsigned int kStatusTimeout = 1u;     // a bounded wait gave up
-constexpr unsigned int kStatusBadOffsets = 2u;  // variable-length offsets outside [0, T] or decreasing
+constexpr unsigned int kStatusBadOffsets = 2u;  // variable-length offsets outside [0, T], decreasing, or
+                                                // a sequence longer than the scan's bound
 
 #ifdef __CUDACC__
 // The segments of chain `chain`: index of its first segment in the packed
 // arrays and its segment count.  Returns false, after recording the event in
-// the status word, when its variable-length offsets are invalid (the chain is
-// then skipped: nothing is read or written for it).
+// the status word, when its variable-length offsets are invalid or its
+// sequence is longer than the launch's L * G segments (the chain is then
+// skipped: nothing is read or written for it).
 __device__ __forceinline__ bool chain_span(const SeqJob& j, int chain, int64_t& base, int& S) {
   if (!j.cu_seg) {
     base = (int64_t)chain * j.S;
@@ -56,7 +58,8 @@ __device__ __forceinline__ bool chain_span(const SeqJob& j, int chain, int64_t& 
   }
   const int n = chain / j.heads, h = chain - n * j.heads;
   const int s0 = j.cu_seg[n], s1 = j.cu_seg[n + 1];
-  if (s0 < 0 || s1 < s0 || s1 > j.T) {
+  // (the groups of a scan phase cover L * G segments per chain)
+  if (s0 < 0 || s1 < s0 || s1 > j.T || (int64_t)(s1 - s0) > (int64_t)j.L * j.G) {
     if (j.status && threadIdx.x == 0) atomicOr(j.status, kStatusBadOffsets);
     return false;
   }

@@ -956,12 +956,10 @@ cudaError_t launch_seq_tc(const SeqJob& job, int release, unsigned int* status, 
   if ((int64_t)job.nchains * job.G > 65535) return cudaErrorInvalidValue;
   // The tensor maps view H/out and M as 2-D arrays of all chains' states, so
   // chains must be packed back to back (H and out are absent in scan phase 1a;
-  // variable-length jobs locate every chain through its offsets).
+  // variable-length jobs locate every chain and group through the offsets).
   if (!job.cu_seg) {
     if ((job.H || job.out) && job.h_chain_stride != (int64_t)job.S * job.K * job.V) return cudaErrorInvalidValue;
     if (job.m_chain_stride != (int64_t)job.S * job.K * job.K) return cudaErrorInvalidValue;
-  } else if (job.G != 1) {
-    return cudaErrorInvalidValue;
   }
   // One column tile per CTA.  (Two tiles per CTA, with tile 0's epilogue
   // overlapping tile 1's MMAs, measured slower on the 32-head K=V=128 S=8

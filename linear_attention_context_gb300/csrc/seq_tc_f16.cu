@@ -758,8 +758,6 @@ cudaError_t launch_seq_tc_f16(const SeqJob& j, int release, unsigned int* status
   if (!j.cu_seg) {
     if ((j.H || j.out) && j.h_chain_stride != (int64_t)j.S * j.K * j.V) return cudaErrorInvalidValue;
     if (j.m_chain_stride != (int64_t)j.S * j.K * j.K) return cudaErrorInvalidValue;
-  } else if (j.G != 1) {
-    return cudaErrorInvalidValue;
   }
   H16Params p;
   memset(&p, 0, sizeof p);

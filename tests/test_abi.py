@@ -146,3 +146,23 @@ def test_stalled_wait_selftest_argument_checks(L):
     assert L.qla_selftest_stalled_wait(H, M, out, 3, 1000, 0, None) == -1    # automatic choice is not an engine
     assert L.qla_selftest_stalled_wait(H, M, out, 1, 1000, 3, None) == -1    # needs S >= 2
     assert L.qla_selftest_stalled_wait(H, M, out, 3, 0, 3, None) == -1       # limit outside [1, 10^7]
+
+
+def call_varlen_ex(L, variant=0, max_segments=0, scan_group=0, **kw):
+    args = dict(H=FAKE, M=FAKE + (1 << 32), h0=None, out=FAKE + (2 << 32), fin=None, cu=FAKE + (5 << 32), N=3,
+                T=10, heads=2, K=64, V=64, layout=0, direction=0, engine=0)
+    args.update(kw)
+    vp = ctypes.c_void_p
+    return L.qla_cp_correct_varlen_ex(vp(args["H"]), vp(args["M"]), vp(args["h0"]), vp(args["out"]),
+                                      vp(args["fin"]), vp(args["cu"]), args["N"], args["T"], args["heads"],
+                                      args["K"], args["V"], args["layout"], args["direction"], variant,
+                                      args["engine"], max_segments, scan_group, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(variant=3), -1), (dict(variant=-1), -1), (dict(max_segments=-1), -1), (dict(max_segments=11), -1),
+    (dict(scan_group=-2), -1), (dict(engine=4), -1), (dict(cu=None), -1), (dict(K=48), -2),
+    (dict(cu=FAKE + (5 << 32) + 2), -3), (dict(out=FAKE + 4096), -4),
+])
+def test_varlen_ex_argument_checks(L, kw, status):
+    assert call_varlen_ex(L, **kw) == status

@@ -1,8 +1,10 @@
-"""GPU parity of the variable-length form (qla_cp_correct_varlen) against the
-fp64 varlen oracle: sequences of different segment counts, including empty
-and one-segment sequences, both layouts and directions, both engines, with
-and without initial states, in place; and the device-side check of the
-offsets (a chain with invalid offsets is skipped and flagged).
+"""GPU parity of the variable-length form (qla_cp_correct_varlen and its
+variant form) against the fp64 varlen oracle: sequences of different segment
+counts, including empty and one-segment sequences, both layouts and
+directions, every engine, with and without initial states, in place, the
+sequential and the scan variant (group counts that leave empty and ragged
+groups); and the device-side checks (a chain with invalid offsets, or longer
+than the scan's bound, is flagged).
 """
 import numpy as np
 import pytest
@@ -22,7 +24,7 @@ def _dev(a):
     return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to("cuda:0")
 
 
-def _run(H, M, h0, cu, layout, direction, engine, in_place=False):
+def _run(H, M, h0, cu, layout, direction, engine, in_place=False, **kw):
     import torch
 
     import linear_attention_context_gb300 as qla
@@ -32,7 +34,7 @@ def _run(H, M, h0, cu, layout, direction, engine, in_place=False):
     fin = torch.empty((N, heads) + H.shape[2:], device="cuda:0")
     out = Hd if in_place else None
     out = qla.cp_correct_varlen(Hd, Md, cud, h0d, out, layout=layout, direction=direction, final_state=fin,
-                                engine=engine)
+                                engine=engine, **kw)
     torch.cuda.synchronize()
     assert qla.device_status() == 0
     return out.cpu().numpy(), fin.cpu().numpy()
@@ -103,3 +105,72 @@ def test_varlen_invalid_offsets_are_flagged_and_skipped(engine):
     assert_parity(got[:, :4], ref, what="valid chains next to an invalid one")
     assert (got[:, 4] == 7.0).all()  # the skipped chain's segment is untouched
     assert qla.device_status() == 0  # the word was cleared
+
+
+@pytest.mark.parametrize("engine", engines_under_test())
+@pytest.mark.parametrize("direction", ["fwd", "rev"])
+@pytest.mark.parametrize("layout", ["kv", "vk"])
+@pytest.mark.parametrize("group,bound", [(1, 13), (2, 13), (3, 13), (5, 13), (4, 0), (13, 20)])
+def test_varlen_scan_parity(group, bound, layout, direction, engine):
+    """Scan variant: every chain is cut into `group` groups of ceil(bound / group)
+    segments (bound 0 = T); sequences of 0 .. 13 segments leave empty and
+    ragged groups."""
+    K = 128
+    if not engine_supports(engine, K, K):
+        pytest.skip(f"engine {engine} does not take K={K}")
+    H, M, h0, cu = qi.make_varlen_inputs(LENGTHS, 2, K, K, seed=41, layout=layout, m_kind="orthogonal",
+                                         h_scale=0.1, init_scale=0.1)
+    ref, rfin = oracle.cp_correct_varlen(H, M, h0, cu, layout, direction)
+    got, fin = _run(H, M, h0, cu, layout, direction, engine, variant="scan", max_segments=bound,
+                    scan_group=group)
+    what = f"varlen scan G={group} bound={bound} {layout} {direction} {engine}"
+    assert_parity(got, ref, what=what)
+    assert_parity(fin, rfin, what=what + " final")
+
+
+@pytest.mark.parametrize("engine", engines_under_test())
+def test_varlen_scan_final_state_only_and_auto(engine):
+    """Final state alone through the scan; and the automatic choice (long
+    sequences, few chains) agrees with the oracle."""
+    import torch
+
+    import linear_attention_context_gb300 as qla
+    K = 64 if engine == "simt" else 128
+    if not engine_supports(engine, K, K):
+        pytest.skip(f"engine {engine} does not take K={K}")
+    lengths = [30, 0, 7]
+    H, M, h0, cu = qi.make_varlen_inputs(lengths, 1, K, K, seed=43, m_kind="householder", h_scale=0.1,
+                                         init_scale=0.1)
+    ref, rfin = oracle.cp_correct_varlen(H, M, h0, cu, "kv", "rev")
+    fin = torch.empty((len(lengths), 1) + H.shape[2:], device="cuda:0")
+    r = qla.cp_correct_varlen(_dev(H), _dev(M), _dev(cu.astype(np.int32)), _dev(h0), None, layout="kv",
+                              direction="rev", final_state=fin, engine=engine, variant="scan", max_segments=30,
+                              want_out=False)
+    torch.cuda.synchronize()
+    assert r is None and qla.device_status() == 0
+    assert_parity(fin.cpu().numpy(), rfin, what=f"varlen scan final only {engine}")
+    got, fin2 = _run(H, M, h0, cu, "kv", "rev", engine, variant="auto", max_segments=30)
+    assert_parity(got, ref, what=f"varlen auto {engine}")
+    assert_parity(fin2, rfin, what="varlen auto final")
+
+
+@pytest.mark.parametrize("engine", engines_under_test())
+def test_varlen_scan_bound_exceeded_is_flagged(engine):
+    import torch
+
+    import linear_attention_context_gb300 as qla
+    K = 128
+    if not engine_supports(engine, K, K):
+        pytest.skip(f"engine {engine} does not take K={K}")
+    H, M, h0, cu = qi.make_varlen_inputs([3, 9, 2], 2, K, K, seed=45)
+    Hd, Md, h0d, cud = _dev(H), _dev(M), _dev(h0), _dev(cu.astype(np.int32))
+    out = torch.zeros_like(Hd)
+    qla.cp_correct_varlen(Hd, Md, cud, h0d, out, engine=engine, variant="scan", max_segments=4, scan_group=2)
+    torch.cuda.synchronize()
+    assert qla.device_status() == 2  # the 9-segment sequence exceeds the bound of 4
+    # the sequences within the bound are still right
+    ref, _ = oracle.cp_correct_varlen(H, M, h0, cu, "kv", "fwd")
+    got = out.cpu().numpy()
+    assert_parity(got[:, :3], ref[:, :3], what="first sequence next to an over-long one")
+    assert_parity(got[:, 12:], ref[:, 12:], what="last sequence next to an over-long one")
+    assert qla.device_status() == 0
