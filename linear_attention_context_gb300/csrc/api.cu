@@ -49,6 +49,11 @@ struct DeviceInfo {
   int sm_count = 0;
   int cc_major = 0, cc_minor = 0;
   unsigned int* status_word = nullptr;
+  // Side stream and fork/join events for the scan's two independent first
+  // phases (null: the phases run one after the other on the caller's stream).
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  std::mutex* side_mutex = nullptr;
 };
 
 std::mutex g_dev_mutex;
@@ -75,6 +80,16 @@ int current_device(DeviceInfo** out) {
       if ((e = cudaGetSymbolAddress(&p, g_device_status)) != cudaSuccess)
         return cuda_fail(e, "cudaGetSymbolAddress(status word)");
       d.status_word = static_cast<unsigned int*>(p);
+      // Created here, at the first call on the device, so that no scan call
+      // (which may run inside a CUDA graph capture) has to create them.
+      if (cudaStreamCreateWithFlags(&d.side, cudaStreamNonBlocking) != cudaSuccess ||
+          cudaEventCreateWithFlags(&d.ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&d.ev_join, cudaEventDisableTiming) != cudaSuccess) {
+        d.side = nullptr;
+        cudaGetLastError();
+      } else {
+        d.side_mutex = new std::mutex;
+      }
     }
     d.probed = true;
   }
@@ -263,6 +278,35 @@ size_t scan_bytes(const Shape& s, int G) {
   return (size_t)s.chains() * G * ((size_t)s.K * s.K + 2 * (size_t)s.state()) * sizeof(float);
 }
 
+// Runs `on_main` on `stream` and `on_side` on the device's side stream
+// concurrently: the side stream waits for everything issued to `stream`
+// before the call, and `stream` waits for the side stream's work before
+// anything issued after the call (event fork and join, which CUDA graph
+// capture follows).  The side stream and its events are shared by the
+// device's callers, so the fork, the side launch and the join are issued
+// under a lock.  Without a side stream both run on `stream`.  (When the two
+// launches' CTAs exceed the SMs, running them concurrently measured neither
+// faster nor slower than one after the other.)
+template <class MainFn, class SideFn>
+int fork_join(const DeviceInfo* d, cudaStream_t stream, MainFn&& on_main, SideFn&& on_side) {
+  if (!d->side) {
+    const int st = on_side(stream);
+    return st != QLA_OK ? st : on_main(stream);
+  }
+  std::lock_guard<std::mutex> lock(*d->side_mutex);
+  cudaError_t e = cudaEventRecord(d->ev_fork, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(fork)");
+  if ((e = cudaStreamWaitEvent(d->side, d->ev_fork, 0)) != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(fork)");
+  const int st_side = on_side(d->side);
+  // join even after a failed side launch, so that a capturing stream is not left forked
+  const cudaError_t e_rec = cudaEventRecord(d->ev_join, d->side);
+  const int st_main = st_side == QLA_OK ? on_main(stream) : st_side;
+  const cudaError_t e_wait = e_rec == cudaSuccess ? cudaStreamWaitEvent(stream, d->ev_join, 0) : e_rec;
+  if (st_main != QLA_OK) return st_main;
+  if (e_wait != cudaSuccess) return cuda_fail(e_wait, "event join");
+  return QLA_OK;
+}
+
 // The scan variant.  For groups g of L consecutive segments (by index):
 //  1a. A_g = M_{last} ... M_{first} over the group's segments (forward products
 //      from the identity, kv view, V' = K); in reverse this is the transpose of
@@ -287,32 +331,31 @@ int run_scan(const float* H, const float* M, const float* h_init, float* out, fl
   const SeqJob base = plain_job(H, M, h_init, out, fin, s);
   int st = QLA_OK;
 
-  {  // 1a: group products of M, forward, kv view, from the identity
-    SeqJob j = base;
-    j.H = nullptr;
-    j.init = nullptr;
-    j.init_mode = kInitIdentity;
-    j.out = nullptr;
-    j.fin = Aagg;
-    j.fin_unit_stride = (int64_t)s.K * s.K;
-    j.L = L;
-    j.G = Gr;
-    j.V = s.K;
-    j.layout = QLA_LAYOUT_KV;
-    j.direction = QLA_FORWARD;
-    st = launch_seq(j, engine_for(j, engine), release, d, stream);
-  }
-  if (st == QLA_OK) {  // 1b: group recurrences from zero
-    SeqJob j = base;
-    j.init = nullptr;
-    j.init_mode = kInitZero;
-    j.out = nullptr;
-    j.fin = bagg;
-    j.fin_unit_stride = s.state();
-    j.L = L;
-    j.G = Gr;
-    st = launch_seq(j, engine_for(j, engine), release, d, stream);
-  }
+  // 1a (group products of M, forward, kv view, from the identity) and 1b
+  // (group recurrences from zero) are independent: they run concurrently.
+  SeqJob j1a = base;
+  j1a.H = nullptr;
+  j1a.init = nullptr;
+  j1a.init_mode = kInitIdentity;
+  j1a.out = nullptr;
+  j1a.fin = Aagg;
+  j1a.fin_unit_stride = (int64_t)s.K * s.K;
+  j1a.L = L;
+  j1a.G = Gr;
+  j1a.V = s.K;
+  j1a.layout = QLA_LAYOUT_KV;
+  j1a.direction = QLA_FORWARD;
+  SeqJob j1b = base;
+  j1b.init = nullptr;
+  j1b.init_mode = kInitZero;
+  j1b.out = nullptr;
+  j1b.fin = bagg;
+  j1b.fin_unit_stride = s.state();
+  j1b.L = L;
+  j1b.G = Gr;
+  st = fork_join(
+      d, stream, [&](cudaStream_t cs) { return launch_seq(j1a, engine_for(j1a, engine), release, d, cs); },
+      [&](cudaStream_t cs) { return launch_seq(j1b, engine_for(j1b, engine), release, d, cs); });
   if (st == QLA_OK) {  // 2: carries across the group aggregates
     SeqJob j = base;
     j.H = bagg;
@@ -378,32 +421,32 @@ int run_scan_in(const float* H, const float* M, const float* h_init, float* out,
   float* carry = bagg + (size_t)s.chains() * Gr * s.state();
   const SeqJob base = plain_job(H, M, h_init, out, fin, s);
   int st;
-  {  // 1a: group products of M, forward, kv view, from the identity
-    SeqJob j = base;
-    j.H = nullptr;
-    j.init = nullptr;
-    j.init_mode = kInitIdentity;
-    j.out = nullptr;
-    j.fin = Aagg;
-    j.fin_unit_stride = (int64_t)s.K * s.K;
-    j.L = L;
-    j.G = Gr;
-    j.V = s.K;
-    j.layout = QLA_LAYOUT_KV;
-    j.direction = QLA_FORWARD;
-    if ((st = launch_seq(j, engine_for(j, engine), release, d, stream)) != QLA_OK) return st;
-  }
-  {  // 1b: group recurrences from zero
-    SeqJob j = base;
-    j.init = nullptr;
-    j.init_mode = kInitZero;
-    j.out = nullptr;
-    j.fin = bagg;
-    j.fin_unit_stride = s.state();
-    j.L = L;
-    j.G = Gr;
-    if ((st = launch_seq(j, engine_for(j, engine), release, d, stream)) != QLA_OK) return st;
-  }
+  // 1a (group products of M, forward, kv view, from the identity) and 1b
+  // (group recurrences from zero) are independent: they run concurrently.
+  SeqJob j1a = base;
+  j1a.H = nullptr;
+  j1a.init = nullptr;
+  j1a.init_mode = kInitIdentity;
+  j1a.out = nullptr;
+  j1a.fin = Aagg;
+  j1a.fin_unit_stride = (int64_t)s.K * s.K;
+  j1a.L = L;
+  j1a.G = Gr;
+  j1a.V = s.K;
+  j1a.layout = QLA_LAYOUT_KV;
+  j1a.direction = QLA_FORWARD;
+  SeqJob j1b = base;
+  j1b.init = nullptr;
+  j1b.init_mode = kInitZero;
+  j1b.out = nullptr;
+  j1b.fin = bagg;
+  j1b.fin_unit_stride = s.state();
+  j1b.L = L;
+  j1b.G = Gr;
+  st = fork_join(
+      d, stream, [&](cudaStream_t cs) { return launch_seq(j1a, engine_for(j1a, engine), release, d, cs); },
+      [&](cudaStream_t cs) { return launch_seq(j1b, engine_for(j1b, engine), release, d, cs); });
+  if (st != QLA_OK) return st;
   {  // 2: carries across the group aggregates
     SeqJob j = base;
     j.H = bagg;
@@ -451,32 +494,31 @@ int run_scan_varlen(const SeqJob& vj, const Shape& s, int engine, int group, con
   float* bagg = Aagg + (size_t)chains * Gr * s.K * s.K;
   float* carry = bagg + (size_t)chains * Gr * s.state();
   int st = QLA_OK;
-  {  // 1a: group products of M, forward, kv view, from the identity
-    SeqJob j = vj;
-    j.H = nullptr;
-    j.init = nullptr;
-    j.init_mode = kInitIdentity;
-    j.out = nullptr;
-    j.fin = Aagg;
-    j.fin_unit_stride = (int64_t)s.K * s.K;
-    j.L = L;
-    j.G = Gr;
-    j.V = s.K;
-    j.layout = QLA_LAYOUT_KV;
-    j.direction = QLA_FORWARD;
-    st = launch_seq(j, engine_for(j, engine), QLA_RELEASE_MEMBAR, d, stream);
-  }
-  if (st == QLA_OK) {  // 1b: group recurrences from zero
-    SeqJob j = vj;
-    j.init = nullptr;
-    j.init_mode = kInitZero;
-    j.out = nullptr;
-    j.fin = bagg;
-    j.fin_unit_stride = s.state();
-    j.L = L;
-    j.G = Gr;
-    st = launch_seq(j, engine_for(j, engine), QLA_RELEASE_MEMBAR, d, stream);
-  }
+  // 1a (group products of M, forward, kv view, from the identity) and 1b
+  // (group recurrences from zero) are independent: they run concurrently.
+  SeqJob j1a = vj;
+  j1a.H = nullptr;
+  j1a.init = nullptr;
+  j1a.init_mode = kInitIdentity;
+  j1a.out = nullptr;
+  j1a.fin = Aagg;
+  j1a.fin_unit_stride = (int64_t)s.K * s.K;
+  j1a.L = L;
+  j1a.G = Gr;
+  j1a.V = s.K;
+  j1a.layout = QLA_LAYOUT_KV;
+  j1a.direction = QLA_FORWARD;
+  SeqJob j1b = vj;
+  j1b.init = nullptr;
+  j1b.init_mode = kInitZero;
+  j1b.out = nullptr;
+  j1b.fin = bagg;
+  j1b.fin_unit_stride = s.state();
+  j1b.L = L;
+  j1b.G = Gr;
+  st = fork_join(
+      d, stream, [&](cudaStream_t cs) { return launch_seq(j1a, engine_for(j1a, engine), QLA_RELEASE_MEMBAR, d, cs); },
+      [&](cudaStream_t cs) { return launch_seq(j1b, engine_for(j1b, engine), QLA_RELEASE_MEMBAR, d, cs); });
   if (st == QLA_OK) {  // 2: carries across the group aggregates (fixed length Gr per chain)
     SeqJob j = vj;
     j.cu_seg = nullptr;
