@@ -196,3 +196,47 @@ def test_scan_integer_exact(direction):
         ref, _ = oracle.cp_correct(H, M, h0, layout, direction)
         got, _ = run(H, M, h0, layout, direction, variant="scan", scan_group=4)
         assert np.array_equal(got, ref)
+
+
+def test_concurrent_scans_from_two_host_threads():
+    """The scan's side stream and events are shared by a device's callers:
+    two host threads running scans on their own streams must both be right."""
+    import threading
+
+    import torch
+
+    import linear_attention_context_gb300 as qla
+    dev = torch.device("cuda:0")
+    c = qi.sweep_case(2, 32)
+    cases = []
+    for layout, direction in (("kv", "fwd"), ("vk", "rev")):
+        H, M, h0 = qi.make_inputs(c, layout)
+        ref, _ = oracle.cp_correct(H, M, h0, layout, direction)
+        cases.append((layout, direction, torch.from_numpy(H).to(dev), torch.from_numpy(M).to(dev),
+                      torch.from_numpy(h0).to(dev), ref))
+    results, errors = {}, []
+
+    def worker(i):
+        try:
+            torch.cuda.set_device(0)
+            layout, direction, Hd, Md, h0d, _ = cases[i]
+            s = torch.cuda.Stream(dev)
+            outs = []
+            for _ in range(20):
+                outs.append(qla.cp_correct(Hd, Md, h0d, layout=layout, direction=direction, variant="scan",
+                                           stream=s))
+            s.synchronize()
+            results[i] = [o.cpu().numpy().astype(np.float64) for o in outs]
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i, (layout, direction, *_, ref) in enumerate(cases):
+        for k, got in enumerate(results[i]):
+            assert_parity(got, ref, what=f"thread {i} call {k} {layout} {direction}")
+    assert qla.device_status() == 0
