@@ -555,9 +555,10 @@ def run_sweep(args):
                             for _ in range(10):
                                 call()
                     stream.synchronize()
-                    for _ in range(3):
-                        g.replay()
-                    stream.synchronize()
+                    with torch.cuda.stream(stream):  # warm-up replays on the timed stream
+                        for _ in range(3):
+                            g.replay()
+                    torch.cuda.synchronize()
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     with torch.cuda.stream(stream):
                         e0.record(stream)
@@ -623,9 +624,10 @@ def run_varlen(args):
                     for _ in range(10):
                         call()
             stream.synchronize()
-            for _ in range(3):
-                g.replay()
-            stream.synchronize()
+            with torch.cuda.stream(stream):  # warm-up replays on the timed stream
+                for _ in range(3):
+                    g.replay()
+            torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             with torch.cuda.stream(stream):
                 e0.record(stream)
@@ -638,6 +640,71 @@ def run_varlen(args):
                           "us_per_call": {k: round(v, 2) for k, v in times.items()}}), flush=True)
     if qla.device_status() != 0:
         raise SystemExit("device status word set during the varlen timings")
+
+
+def run_configs(args):
+    """Configs 0-2 one at a time (config 3: --large, config 4: --sweep): µs per
+    call of each (layout, direction) of the config, graph-replayed, L2 flushed
+    by rotating input copies where the inputs are smaller than L2.  One JSON
+    line per config; not the headline metric."""
+    import numpy as np
+    import torch
+
+    import linear_attention_context_gb300 as qla
+    import qla_inputs as qi
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream(dev)
+    peak, peak_source = load_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    plan = {"c0": [("kv", "fwd")], "c1": [("kv", "fwd"), ("vk", "fwd")], "c2": [("kv", "rev"), ("vk", "rev")]}
+    for name, combos in plan.items():
+        c = qi.WORKLOADS[name]
+        times = {}
+        for layout, direction in combos:
+            H, M, h0 = qi.make_inputs(c, layout)
+            per_set = H.nbytes + M.nbytes + (h0.nbytes if h0 is not None else 0) + H.nbytes
+            nsets = max(1, min(16, int(np.ceil(2 * l2 / per_set))))
+            sets = []
+            for _ in range(nsets):
+                sets.append((torch.from_numpy(H).to(dev), torch.from_numpy(M).to(dev),
+                             None if h0 is None else torch.from_numpy(h0).to(dev), torch.empty(H.shape, dtype=torch.float32, device=dev)))
+            calls = 16 * nsets
+
+            def body():
+                for _ in range(16):
+                    for Hd, Md, h0d, out in sets:
+                        qla.cp_correct(Hd, Md, h0d, out, layout=layout, direction=direction, stream=stream)
+            with torch.cuda.stream(stream):
+                body()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    body()
+            stream.synchronize()
+            with torch.cuda.stream(stream):  # warm-up replays on the timed stream
+                for _ in range(3):
+                    g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(args.sweep_reps):
+                    g.replay()
+                e1.record(stream)
+            stream.synchronize()
+            times[f"{layout} {direction}"] = e0.elapsed_time(e1) * 1e3 / (calls * args.sweep_reps)
+        us = float(np.mean(list(times.values())))
+        b = algorithmic_bytes(c.B * c.heads, c.S, c.K, c.V, with_init=c.init_kind != "none")
+        line = {"config": name, "B": c.B, "heads": c.heads, "K": c.K, "V": c.V, "S": c.S,
+                "us_per_call": {k: round(v, 3) for k, v in times.items()}, "mean_us": round(us, 3),
+                "engine": qla.resolve(c.B, c.heads, c.S, c.K, c.V)[1], "algorithmic_bytes": b,
+                "hbm_gbs": round(b / (us * 1e-6) / 1e9, 1)}
+        line["hbm_frac"] = round(b / (us * 1e-6) / 1e9 / peak, 4)
+        line["peak"] = f"{peak} GB/s ({peak_source})"
+        rot = per_set * len(sets)
+        line["l2"] = (f"{len(sets)} rotating input/output sets, {rot / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB"
+                      + ("" if rot >= 2 * l2 else " (the sets fit in L2: inputs partly L2-resident)"))
+        print(json.dumps(line), flush=True)
 
 
 def run_large(args):
@@ -697,6 +764,7 @@ def main():
     ap.add_argument("--sweep-reps", type=int, default=20)
     ap.add_argument("--large", action="store_true", help="time the 4 x 64-head K=V=256 S=32 workload")
     ap.add_argument("--varlen", action="store_true", help="time variable-length calls, sequential vs scan")
+    ap.add_argument("--configs", action="store_true", help="time configs 0-2 one at a time")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -706,6 +774,8 @@ def main():
         run_large(args)
     elif args.varlen:
         run_varlen(args)
+    elif args.configs:
+        run_configs(args)
     else:
         run_ours(args)
 

@@ -179,6 +179,16 @@ QLA_API int qla_cp_correct_varlen_ex(const float* H, const float* M, const float
  * size (0 = automatic); 0 when the scan does not apply. */
 QLA_API size_t qla_scan_workspace_bytes(int B, int heads, int S, int K, int V, int scan_group);
 
+/* Process-wide override of the automatic variant choice: QLA_VARIANT_SEQ or
+ * QLA_VARIANT_SCAN make every call that asks for QLA_VARIANT_AUTO (and
+ * qla_cp_correct, which always does) use that variant; QLA_VARIANT_AUTO
+ * restores the shape-based rule.  Its initial value comes from the
+ * environment variable QLA_VARIANT ("auto", "seq", "scan" or 0, 1, 2; unset or
+ * anything else: auto), read at the first call that needs it.  Returns
+ * QLA_ERR_INVALID_ARG for other values.  The choice never changes results
+ * beyond the parity bar (the variants compute the same recurrence). */
+QLA_API int qla_set_variant(int variant);
+
 /* The variant and engine QLA_*_AUTO resolve to for this shape on the current
  * device (written to *variant and *engine; either may be NULL). */
 QLA_API int qla_resolve(int B, int heads, int S, int K, int V, int layout, int* variant, int* engine);

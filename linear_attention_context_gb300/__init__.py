@@ -32,7 +32,7 @@ STATUS = {0: "QLA_OK", -1: "QLA_ERR_INVALID_ARG", -2: "QLA_ERR_UNSUPPORTED", -3:
 
 # Every function include/qla.h declares.
 EXPORTS = ("qla_cp_correct", "qla_cp_correct_ex", "qla_cp_correct_varlen", "qla_cp_correct_varlen_ex",
-           "qla_scan_workspace_bytes",
+           "qla_scan_workspace_bytes", "qla_set_variant",
            "qla_resolve", "qla_status_string", "qla_last_error", "qla_device_status", "qla_selftest_stalled_wait",
            "qla_cp_correct_scan_static", "qla_version")
 
@@ -71,6 +71,8 @@ def lib():
         L.qla_cp_correct_varlen.restype = ci
         L.qla_cp_correct_varlen_ex.argtypes = [vp, vp, vp, vp, vp, vp] + [ci] * 11 + [vp]
         L.qla_cp_correct_varlen_ex.restype = ci
+        L.qla_set_variant.argtypes = [ci]
+        L.qla_set_variant.restype = ci
         L.qla_scan_workspace_bytes.argtypes = [ci] * 6
         L.qla_scan_workspace_bytes.restype = cz
         L.qla_resolve.argtypes = [ci] * 6 + [ctypes.POINTER(ci), ctypes.POINTER(ci)]
@@ -216,6 +218,12 @@ def cp_correct_varlen(H, M, cu_seg, h_init=None, out=None, *, layout="kv", direc
                                             int(max_segments), int(scan_group), _stream_handle(stream))
     check(rc)
     return out
+
+
+def set_variant(variant: str):
+    """Process-wide override of the automatic variant choice ("auto", "seq" or
+    "scan"); the initial value comes from the QLA_VARIANT environment variable."""
+    check(lib().qla_set_variant(VARIANTS[variant]))
 
 
 def scan_workspace_bytes(B, heads, S, K, V, scan_group=0) -> int:

@@ -6,7 +6,9 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
+#include <cstdlib>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -218,9 +220,33 @@ int engine_for(const SeqJob& j, int engine) {
 // three launches whose parallel phases hold tiles * G CTAs.  Measured on
 // GB300 (K = V = 128, tensor-core engine): it wins for S >= 32 with up to
 // 16 column tiles (1.25x - 2.9x) and loses for S <= 8 or 128 tiles.
+// Process-wide override of the automatic variant choice (qla_set_variant);
+// -1 until first read, then initialised from the QLA_VARIANT environment
+// variable ("auto", "seq", "scan" or 0, 1, 2; anything else means auto).
+std::atomic<int> g_variant_override{-1};
+
+int parse_variant_env(const char* v) {
+  if (!v) return QLA_VARIANT_AUTO;
+  if (!strcmp(v, "seq") || !strcmp(v, "1")) return QLA_VARIANT_SEQ;
+  if (!strcmp(v, "scan") || !strcmp(v, "2")) return QLA_VARIANT_SCAN;
+  return QLA_VARIANT_AUTO;
+}
+
+int variant_override() {
+  int v = g_variant_override.load(std::memory_order_relaxed);
+  if (v < 0) {
+    int expected = -1;
+    g_variant_override.compare_exchange_strong(expected, parse_variant_env(std::getenv("QLA_VARIANT")));
+    v = g_variant_override.load(std::memory_order_relaxed);
+  }
+  return v;
+}
+
 int resolve_variant(const Shape& s, int variant, const DeviceInfo* d) {
   (void)d;
   if (variant != QLA_VARIANT_AUTO) return variant;
+  const int forced = variant_override();
+  if (forced != QLA_VARIANT_AUTO) return forced;
   const int64_t tiles = s.chains() * ((s.V + 31) / 32);
   return (s.S >= 24 && tiles <= 16) ? QLA_VARIANT_SCAN : QLA_VARIANT_SEQ;
 }
@@ -608,6 +634,14 @@ size_t qla_scan_workspace_bytes(int B, int heads, int S, int K, int V, int scan_
   const int G = scan_group > 0 ? std::min(scan_group, S) : auto_groups(S);
   const int L = (S + G - 1) / G;
   return scan_bytes(s, (S + L - 1) / L);
+}
+
+int qla_set_variant(int variant) {
+  t_last_error.clear();
+  if (variant != QLA_VARIANT_AUTO && variant != QLA_VARIANT_SEQ && variant != QLA_VARIANT_SCAN)
+    return fail(QLA_ERR_INVALID_ARG, "unknown variant %d", variant);
+  g_variant_override.store(variant, std::memory_order_relaxed);
+  return QLA_OK;
 }
 
 int qla_resolve(int B, int heads, int S, int K, int V, int layout, int* variant, int* engine) {

@@ -166,3 +166,11 @@ def call_varlen_ex(L, variant=0, max_segments=0, scan_group=0, **kw):
 ])
 def test_varlen_ex_argument_checks(L, kw, status):
     assert call_varlen_ex(L, **kw) == status
+
+
+def test_set_variant_checks(L):
+    assert L.qla_set_variant(3) == -1
+    assert L.qla_set_variant(-1) == -1
+    assert L.qla_set_variant(1) == 0
+    assert L.qla_set_variant(2) == 0
+    assert L.qla_set_variant(0) == 0  # back to the automatic rule for the rest of the process

@@ -240,3 +240,35 @@ def test_concurrent_scans_from_two_host_threads():
         for k, got in enumerate(results[i]):
             assert_parity(got, ref, what=f"thread {i} call {k} {layout} {direction}")
     assert qla.device_status() == 0
+
+
+def test_process_wide_variant_override():
+    """qla_set_variant forces the variant of every automatic choice (the plain
+    entry point included); QLA_VARIANT sets its initial value."""
+    import os
+    import subprocess
+    import sys
+
+    import torch
+
+    import linear_attention_context_gb300 as qla
+    assert qla.resolve(1, 32, 8, 128, 128, "kv")[0] == "seq"
+    c = qi.sweep_case(2, 8)
+    H, M, h0 = qi.make_inputs(c, "vk")
+    ref, _ = oracle.cp_correct(H, M, h0, "vk", "rev")
+    try:
+        qla.set_variant("scan")
+        assert qla.resolve(1, 32, 8, 128, 128, "kv")[0] == "scan"
+        got = qla.cp_correct(torch.from_numpy(H).cuda(), torch.from_numpy(M).cuda(), torch.from_numpy(h0).cuda(),
+                             layout="vk", direction="rev")
+        torch.cuda.synchronize()
+        assert_parity(got.cpu().numpy().astype(np.float64), ref, what="forced scan")
+    finally:
+        qla.set_variant("auto")
+    assert qla.resolve(1, 32, 8, 128, 128, "kv")[0] == "seq"
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = "import linear_attention_context_gb300 as q; print(q.resolve(1, 32, 8, 128, 128, 'kv')[0])"
+    env = dict(os.environ, QLA_VARIANT="scan")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == "scan"
