@@ -535,50 +535,53 @@ def run_sweep(args):
     torch.cuda.set_device(0)
     stream = torch.cuda.Stream(dev)
     lines = []
-    for heads in qi.SWEEP_HEADS:
-        for S_ in qi.SWEEP_S:
-            c = qi.sweep_case(heads, S_)
-            for layout, direction in (("kv", "fwd"), ("vk", "rev")):
-                H, M, h0 = qi.make_inputs(c, layout)
-                Hd, Md, h0d = (torch.from_numpy(a).to(dev) for a in (H, M, h0))
-                out = torch.empty_like(Hd)
-                times = {}
-                for variant in ("seq", "scan"):
-                    def call():
-                        qla.cp_correct(Hd, Md, h0d, out, layout=layout, direction=direction, variant=variant,
-                                       stream=stream)
-                    with torch.cuda.stream(stream):
-                        for _ in range(3):
+    points = [(h, s_) for h in qi.SWEEP_HEADS for s_ in qi.SWEEP_S]
+    if args.sweep_point:
+        h, s_ = (int(x) for x in args.sweep_point.split(","))
+        points = [(h, s_)]
+    for heads, S_ in points:
+        c = qi.sweep_case(heads, S_)
+        for layout, direction in (("kv", "fwd"), ("vk", "rev")):
+            H, M, h0 = qi.make_inputs(c, layout)
+            Hd, Md, h0d = (torch.from_numpy(a).to(dev) for a in (H, M, h0))
+            out = torch.empty_like(Hd)
+            times = {}
+            for variant in ("seq", "scan"):
+                def call():
+                    qla.cp_correct(Hd, Md, h0d, out, layout=layout, direction=direction, variant=variant,
+                                   stream=stream)
+                with torch.cuda.stream(stream):
+                    for _ in range(3):
+                        call()
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=stream):
+                        for _ in range(10):
                             call()
-                        g = torch.cuda.CUDAGraph()
-                        with torch.cuda.graph(g, stream=stream):
-                            for _ in range(10):
-                                call()
-                    stream.synchronize()
-                    with torch.cuda.stream(stream):  # warm-up replays on the timed stream
-                        for _ in range(3):
-                            g.replay()
-                    torch.cuda.synchronize()
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    with torch.cuda.stream(stream):
-                        e0.record(stream)
-                        for _ in range(args.sweep_reps):
-                            g.replay()
-                        e1.record(stream)
-                    stream.synchronize()
-                    times[variant] = e0.elapsed_time(e1) * 1e3 / (10 * args.sweep_reps)
-                auto = qla.resolve(1, heads, S_, 128, 128, layout)[0]
-                # the scan's executed tensor work (3xTF32: 3x) per chain: group
-                # products of M, S steps of K^3; group recurrences (S steps),
-                # carries (G) and re-runs (S - G), K^2 V each
-                Kk = Vv = 128
-                G = scan_groups(S_)
-                flops = 3 * 2 * heads * (S_ * Kk ** 3 + 2 * S_ * Kk * Kk * Vv)
-                rate = flops / (times["scan"] * 1e-6) / 1e12
-                lines.append({"sweep": {"heads": heads, "S": S_, "layout": layout, "direction": direction},
-                              "us_per_call": {k: round(v, 2) for k, v in times.items()},
-                              "auto": auto, "bytes_per_call": algorithmic_bytes(heads, S_, 128, 128),
-                              "scan_tensor": {"groups": G, "executed_tflops": round(rate, 1)}})
+                stream.synchronize()
+                with torch.cuda.stream(stream):  # warm-up replays on the timed stream
+                    for _ in range(3):
+                        g.replay()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    e0.record(stream)
+                    for _ in range(args.sweep_reps):
+                        g.replay()
+                    e1.record(stream)
+                stream.synchronize()
+                times[variant] = e0.elapsed_time(e1) * 1e3 / (10 * args.sweep_reps)
+            auto = qla.resolve(1, heads, S_, 128, 128, layout)[0]
+            # the scan's executed tensor work (3xTF32: 3x) per chain: group
+            # products of M, S steps of K^3; group recurrences (S steps),
+            # carries (G) and re-runs (S - G), K^2 V each
+            Kk = Vv = 128
+            G = scan_groups(S_)
+            flops = 3 * 2 * heads * (S_ * Kk ** 3 + 2 * S_ * Kk * Kk * Vv)
+            rate = flops / (times["scan"] * 1e-6) / 1e12
+            lines.append({"sweep": {"heads": heads, "S": S_, "layout": layout, "direction": direction},
+                          "us_per_call": {k: round(v, 2) for k, v in times.items()},
+                          "auto": auto, "bytes_per_call": algorithmic_bytes(heads, S_, 128, 128),
+                          "scan_tensor": {"groups": G, "executed_tflops": round(rate, 1)}})
     # the matmul peak last: its power draw would lower the clocks of the timings
     peaks = compute_peaks(dev)
     print(json.dumps({"compute_peaks": peaks}), flush=True)
@@ -762,6 +765,7 @@ def main():
     ap.add_argument("--skip-peaks", action="store_true", help="skip the TF32 matmul peak measurement")
     ap.add_argument("--sweep", action="store_true", help="time sequential vs scan over the low batch*heads sweep")
     ap.add_argument("--sweep-reps", type=int, default=20)
+    ap.add_argument("--sweep-point", default="", help="heads,S: one point of the sweep only")
     ap.add_argument("--large", action="store_true", help="time the 4 x 64-head K=V=256 S=32 workload")
     ap.add_argument("--varlen", action="store_true", help="time variable-length calls, sequential vs scan")
     ap.add_argument("--configs", action="store_true", help="time configs 0-2 one at a time")
