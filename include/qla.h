@@ -33,8 +33,10 @@
  *     out    same shape as H
  *
  * Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t; NULL
- * is the legacy default stream).  A status other than QLA_OK means nothing was
- * launched.  Device-side faults surface at the caller's next synchronisation,
+ * is the legacy default stream).  A status other than QLA_OK from the argument
+ * checks means nothing was launched; a launch failure inside the scan variant
+ * may leave its earlier phases enqueued (their results are then unused
+ * scratch).  Device-side faults surface at the caller's next synchronisation,
  * as with any CUDA launch.
  *
  * Aliasing: out == H (exactly the same pointer) is supported and computes the
