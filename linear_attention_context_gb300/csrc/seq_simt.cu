@@ -10,10 +10,13 @@
 //
 // One CTA owns a 32-column tile of the kv-view state of one unit (chain,
 // group) for all of that unit's segments.  Per step it streams the
-// propagation matrix through shared memory in 32-row chunks of A (A = M going
-// forward, M^T in reverse), keeps the state tile in shared memory, and each of
-// its 256 threads accumulates R x 4 outputs (R = K / 32 rows spaced 32 apart,
-// 4 adjacent columns) in registers.
+// propagation matrix through shared memory in 32-wide k chunks of A (A = M
+// going forward, M^T in reverse), keeps the state tile in shared memory, and
+// each of its 256 threads accumulates R x 4 outputs (R = K / 32 rows spaced 32
+// apart, 4 adjacent columns) in registers.  The chunks go through a two-stage
+// ring filled with cp.async one chunk ahead, across step boundaries too (M
+// does not depend on the state), so a chunk's global latency overlaps the
+// previous chunk's arithmetic.
 //
 // In-place (out == H): a thread reads its H_seg elements before it writes
 // out[seg] over the same addresses, and no other thread touches them.
@@ -30,12 +33,33 @@ __device__ __forceinline__ int64_t state_index(int layout, int K, int V, int k, 
   return layout == 0 ? (int64_t)k * V + v : (int64_t)v * K + k;
 }
 
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Floats of one chunk stage: forward [K rows m][33] (row m of A, 32 k + pad),
+// reverse [32 rows k][K + 1] (row k of M = column of A, + pad).  Both pads keep
+// the compute's shared loads free of bank conflicts.
+template <int K>
+__host__ __device__ constexpr int stage_floats() {
+  return K * 33 > 32 * (K + 1) ? K * 33 : 32 * (K + 1);
+}
+
 template <int R, int LAYOUT>
 __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
   constexpr int K = R * 32;
+  constexpr int CH = K / 32;  // chunks per step
+  constexpr int SF = stage_floats<K>();
   extern __shared__ __align__(16) float smem[];
   float* Xs = smem;                 // [K][kXsLd]    state tile, kv view
-  float* As = smem + K * kXsLd;     // [32][K + 1]   chunk of A, transposed: As[kk][m] = A[m][kc + kk]
+  float* As = smem + K * kXsLd;     // [2][SF]       chunk ring
 
   const int t = threadIdx.x;
   // kv: 8 column groups across a warp, so float4 global accesses along v coalesce.
@@ -54,6 +78,7 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
   const int s_lo = g * j.L;
   const int n = min(j.L, S - s_lo);
   const int64_t st = (int64_t)K * V;
+  const bool fwd = j.direction == 0;
 
   const float* Hc = j.H ? j.H + cbase * st : nullptr;
   float* Oc = j.out ? j.out + cbase * st : nullptr;
@@ -75,8 +100,30 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
   }
 
   const int nsteps = n - 1 + (j.fin ? 1 : 0);
+  const int total = nsteps > 0 ? nsteps * CH : 0;  // chunks over all steps
+  auto seg_of = [&](int jj) { return fwd ? s_lo + jj : s_lo + n - 1 - jj; };
+  // Chunk c (step c / CH, k block c % CH) -> stage c & 1, one 4-byte cp.async
+  // per element: forward A[m][kc + kk] = M[m][kc + kk], reverse A[m][kc + kk] =
+  // M[kc + kk][m]; consecutive threads read consecutive global floats.
+  auto issue_chunk = [&](int c) {
+    const float* Ms = Mc + (int64_t)seg_of(c / CH) * K * K;
+    const int kc = (c % CH) * 32;
+    float* dst = As + (c & 1) * SF;
+    for (int e = t; e < 32 * K; e += kThreads) {
+      if (fwd) {
+        const int m = e >> 5, kk = e & 31;
+        cp_async4(dst + m * 33 + kk, Ms + (int64_t)m * K + kc + kk);
+      } else {
+        const int kk = e / K, m = e - kk * K;
+        cp_async4(dst + kk * (K + 1) + m, Ms + (int64_t)(kc + kk) * K + m);
+      }
+    }
+  };
+  if (total > 0) issue_chunk(0);
+  cp_async_commit();
+
   for (int jj = 0; jj < n; ++jj) {
-    const int seg = j.direction == 0 ? s_lo + jj : s_lo + n - 1 - jj;
+    const int seg = seg_of(jj);
     const bool do_step = jj < nsteps;
     float h[R][4];
 #pragma unroll
@@ -112,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
     }
     if (!do_step) break;
 
-    __syncthreads();  // the previous step's readers of Xs and As are done
+    __syncthreads();  // the previous step's readers of Xs are done
 #pragma unroll
     for (int q = 0; q < R; ++q)
       *reinterpret_cast<float4*>(Xs + (rg + 32 * q) * kXsLd + cg * 4) =
@@ -124,29 +171,21 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[q][e] = 0.f;
 
-    const float* Ms = Mc + (int64_t)seg * K * K;
-    for (int kc = 0; kc < K; kc += 32) {
-      __syncthreads();  // Xs written; the previous chunk's readers of As are done
-      if (j.direction == 0) {
-        // A = M: As[kk][m] = M[m][kc + kk]; 32 consecutive kk per m keep the global reads coalesced.
-        for (int e = t; e < 32 * K; e += kThreads) {
-          const int m = e >> 5, kk = e & 31;
-          As[kk * (K + 1) + m] = __ldg(Ms + (int64_t)m * K + kc + kk);
-        }
-      } else {
-        // A = M^T: As[kk][m] = M[kc + kk][m].
-        for (int e = t; e < 32 * K; e += kThreads) {
-          const int kk = e / K, m = e - kk * K;
-          As[kk * (K + 1) + m] = __ldg(Ms + (int64_t)(kc + kk) * K + m);
-        }
-      }
-      __syncthreads();
+    for (int kb = 0; kb < CH; ++kb) {
+      const int c = jj * CH + kb;
+      __syncthreads();  // every thread is done with chunk c - 1, whose stage chunk c + 1 reuses; Xs written
+      if (c + 1 < total) issue_chunk(c + 1);
+      cp_async_commit();
+      cp_async_wait<1>();  // this thread's copies of chunk c have landed
+      __syncthreads();     // everyone's have
+      const float* A = As + (c & 1) * SF;
+      const int kc = kb * 32;
 #pragma unroll 8
       for (int kk = 0; kk < 32; ++kk) {
         const float4 xv = *reinterpret_cast<const float4*>(Xs + (kc + kk) * kXsLd + cg * 4);
 #pragma unroll
         for (int q = 0; q < R; ++q) {
-          const float a = As[kk * (K + 1) + rg + 32 * q];
+          const float a = fwd ? A[(rg + 32 * q) * 33 + kk] : A[kk * (K + 1) + rg + 32 * q];
           acc[q][0] = fmaf(a, xv.x, acc[q][0]);
           acc[q][1] = fmaf(a, xv.y, acc[q][1]);
           acc[q][2] = fmaf(a, xv.z, acc[q][2]);
@@ -159,6 +198,7 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) x[q][e] = acc[q][e] + h[q][e];
   }
+  cp_async_wait<0>();  // no copy may land after the CTA is gone
 
   if (j.fin) {
     float* F = j.fin + u * j.fin_unit_stride;
@@ -174,7 +214,7 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
 template <int R, int LAYOUT>
 cudaError_t launch_one(const SeqJob& j, cudaStream_t stream) {
   constexpr int K = R * 32;
-  const size_t smem = sizeof(float) * ((size_t)K * kXsLd + 32 * (size_t)(K + 1));
+  const size_t smem = sizeof(float) * ((size_t)K * kXsLd + 2 * (size_t)stage_floats<K>());
   auto kern = seq_simt_kernel<R, LAYOUT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
