@@ -342,23 +342,19 @@ int fork_join(const DeviceInfo* d, cudaStream_t stream, MainFn&& on_main, SideFn
 //  2.  The same recurrence over the G aggregates, (M', H') = (A_g, b_g), from
 //      h_init: its exclusive outputs are the states entering each group.
 //  3.  Every group re-run from its entering state, writing out.
-int run_scan(const float* H, const float* M, const float* h_init, float* out, float* fin, const Shape& s,
-             int engine, int release, int group, const DeviceInfo* d, cudaStream_t stream) {
-  const int G = group > 0 ? std::min(group, s.S) : auto_groups(s.S);
-  const int L = (s.S + G - 1) / G;
-  const int Gr = (s.S + L - 1) / L;  // groups actually formed
-  const size_t bytes = scan_bytes(s, Gr);
-  float* ws = nullptr;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), bytes, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(scan workspace)");
+// `base` is the job of the whole call (fixed length, or variable length with
+// offsets: then phases 1a, 1b and 3 locate each (chain, group) through them,
+// and a group past its sequence's end is empty, with the identity and zero
+// as aggregates, which phase 2 steps through unchanged in either direction).
+// `ws` holds A_agg [chains][Gr][K][K], then b_agg and carries
+// [chains][Gr][state] (scan_bytes).
+int scan_phases(const SeqJob& base, const Shape& s, int L, int Gr, float* ws, int engine, int release,
+                const DeviceInfo* d, cudaStream_t stream) {
+  const int64_t chains = base.nchains;
   float* Aagg = ws;
-  float* bagg = Aagg + (size_t)s.chains() * Gr * s.K * s.K;
-  float* carry = bagg + (size_t)s.chains() * Gr * s.state();
-  const SeqJob base = plain_job(H, M, h_init, out, fin, s);
-  int st = QLA_OK;
-
-  // 1a (group products of M, forward, kv view, from the identity) and 1b
-  // (group recurrences from zero) are independent: they run concurrently.
+  float* bagg = Aagg + (size_t)chains * Gr * s.K * s.K;
+  float* carry = bagg + (size_t)chains * Gr * s.state();
+  // 1a and 1b are independent: they run concurrently.
   SeqJob j1a = base;
   j1a.H = nullptr;
   j1a.init = nullptr;
@@ -379,23 +375,25 @@ int run_scan(const float* H, const float* M, const float* h_init, float* out, fl
   j1b.fin_unit_stride = s.state();
   j1b.L = L;
   j1b.G = Gr;
-  st = fork_join(
+  int st = fork_join(
       d, stream, [&](cudaStream_t cs) { return launch_seq(j1a, engine_for(j1a, engine), release, d, cs); },
       [&](cudaStream_t cs) { return launch_seq(j1b, engine_for(j1b, engine), release, d, cs); });
-  if (st == QLA_OK) {  // 2: carries across the group aggregates
+  if (st != QLA_OK) return st;
+  {  // 2: carries across the group aggregates (fixed length Gr per chain)
     SeqJob j = base;
+    j.cu_seg = nullptr;
     j.H = bagg;
     j.M = Aagg;
     j.h_chain_stride = (int64_t)Gr * s.state();
     j.m_chain_stride = (int64_t)Gr * s.K * s.K;
     j.out = carry;
-    j.fin = fin;
     j.S = Gr;
     j.L = Gr;
     j.G = 1;
-    st = launch_seq(j, engine_for(j, engine), release, d, stream);
+    j.nstates = chains * Gr;
+    if ((st = launch_seq(j, engine_for(j, engine), release, d, stream)) != QLA_OK) return st;
   }
-  if (st == QLA_OK && out) {  // 3: re-run each group from its entering state
+  if (base.out) {  // 3: re-run each group from its entering state
     SeqJob j = base;
     j.init = carry;
     j.init_mode = kInitPointer;
@@ -403,11 +401,37 @@ int run_scan(const float* H, const float* M, const float* h_init, float* out, fl
     j.fin = nullptr;
     j.L = L;
     j.G = Gr;
-    st = launch_seq(j, engine_for(j, engine), release, d, stream);
+    if ((st = launch_seq(j, engine_for(j, engine), release, d, stream)) != QLA_OK) return st;
   }
+  return QLA_OK;
+}
+
+// Group length L and the number of groups actually formed for S segments and
+// a requested group count (0: automatic).
+void scan_groups_for(int S, int group, int* L, int* Gr) {
+  const int G = group > 0 ? std::min(group, S) : auto_groups(S);
+  *L = (S + G - 1) / G;
+  *Gr = (S + *L - 1) / *L;
+}
+
+// The scan with its workspace from the stream-ordered allocator.
+int run_scan_alloc(const SeqJob& base, const Shape& s, int engine, int release, int group, const DeviceInfo* d,
+                   cudaStream_t stream) {
+  int L, Gr;
+  scan_groups_for(s.S, group, &L, &Gr);
+  const size_t bytes = (size_t)base.nchains * Gr * ((size_t)s.K * s.K + 2 * (size_t)s.state()) * sizeof(float);
+  float* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), bytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(scan workspace)");
+  const int st = scan_phases(base, s, L, Gr, ws, engine, release, d, stream);
   e = cudaFreeAsync(ws, stream);
   if (st == QLA_OK && e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(scan workspace)");
   return st;
+}
+
+int run_scan(const float* H, const float* M, const float* h_init, float* out, float* fin, const Shape& s,
+             int engine, int release, int group, const DeviceInfo* d, cudaStream_t stream) {
+  return run_scan_alloc(plain_job(H, M, h_init, out, fin, s), s, engine, release, group, d, stream);
 }
 
 // ---------------------------------------------------------------- allocation-free scan
@@ -437,141 +461,20 @@ int scan_static_pointer(float** out) {
   return QLA_OK;
 }
 
-// The four scan phases of run_scan(), on a caller-provided workspace.
+// The scan phases on a caller-provided workspace (`group` groups requested,
+// 0 = automatic, as for the workspace size).
 int run_scan_in(const float* H, const float* M, const float* h_init, float* out, float* fin, const Shape& s,
-                int engine, int release, int G, float* ws, const DeviceInfo* d, cudaStream_t stream) {
-  const int L = (s.S + G - 1) / G;
-  const int Gr = (s.S + L - 1) / L;
-  float* Aagg = ws;
-  float* bagg = Aagg + (size_t)s.chains() * Gr * s.K * s.K;
-  float* carry = bagg + (size_t)s.chains() * Gr * s.state();
-  const SeqJob base = plain_job(H, M, h_init, out, fin, s);
-  int st;
-  // 1a (group products of M, forward, kv view, from the identity) and 1b
-  // (group recurrences from zero) are independent: they run concurrently.
-  SeqJob j1a = base;
-  j1a.H = nullptr;
-  j1a.init = nullptr;
-  j1a.init_mode = kInitIdentity;
-  j1a.out = nullptr;
-  j1a.fin = Aagg;
-  j1a.fin_unit_stride = (int64_t)s.K * s.K;
-  j1a.L = L;
-  j1a.G = Gr;
-  j1a.V = s.K;
-  j1a.layout = QLA_LAYOUT_KV;
-  j1a.direction = QLA_FORWARD;
-  SeqJob j1b = base;
-  j1b.init = nullptr;
-  j1b.init_mode = kInitZero;
-  j1b.out = nullptr;
-  j1b.fin = bagg;
-  j1b.fin_unit_stride = s.state();
-  j1b.L = L;
-  j1b.G = Gr;
-  st = fork_join(
-      d, stream, [&](cudaStream_t cs) { return launch_seq(j1a, engine_for(j1a, engine), release, d, cs); },
-      [&](cudaStream_t cs) { return launch_seq(j1b, engine_for(j1b, engine), release, d, cs); });
-  if (st != QLA_OK) return st;
-  {  // 2: carries across the group aggregates
-    SeqJob j = base;
-    j.H = bagg;
-    j.M = Aagg;
-    j.h_chain_stride = (int64_t)Gr * s.state();
-    j.m_chain_stride = (int64_t)Gr * s.K * s.K;
-    j.out = carry;
-    j.fin = fin;
-    j.S = Gr;
-    j.L = Gr;
-    j.G = 1;
-    if ((st = launch_seq(j, engine_for(j, engine), release, d, stream)) != QLA_OK) return st;
-  }
-  if (out) {  // 3: re-run each group from its entering state
-    SeqJob j = base;
-    j.init = carry;
-    j.init_mode = kInitPointer;
-    j.init_unit_stride = s.state();
-    j.fin = nullptr;
-    j.L = L;
-    j.G = Gr;
-    if ((st = launch_seq(j, engine_for(j, engine), release, d, stream)) != QLA_OK) return st;
-  }
-  return QLA_OK;
+                int engine, int release, int group, float* ws, const DeviceInfo* d, cudaStream_t stream) {
+  int L, Gr;
+  scan_groups_for(s.S, group, &L, &Gr);
+  return scan_phases(plain_job(H, M, h_init, out, fin, s), s, L, Gr, ws, engine, release, d, stream);
 }
 
-// The scan variant for variable-length calls.  Every chain gets G groups of
-// L segments, L = ceil(Smax / G) from the caller's bound Smax on any
-// sequence's length; groups past a sequence's end are empty, so their
-// aggregates are the identity (1a) and zero (1b), and phase 2 steps through
-// them unchanged (in either direction).  Phases 1a, 1b and 3 locate each
-// (chain, group) through the offsets; phase 2 is a fixed-length recurrence
-// over the G aggregates of each chain.
+// The scan variant for variable-length calls: every chain gets the groups
+// that the caller's bound s.S on any sequence's length needs (scan_phases).
 int run_scan_varlen(const SeqJob& vj, const Shape& s, int engine, int group, const DeviceInfo* d,
                     cudaStream_t stream) {
-  const int G = group > 0 ? std::min(group, s.S) : auto_groups(s.S);
-  const int L = (s.S + G - 1) / G;
-  const int Gr = (s.S + L - 1) / L;  // groups actually formed
-  const int64_t chains = vj.nchains;
-  const size_t bytes = (size_t)chains * Gr * ((size_t)s.K * s.K + 2 * (size_t)s.state()) * sizeof(float);
-  float* ws = nullptr;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), bytes, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(scan workspace)");
-  float* Aagg = ws;
-  float* bagg = Aagg + (size_t)chains * Gr * s.K * s.K;
-  float* carry = bagg + (size_t)chains * Gr * s.state();
-  int st = QLA_OK;
-  // 1a (group products of M, forward, kv view, from the identity) and 1b
-  // (group recurrences from zero) are independent: they run concurrently.
-  SeqJob j1a = vj;
-  j1a.H = nullptr;
-  j1a.init = nullptr;
-  j1a.init_mode = kInitIdentity;
-  j1a.out = nullptr;
-  j1a.fin = Aagg;
-  j1a.fin_unit_stride = (int64_t)s.K * s.K;
-  j1a.L = L;
-  j1a.G = Gr;
-  j1a.V = s.K;
-  j1a.layout = QLA_LAYOUT_KV;
-  j1a.direction = QLA_FORWARD;
-  SeqJob j1b = vj;
-  j1b.init = nullptr;
-  j1b.init_mode = kInitZero;
-  j1b.out = nullptr;
-  j1b.fin = bagg;
-  j1b.fin_unit_stride = s.state();
-  j1b.L = L;
-  j1b.G = Gr;
-  st = fork_join(
-      d, stream, [&](cudaStream_t cs) { return launch_seq(j1a, engine_for(j1a, engine), QLA_RELEASE_MEMBAR, d, cs); },
-      [&](cudaStream_t cs) { return launch_seq(j1b, engine_for(j1b, engine), QLA_RELEASE_MEMBAR, d, cs); });
-  if (st == QLA_OK) {  // 2: carries across the group aggregates (fixed length Gr per chain)
-    SeqJob j = vj;
-    j.cu_seg = nullptr;
-    j.H = bagg;
-    j.M = Aagg;
-    j.h_chain_stride = (int64_t)Gr * s.state();
-    j.m_chain_stride = (int64_t)Gr * s.K * s.K;
-    j.out = carry;
-    j.S = Gr;
-    j.L = Gr;
-    j.G = 1;
-    j.nstates = chains * Gr;
-    st = launch_seq(j, engine_for(j, engine), QLA_RELEASE_MEMBAR, d, stream);
-  }
-  if (st == QLA_OK && vj.out) {  // 3: re-run each group from its entering state
-    SeqJob j = vj;
-    j.init = carry;
-    j.init_mode = kInitPointer;
-    j.init_unit_stride = s.state();
-    j.fin = nullptr;
-    j.L = L;
-    j.G = Gr;
-    st = launch_seq(j, engine_for(j, engine), QLA_RELEASE_MEMBAR, d, stream);
-  }
-  e = cudaFreeAsync(ws, stream);
-  if (st == QLA_OK && e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(scan workspace)");
-  return st;
+  return run_scan_alloc(vj, s, engine, QLA_RELEASE_MEMBAR, group, d, stream);
 }
 
 }  // namespace
@@ -594,9 +497,9 @@ int qla_cp_correct_scan_static(const float* H, const float* M, const float* h_in
   if (release < QLA_RELEASE_MEMBAR || release > QLA_RELEASE_NONE)
     return fail(QLA_ERR_INVALID_ARG, "unknown release mode %d", release);
   if (scan_group < 0) return fail(QLA_ERR_INVALID_ARG, "scan_group must be >= 0");
-  const int G = scan_group > 0 ? std::min(scan_group, S) : auto_groups(S);
-  const int L = (S + G - 1) / G;
-  const size_t need = scan_bytes(s, (S + L - 1) / L);
+  int L, Gr;
+  scan_groups_for(S, scan_group, &L, &Gr);
+  const size_t need = scan_bytes(s, Gr);
   if (need > QLA_SCAN_STATIC_BYTES)
     return fail(QLA_ERR_UNSUPPORTED,
                 "this shape needs %zu bytes of scan scratch; the allocation-free scan holds %u bytes "
@@ -609,7 +512,7 @@ int qla_cp_correct_scan_static(const float* H, const float* M, const float* h_in
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const int eng = resolve_engine(s, engine);
   if (S == 1) return launch_seq(plain_job(H, M, h_init, out, final_state, s), eng, release, d, cs);
-  return run_scan_in(H, M, h_init, out, final_state, s, eng, release, G, ws, d, cs);
+  return run_scan_in(H, M, h_init, out, final_state, s, eng, release, scan_group, ws, d, cs);
 }
 
 const char* qla_status_string(int status) {
@@ -631,9 +534,9 @@ const char* qla_last_error(void) { return t_last_error.c_str(); }
 size_t qla_scan_workspace_bytes(int B, int heads, int S, int K, int V, int scan_group) {
   if (B < 1 || heads < 1 || S < 1 || K < 1 || V < 1) return 0;
   Shape s{B, heads, S, K, V, 0, 0};
-  const int G = scan_group > 0 ? std::min(scan_group, S) : auto_groups(S);
-  const int L = (S + G - 1) / G;
-  return scan_bytes(s, (S + L - 1) / L);
+  int L, Gr;
+  scan_groups_for(S, scan_group, &L, &Gr);
+  return scan_bytes(s, Gr);
 }
 
 int qla_set_variant(int variant) {
