@@ -85,9 +85,6 @@
 // Every wait is bounded (see ptx.cuh); on expiry the CTA drains its copies in
 // flight, frees TMEM and returns with the device status word set.
 #include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
 
 #include "ptx.cuh"
 #include "qla_internal.h"
@@ -877,19 +874,7 @@ cudaError_t launch_k(const SeqJob& j, int release, unsigned int* status, uint64_
   p.in_place = j.out != nullptr && (const void*)j.out == (const void*)j.H;
   p.release = release;
   p.stall_test = stall_test;
-  const uint64_t states = j.cu_seg ? (uint64_t)j.nstates : (uint64_t)j.nchains * j.S;
-  const bool kv = j.layout == 0;
-  const uint64_t rows = states * (kv ? (uint64_t)K : (uint64_t)j.V);
-  const uint64_t cols = kv ? (uint64_t)j.V : (uint64_t)K;
-  // H: kv box VT columns x K rows ((4 VT)-byte swizzle); vk box K columns x VT rows
-  if (p.has_h && !make_map(&p.map_h, j.H, rows, cols, kv ? VT : K, kv ? K : VT, kv ? 4 * VT : 0))
-    return cudaErrorInvalidValue;
-  // out: per-warp stores of [32 rows][EC columns] (kv, (4 EC)-byte swizzle) or [EC rows][32 columns] (vk)
-  if (j.out && !make_map(&p.map_out, j.out, rows, cols, kv ? C::EC : 32, kv ? 32 : C::EC, kv ? 4 * C::EC : 0))
-    return cudaErrorInvalidValue;
-  const bool fwd = j.direction == 0;
-  if (!make_map(&p.map_m, j.M, states * K, K, fwd ? 32 : 128, fwd ? 128 : 32, fwd ? 128 : 0))
-    return cudaErrorInvalidValue;
+  if (!make_job_maps(j, VT, C::EC, &p.map_h, &p.map_out, &p.map_m)) return cudaErrorInvalidValue;
   auto kern = seq_tc_kernel<K, TILES, VT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
@@ -916,51 +901,11 @@ extern "C" __attribute__((visibility("default"))) int qla_debug_trace(long long*
 }
 #endif
 
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows,
-              int swizzle) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 4};
-  cuuint32_t box[2] = {box_cols, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapSwizzle sw = swizzle == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
-                                : swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                : swizzle == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
-                                                : CU_TENSOR_MAP_SWIZZLE_NONE;
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 bool tc_supports(int K, int V) { return (K == 128 || K == 256) && V % kCtaCols == 0 && V >= kCtaCols; }
 
 cudaError_t launch_seq_tc(const SeqJob& job, int release, unsigned int* status, uint64_t limit_ns, int stall_test,
                           cudaStream_t stream) {
-  if (!tc_supports(job.K, job.V)) return cudaErrorInvalidValue;
-  if ((int64_t)job.nchains * job.G > 65535) return cudaErrorInvalidValue;
-  // The tensor maps view H/out and M as 2-D arrays of all chains' states, so
-  // chains must be packed back to back (H and out are absent in scan phase 1a;
-  // variable-length jobs locate every chain and group through the offsets).
-  if (!job.cu_seg) {
-    if ((job.H || job.out) && job.h_chain_stride != (int64_t)job.S * job.K * job.V) return cudaErrorInvalidValue;
-    if (job.m_chain_stride != (int64_t)job.S * job.K * job.K) return cudaErrorInvalidValue;
-  }
+  if (!tc_supports(job.K, job.V) || !tma_job_supported(job)) return cudaErrorInvalidValue;
   // One column tile per CTA.  (Two tiles per CTA, with tile 0's epilogue
   // overlapping tile 1's MMAs, measured slower on the 32-head K=V=128 S=8
   // workload: 27.6 us against 19.9 us per call.)

@@ -750,15 +750,7 @@ bool tc_f16_supports(int K, int V) { return K == 128 && V % h16::VT == 0 && V >=
 cudaError_t launch_seq_tc_f16(const SeqJob& j, int release, unsigned int* status, uint64_t limit_ns, int stall_test,
                               cudaStream_t stream) {
   using namespace h16;
-  if (!tc_f16_supports(j.K, j.V)) return cudaErrorInvalidValue;
-  if ((int64_t)j.nchains * j.G > 65535) return cudaErrorInvalidValue;
-  // The tensor maps view H/out and M as 2-D arrays of all chains' states, so
-  // chains must be packed back to back (variable-length jobs locate every
-  // chain through its offsets).
-  if (!j.cu_seg) {
-    if ((j.H || j.out) && j.h_chain_stride != (int64_t)j.S * j.K * j.V) return cudaErrorInvalidValue;
-    if (j.m_chain_stride != (int64_t)j.S * j.K * j.K) return cudaErrorInvalidValue;
-  }
+  if (!tc_f16_supports(j.K, j.V) || !tma_job_supported(j)) return cudaErrorInvalidValue;
   H16Params p;
   memset(&p, 0, sizeof p);
   p.job = j;
@@ -768,19 +760,7 @@ cudaError_t launch_seq_tc_f16(const SeqJob& j, int release, unsigned int* status
   p.in_place = j.out != nullptr && (const void*)j.out == (const void*)j.H;
   p.release = release;
   p.stall_test = stall_test;
-  const uint64_t states = j.cu_seg ? (uint64_t)j.nstates : (uint64_t)j.nchains * j.S;
-  const bool kv = j.layout == 0;
-  const uint64_t rows = states * (kv ? (uint64_t)K : (uint64_t)j.V);
-  const uint64_t cols = kv ? (uint64_t)j.V : (uint64_t)K;
-  // H: kv box 32 columns x 128 rows (128-byte swizzle); vk box 128 columns x 32 rows
-  if (p.has_h && !make_map(&p.map_h, j.H, rows, cols, kv ? VT : K, kv ? K : VT, kv ? 128 : 0))
-    return cudaErrorInvalidValue;
-  // out: per-warp stores of [32 rows][8 columns] (kv, 32-byte swizzle) or [8 rows][32 columns] (vk)
-  if (j.out && !make_map(&p.map_out, j.out, rows, cols, kv ? EC : 32, kv ? 32 : EC, kv ? 4 * EC : 0))
-    return cudaErrorInvalidValue;
-  const bool fwd = j.direction == 0;
-  if (!make_map(&p.map_m, j.M, states * K, K, fwd ? 32 : 128, fwd ? 128 : 32, fwd ? 128 : 0))
-    return cudaErrorInvalidValue;
+  if (!make_job_maps(j, VT, EC, &p.map_h, &p.map_out, &p.map_m)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(seq_tc_f16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(j.V / VT, j.nchains * j.G);
