@@ -79,6 +79,9 @@ EDGE = [
     (2, 1, 9, 128, 64, True),
     (1, 3, 6, 256, 128, False),
     (1, 1, 3, 224, 96, True),
+    (1, 2, 3, 128, 32, True),   # one column tile per chain
+    (1, 1, 4, 128, 256, True),  # eight column tiles per chain
+    (2, 2, 2, 256, 32, False),
 ]
 
 
