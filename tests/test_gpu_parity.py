@@ -275,3 +275,31 @@ def test_process_wide_variant_override():
     r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == "scan"
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+def test_long_norm_preserving_chain(engine):
+    """S = 128 with orthogonal M (no decay): the worst case for the tensor-core
+    engines' accumulators, which round toward zero (a coherent shrink of about
+    4e-8 per step); still inside the bar."""
+    if not engine_supports(engine, 128, 128):
+        pytest.skip(f"engine {engine} does not take K=128")
+    c = qi.Case(B=1, heads=2, S=128, K=128, V=128, seed=11, m_kind="orthogonal", m_scale=1.0, h_scale=0.1,
+                init_kind="gaussian", init_scale=0.1)
+    H, M, h0 = qi.make_inputs(c, "kv")
+    for direction in DIRS:
+        ref, _ = oracle.cp_correct(H, M, h0, "kv", direction)
+        got, _ = run(H, M, h0, "kv", direction, engine=engine, variant="seq")
+        assert_parity(got, ref, what=f"S=128 orthogonal {direction} {engine}")
+
+
+def test_ffma_engine_on_a_very_long_chain():
+    """S = 512 with orthogonal M: the FFMA engine (round-to-nearest fp32
+    accumulation) stays inside the bar where the tensor-core engines' drift
+    does not (1.3e-5 at S = 256, 2.6e-5 at S = 512, measured)."""
+    c = qi.Case(B=1, heads=1, S=512, K=128, V=64, seed=13, m_kind="orthogonal", m_scale=1.0, h_scale=0.1,
+                init_kind="gaussian", init_scale=0.1)
+    H, M, h0 = qi.make_inputs(c, "vk")
+    ref, _ = oracle.cp_correct(H, M, h0, "vk", "fwd")
+    got, _ = run(H, M, h0, "vk", "fwd", engine="simt", variant="seq")
+    assert_parity(got, ref, what="S=512 orthogonal simt")
