@@ -198,6 +198,23 @@ QLA_API size_t qla_scan_workspace_bytes(int B, int heads, int S, int K, int V, i
  * beyond the parity bar (the variants compute the same recurrence). */
 QLA_API int qla_set_variant(int variant);
 
+/* Process-wide switch (0 off, 1 on) for programmatic dependent launch
+ * (xuesongtap, "PTX 内存一致性", section on PDL and griddepcontrol): when on,
+ * the sequential variant's kernel is launched with programmatic stream
+ * serialization, so it may become resident while the stream's previous kernel
+ * is still running, once that kernel has triggered (griddepcontrol.
+ * launch_dependents) in all its CTAs.  Every kernel of this library executes
+ * griddepcontrol.wait before its first global-memory access (H, M, h_init,
+ * the offsets, out, final_state), so data the previous kernel writes is
+ * read only after that kernel has completed and its writes are visible: the
+ * trigger never stands for data readiness.  The kernels trigger their own
+ * dependents after their last step.  The scan variant's launches follow an
+ * allocation or an event and are never dependent launches.  Initial value from
+ * the environment variable QLA_PDL ("1" or "on": on; anything else: off), read
+ * at the first call that needs it.  Returns QLA_ERR_INVALID_ARG for other
+ * values. */
+QLA_API int qla_set_dependent_launch(int enable);
+
 /* The variant and engine QLA_*_AUTO resolve to for this shape on the current
  * device (written to *variant and *engine; either may be NULL). */
 QLA_API int qla_resolve(int B, int heads, int S, int K, int V, int layout, int* variant, int* engine);
@@ -231,6 +248,18 @@ QLA_API int qla_device_status(int* flags);
  */
 QLA_API int qla_selftest_stalled_wait(const float* H, const float* M, float* out, int S,
                               int wait_limit_us, int engine, void* stream);
+
+/*
+ * Test producer for the dependent launch: copies `bytes` (a multiple of 16)
+ * from src to dst (device pointers, 16-byte aligned, not overlapping) on
+ * `stream` with a few CTAs that trigger their dependents at once and then
+ * sleep `delay_us` (0 .. 100000) microseconds before copying.  A correction
+ * launched right after it with the dependent launch switched on starts
+ * during the sleep, so it reads the copied bytes correctly only through its
+ * griddepcontrol.wait.  Returns the launch status.
+ */
+QLA_API int qla_selftest_dependent_producer(const void* src, void* dst, size_t bytes, int delay_us,
+                                            void* stream);
 
 /*
  * The scan variant without any allocation (this entry point has no

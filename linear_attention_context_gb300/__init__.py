@@ -32,9 +32,9 @@ STATUS = {0: "QLA_OK", -1: "QLA_ERR_INVALID_ARG", -2: "QLA_ERR_UNSUPPORTED", -3:
 
 # Every function include/qla.h declares.
 EXPORTS = ("qla_cp_correct", "qla_cp_correct_ex", "qla_cp_correct_varlen", "qla_cp_correct_varlen_ex",
-           "qla_scan_workspace_bytes", "qla_set_variant",
+           "qla_scan_workspace_bytes", "qla_set_variant", "qla_set_dependent_launch",
            "qla_resolve", "qla_status_string", "qla_last_error", "qla_device_status", "qla_selftest_stalled_wait",
-           "qla_cp_correct_scan_static", "qla_version")
+           "qla_selftest_dependent_producer", "qla_cp_correct_scan_static", "qla_version")
 
 # Bytes of scratch the allocation-free scan entry point holds (QLA_SCAN_STATIC_BYTES).
 SCAN_STATIC_BYTES = 8 << 20
@@ -73,6 +73,10 @@ def lib():
         L.qla_cp_correct_varlen_ex.restype = ci
         L.qla_set_variant.argtypes = [ci]
         L.qla_set_variant.restype = ci
+        L.qla_set_dependent_launch.argtypes = [ci]
+        L.qla_set_dependent_launch.restype = ci
+        L.qla_selftest_dependent_producer.argtypes = [vp, vp, ctypes.c_size_t, ci, vp]
+        L.qla_selftest_dependent_producer.restype = ci
         L.qla_scan_workspace_bytes.argtypes = [ci] * 6
         L.qla_scan_workspace_bytes.restype = cz
         L.qla_resolve.argtypes = [ci] * 6 + [ctypes.POINTER(ci), ctypes.POINTER(ci)]
@@ -224,6 +228,23 @@ def set_variant(variant: str):
     """Process-wide override of the automatic variant choice ("auto", "seq" or
     "scan"); the initial value comes from the QLA_VARIANT environment variable."""
     check(lib().qla_set_variant(VARIANTS[variant]))
+
+
+def set_dependent_launch(enable: bool):
+    """Process-wide switch for programmatic dependent launch of the sequential
+    variant's kernel; the initial value comes from the QLA_PDL environment
+    variable."""
+    check(lib().qla_set_dependent_launch(1 if enable else 0))
+
+
+def selftest_dependent_producer(src, dst, delay_us: int, stream=None):
+    """Copies src into dst (same-size contiguous CUDA tensors) with a test
+    producer that lets its dependents start at once and copies only after
+    `delay_us` microseconds."""
+    if src.numel() * src.element_size() != dst.numel() * dst.element_size():
+        raise ValueError("src and dst differ in size")
+    check(lib().qla_selftest_dependent_producer(_ptr(src), _ptr(dst), src.numel() * src.element_size(),
+                                                int(delay_us), _stream_handle(stream)))
 
 
 def scan_workspace_bytes(B, heads, S, K, V, scan_group=0) -> int:

@@ -242,6 +242,28 @@ int variant_override() {
   return v;
 }
 
+// Process-wide choice of programmatic dependent launch for the sequential
+// variant's launch (-1: not read yet; initial value from QLA_PDL).
+std::atomic<int> g_dependent_launch{-1};
+
+int dependent_launch() {
+  int v = g_dependent_launch.load(std::memory_order_relaxed);
+  if (v < 0) {
+    const char* e = std::getenv("QLA_PDL");
+    int expected = -1;
+    g_dependent_launch.compare_exchange_strong(expected, (e && (!strcmp(e, "1") || !strcmp(e, "on"))) ? 1 : 0);
+    v = g_dependent_launch.load(std::memory_order_relaxed);
+  }
+  return v;
+}
+
+// The sequential variant's single launch, as a programmatic dependent of the
+// stream's previous kernel when the process-wide switch is on.
+SeqJob dependent(SeqJob j) {
+  j.pdl = dependent_launch();
+  return j;
+}
+
 int resolve_variant(const Shape& s, int variant, const DeviceInfo* d) {
   (void)d;
   if (variant != QLA_VARIANT_AUTO) return variant;
@@ -482,6 +504,24 @@ int run_scan_varlen(const SeqJob& vj, const Shape& s, int engine, int group, con
 
 using namespace qla;
 
+// Test producer for programmatic dependent launch: every CTA lets its
+// dependents start at once, then holds its copy back for `delay_ns`, so a
+// dependent that touched the copied bytes before its griddepcontrol.wait
+// would see their previous contents.  The delay is a bounded sleep on the
+// global timer.
+__global__ void dependent_producer_kernel(const float4* __restrict__ src, float4* __restrict__ dst, size_t n,
+                                          uint64_t delay_ns) {
+  griddep_launch_dependents();
+  uint64_t t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  do {
+    __nanosleep(1000);
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  } while (t - t0 < delay_ns);
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
 extern "C" {
 
 int qla_version(void) { return 100; }
@@ -511,7 +551,7 @@ int qla_cp_correct_scan_static(const float* H, const float* M, const float* h_in
   if ((st = scan_static_pointer(&ws)) != QLA_OK) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const int eng = resolve_engine(s, engine);
-  if (S == 1) return launch_seq(plain_job(H, M, h_init, out, final_state, s), eng, release, d, cs);
+  if (S == 1) return launch_seq(dependent(plain_job(H, M, h_init, out, final_state, s)), eng, release, d, cs);
   return run_scan_in(H, M, h_init, out, final_state, s, eng, release, scan_group, ws, d, cs);
 }
 
@@ -547,6 +587,13 @@ int qla_set_variant(int variant) {
   return QLA_OK;
 }
 
+int qla_set_dependent_launch(int enable) {
+  t_last_error.clear();
+  if (enable != 0 && enable != 1) return fail(QLA_ERR_INVALID_ARG, "enable must be 0 or 1 (got %d)", enable);
+  g_dependent_launch.store(enable, std::memory_order_relaxed);
+  return QLA_OK;
+}
+
 int qla_resolve(int B, int heads, int S, int K, int V, int layout, int* variant, int* engine) {
   t_last_error.clear();
   DeviceInfo* d = nullptr;
@@ -578,7 +625,7 @@ int qla_cp_correct_ex(const float* H, const float* M, const float* h_init, float
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (v == QLA_VARIANT_SCAN && S > 1)
     return run_scan(H, M, h_init, out, final_state, s, eng, release, scan_group, d, cs);
-  return launch_seq(plain_job(H, M, h_init, out, final_state, s), eng, release, d, cs);
+  return launch_seq(dependent(plain_job(H, M, h_init, out, final_state, s)), eng, release, d, cs);
 }
 
 int qla_cp_correct(const float* H, const float* M, const float* h_init, float* out, int B, int heads, int S, int K,
@@ -634,7 +681,7 @@ int qla_cp_correct_varlen_ex(const float* H, const float* M, const float* h_init
   j.heads = heads;
   j.T = T;
   j.nstates = (int64_t)heads * T;
-  if (var == QLA_VARIANT_SEQ || Smax < 2) return launch_seq(j, eng, QLA_RELEASE_MEMBAR, d, cs);
+  if (var == QLA_VARIANT_SEQ || Smax < 2) return launch_seq(dependent(j), eng, QLA_RELEASE_MEMBAR, d, cs);
   return run_scan_varlen(j, s, eng, scan_group, d, cs);
 }
 
@@ -677,6 +724,27 @@ int qla_selftest_stalled_wait(const float* H, const float* M, float* out, int S,
                                           : launch_seq_tc_f16(j, QLA_RELEASE_MEMBAR, d->status_word, limit, 1, cs);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return QLA_OK;
+}
+
+int qla_selftest_dependent_producer(const void* src, void* dst, size_t bytes, int delay_us, void* stream) {
+  t_last_error.clear();
+  if (!src || !dst) return fail(QLA_ERR_INVALID_ARG, "src and dst must not be NULL");
+  if (bytes % 16) return fail(QLA_ERR_INVALID_ARG, "bytes must be a multiple of 16 (got %zu)", bytes);
+  if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15)
+    return fail(QLA_ERR_ALIGNMENT, "src and dst must be 16-byte aligned");
+  const uintptr_t a = reinterpret_cast<uintptr_t>(src), b = reinterpret_cast<uintptr_t>(dst);
+  if (bytes && a < b + bytes && b < a + bytes) return fail(QLA_ERR_ALIAS, "src and dst overlap");
+  if (delay_us < 0 || delay_us > 100000) return fail(QLA_ERR_INVALID_ARG, "delay_us must be in [0, 100000]");
+  DeviceInfo* d = nullptr;
+  int st = current_device(&d);
+  if (st != QLA_OK) return st;
+  if (bytes == 0 && delay_us == 0) return QLA_OK;
+  // A few CTAs only, so that the dependent grid finds free SMs and starts
+  // while the producer is still sleeping.
+  dependent_producer_kernel<<<std::min(16, d->sm_count), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const float4*>(src), static_cast<float4*>(dst), bytes / 16, (uint64_t)delay_us * 1000ull);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? QLA_OK : cuda_fail(e, "kernel launch");
 }
 
 }  // extern "C"

@@ -35,6 +35,7 @@ struct SeqJob {
   int heads, T;
   int64_t nstates;        // states in H / out / M (nchains * S, or heads * T)
   unsigned int* status;   // device status word (bit 1: invalid offsets)
+  int pdl;                // launch as a programmatic dependent of the stream's previous kernel
 };
 
 enum InitMode { kInitZero = 0, kInitPointer = 1, kInitIdentity = 2 };
@@ -45,6 +46,20 @@ constexpr unsigned int kStatusBadOffsets = 2u;  // variable-length offsets outsi
                                                 // a sequence longer than the scan's bound
 
 #ifdef __CUDACC__
+// Programmatic dependent launch (xuesongtap, "PTX 内存一致性", section on PDL):
+// a kernel launched with programmatic stream serialization may start while the
+// stream's previous kernel is still running, once that kernel's CTAs have all
+// issued launch_dependents or exited.  The trigger says nothing about data:
+// griddepcontrol.wait returns only after the prerequisite grids have completed
+// and their memory operations are visible, so every kernel here executes it
+// before its first global-memory access (it returns at once when the launch
+// has no programmatic prerequisite).  The "memory" clobbers keep the compiler
+// from moving loads, non-coherent ones included, above the wait.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // The segments of chain `chain`: index of its first segment in the packed
 // arrays and its segment count.  Returns false, after recording the event in
 // the status word, when its variable-length offsets are invalid or its
@@ -68,6 +83,23 @@ __device__ __forceinline__ bool chain_span(const SeqJob& j, int chain, int64_t& 
   return true;
 }
 #endif
+
+// Launches `kern` with the optional programmatic-serialization attribute.
+template <class P>
+cudaError_t launch_kernel(void (*kern)(P), dim3 grid, unsigned threads, size_t smem, cudaStream_t stream, bool pdl,
+                          const P& params) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, params);
+}
 
 // seq_simt.cu: plain FFMA kernel, any K, V that are multiples of 32 up to 256.
 cudaError_t launch_seq_simt(const SeqJob& job, cudaStream_t stream);

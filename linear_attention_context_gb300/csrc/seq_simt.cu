@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
   const int g = u - chain * j.G;
   int64_t cbase;  // the chain's first segment in the packed arrays
   int S;
+  griddep_wait();  // (before the first global access: the offsets may be the previous kernel's output)
   if (!chain_span(j, chain, cbase, S)) return;
   const int s_lo = g * j.L;
   const int n = min(j.L, S - s_lo);
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
       for (int e = 0; e < 4; ++e) x[q][e] = acc[q][e] + h[q][e];
   }
   cp_async_wait<0>();  // no copy may land after the CTA is gone
+  griddep_launch_dependents();
 
   if (j.fin) {
     float* F = j.fin + u * j.fin_unit_stride;
@@ -219,8 +221,8 @@ cudaError_t launch_one(const SeqJob& j, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(j.V / kTileV, j.nchains * j.G);
-  kern<<<grid, kThreads, smem, stream>>>(j);
-  return cudaGetLastError();
+  e = launch_kernel(kern, grid, kThreads, smem, stream, j.pdl != 0, j);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int LAYOUT>

@@ -391,6 +391,7 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
   const int g = u - chain * j.G;
   int64_t cbase;  // the chain's first segment in the packed arrays
   int S;
+  griddep_wait();  // (before the first global access: the offsets may be the previous kernel's output)
   if (!chain_span(j, chain, cbase, S)) return;  // invalid offsets: recorded, nothing touched
   const int s_lo = g * j.L;
   const int n = min(j.L, S - s_lo);
@@ -847,6 +848,7 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
     __syncwarp();
   }
 
+  griddep_launch_dependents();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -878,11 +880,9 @@ cudaError_t launch_k(const SeqJob& j, int release, unsigned int* status, uint64_
   auto kern = seq_tc_kernel<K, TILES, VT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
-  // (Programmatic dependent launch, letting this set-up overlap the previous
-  // kernel's tail, measured about 1 us slower per call here; not used.)
   dim3 grid(j.V / (TILES * VT), j.nchains * j.G);
-  kern<<<grid, 32 * C::WARPS, C::SMEM, stream>>>(p);
-  return cudaGetLastError();
+  e = launch_kernel(kern, grid, 32 * C::WARPS, C::SMEM, stream, j.pdl != 0, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -294,6 +294,7 @@ __global__ void __launch_bounds__(32 * h16::WARPS, 1) seq_tc_f16_kernel(const __
   const int g = u - chain * j.G;
   int64_t cbase;  // the chain's first segment in the packed arrays
   int S;
+  griddep_wait();  // (before the first global access: the offsets may be the previous kernel's output)
   if (!chain_span(j, chain, cbase, S)) return;  // invalid offsets: recorded, nothing touched
   const int s_lo = g * j.L;
   const int n = min(j.L, S - s_lo);
@@ -727,6 +728,7 @@ __global__ void __launch_bounds__(32 * h16::WARPS, 1) seq_tc_f16_kernel(const __
     __syncwarp();
   }
 
+  griddep_launch_dependents();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -764,8 +766,8 @@ cudaError_t launch_seq_tc_f16(const SeqJob& j, int release, unsigned int* status
   cudaError_t e = cudaFuncSetAttribute(seq_tc_f16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(j.V / VT, j.nchains * j.G);
-  seq_tc_f16_kernel<<<grid, 32 * WARPS, SMEM, stream>>>(p);
-  return cudaGetLastError();
+  e = launch_kernel(seq_tc_f16_kernel, grid, 32 * WARPS, SMEM, stream, j.pdl != 0, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace qla

@@ -174,3 +174,26 @@ def test_set_variant_checks(L):
     assert L.qla_set_variant(1) == 0
     assert L.qla_set_variant(2) == 0
     assert L.qla_set_variant(0) == 0  # back to the automatic rule for the rest of the process
+
+
+def test_set_dependent_launch_checks(L):
+    assert L.qla_set_dependent_launch(2) == -1
+    assert L.qla_set_dependent_launch(-1) == -1
+    assert L.qla_set_dependent_launch(1) == 0
+    assert L.qla_set_dependent_launch(0) == 0  # off again for the rest of the process
+
+
+@pytest.mark.parametrize("src, dst, nbytes, delay, status", [
+    (None, 0x1000, 16, 0, -1),         # NULL source
+    (0x1000, None, 16, 0, -1),         # NULL destination
+    (0x1000, 0x2000, 20, 0, -1),       # not a multiple of 16 bytes
+    (0x1008, 0x2000, 16, 0, -3),       # misaligned
+    (0x1000, 0x1010, 32, 0, -4),       # overlapping
+    (0x1000, 0x2000, 16, -1, -1),      # negative delay
+    (0x1000, 0x2000, 16, 100001, -1),  # delay above the bound
+])
+def test_dependent_producer_checks(L, src, dst, nbytes, delay, status):
+    # (every case fails its host-side check before the device is touched)
+    vp = ctypes.c_void_p
+    assert L.qla_selftest_dependent_producer(None if src is None else vp(src), None if dst is None else vp(dst),
+                                             nbytes, delay, None) == status
