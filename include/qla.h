@@ -45,8 +45,10 @@
  * returns QLA_ERR_ALIAS.  H, M and h_init are never written.
  *
  * Limits: B, heads, S >= 1; K and V multiples of 32 in [32, 256]; every pointer
- * 16-byte aligned; B*heads*S*K*max(K,V) < 2^62.  The device must be sm_103
- * (GB300): checked once per device, QLA_ERR_ARCH otherwise.
+ * 16-byte aligned; B*heads*S*(V/32) < 2^31 (one CTA per chain and 32-column
+ * tile, per scan group in the scan variant) and B*heads*S*K*max(K,V) < 2^62
+ * (QLA_ERR_UNSUPPORTED or QLA_ERR_INVALID_ARG otherwise).  The device must be
+ * sm_103 (GB300): checked once per device, QLA_ERR_ARCH otherwise.
  */
 #ifndef QLA_H_
 #define QLA_H_
@@ -158,7 +160,8 @@ QLA_API int qla_cp_correct_ex(const float* H, const float* M, const float* h_ini
  * the offsets' values; a kernel that finds a chain's offsets outside [0, T]
  * or decreasing skips that chain (reads and writes nothing for it) and sets
  * bit 1 (value 2) of the device status word (qla_device_status).
- * Requires N * heads <= 65535.
+ * Requires N*heads*(V/32) < 2^31 (times the scan's group count for the scan
+ * variant) and heads*T < 2^31.
  */
 QLA_API int qla_cp_correct_varlen(const float* H, const float* M, const float* h_init, float* out,
                           float* final_state, const int* cu_seg, int N, int T, int heads, int K,

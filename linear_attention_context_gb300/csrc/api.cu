@@ -130,7 +130,9 @@ int check_args(const float* H, const float* M, const float* h_init, const float*
     return fail(QLA_ERR_UNSUPPORTED, "K and V must be multiples of 32 in [32, 256] (got K=%d, V=%d)", s.K, s.V);
   const double elems = (double)s.chains() * s.S * s.K * std::max(s.K, s.V);
   if (elems >= 4.6e18) return fail(QLA_ERR_INVALID_ARG, "problem too large for 64-bit indexing");
-  if (s.chains() * s.S > (int64_t)1 << 31) return fail(QLA_ERR_UNSUPPORTED, "B*heads*S must be below 2^31");
+  // one CTA per (chain, group, 32-column tile): a scan's G groups per chain are at most S
+  if (s.chains() * s.S * ((s.V + 31) / 32) > 0x7fffffff)
+    return fail(QLA_ERR_UNSUPPORTED, "B*heads*S*(V/32) must be below 2^31");
   const void* ptrs[] = {H, M, h_init, out, fin};
   const char* names[] = {"H", "M", "h_init", "out", "final_state"};
   for (int i = 0; i < 5; ++i)
@@ -166,7 +168,7 @@ int check_varlen_args(const float* H, const float* M, const float* h_init, const
   if (!out && !fin) return fail(QLA_ERR_INVALID_ARG, "out and final_state are both NULL: nothing to compute");
   if (K % 32 || K > 256 || V % 32 || V > 256)
     return fail(QLA_ERR_UNSUPPORTED, "K and V must be multiples of 32 in [32, 256] (got K=%d, V=%d)", K, V);
-  if ((int64_t)N * heads > 65535) return fail(QLA_ERR_UNSUPPORTED, "N*heads must be at most 65535");
+  if ((int64_t)N * heads * (V / 32) > 0x7fffffff) return fail(QLA_ERR_UNSUPPORTED, "N*heads*(V/32) must be below 2^31");
   if ((int64_t)heads * T >= (int64_t)1 << 31) return fail(QLA_ERR_UNSUPPORTED, "heads*T must be below 2^31");
   const void* ptrs[] = {H, M, h_init, out, fin};
   const char* names[] = {"H", "M", "h_init", "out", "final_state"};
@@ -682,6 +684,10 @@ int qla_cp_correct_varlen_ex(const float* H, const float* M, const float* h_init
   j.T = T;
   j.nstates = (int64_t)heads * T;
   if (var == QLA_VARIANT_SEQ || Smax < 2) return launch_seq(dependent(j), eng, QLA_RELEASE_MEMBAR, d, cs);
+  int L, Gr;
+  scan_groups_for(s.S, scan_group, &L, &Gr);
+  if ((int64_t)N * heads * Gr * (V / 32) > 0x7fffffff)
+    return fail(QLA_ERR_UNSUPPORTED, "N*heads*G*(V/32) must be below 2^31 for the scan variant");
   return run_scan_varlen(j, s, eng, scan_group, d, cs);
 }
 

@@ -82,7 +82,32 @@ __device__ __forceinline__ bool chain_span(const SeqJob& j, int chain, int64_t& 
   S = s1 - s0;
   return true;
 }
+
+// Grid: x = column tile, units along y and then z (job_grid), so a unit's
+// tiles are adjacent in launch order and the unit count is not held to the
+// 65535 limit of one grid dimension.  Returns false for the padding CTAs of
+// the last z slab, which have no unit.
+__device__ __forceinline__ bool unit_and_tile(const SeqJob& j, int& u, int& tile) {
+  tile = (int)blockIdx.x;
+  if (blockIdx.z == 0) {  // every unit of a grid with at most 65535 of them
+    u = (int)blockIdx.y;
+    return true;
+  }
+  const unsigned uu = blockIdx.z * gridDim.y + blockIdx.y;  // below 65535^2: no wrap
+  u = (int)uu;
+  return uu < (unsigned)(j.nchains * j.G);
+}
 #endif
+
+// The grid of a job with `ntiles` column tiles per unit: (ntiles, units) while
+// the units fit one dimension, else (ntiles, 65535, slabs).  x = 0 when the
+// units exceed 2^31 - 1.
+inline dim3 job_grid(const SeqJob& j, int ntiles) {
+  const int64_t units = (int64_t)j.nchains * j.G;
+  if (units < 1 || units > 0x7fffffff || ntiles < 1) return dim3(0, 1, 1);
+  if (units <= 65535) return dim3((unsigned)ntiles, (unsigned)units, 1);
+  return dim3((unsigned)ntiles, 65535u, (unsigned)((units + 65534) / 65535));
+}
 
 // Launches `kern` with the optional programmatic-serialization attribute.
 template <class P>

@@ -67,9 +67,10 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
   const int cg = LAYOUT == 0 ? (t & 7) : (t >> 5);
   const int rg = LAYOUT == 0 ? (t >> 3) : (t & 31);
   const int V = j.V;
-  const int v0 = blockIdx.x * kTileV + cg * 4;
+  int u, tile;
+  if (!unit_and_tile(j, u, tile)) return;
+  const int v0 = tile * kTileV + cg * 4;
 
-  const int u = blockIdx.y;
   const int chain = u / j.G;
   const int g = u - chain * j.G;
   int64_t cbase;  // the chain's first segment in the packed arrays
@@ -220,7 +221,7 @@ cudaError_t launch_one(const SeqJob& j, cudaStream_t stream) {
   auto kern = seq_simt_kernel<R, LAYOUT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(j.V / kTileV, j.nchains * j.G);
+  const dim3 grid = job_grid(j, j.V / kTileV);
   e = launch_kernel(kern, grid, kThreads, smem, stream, j.pdl != 0, j);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -244,7 +245,7 @@ cudaError_t dispatch_r(const SeqJob& j, cudaStream_t s) {
 
 cudaError_t launch_seq_simt(const SeqJob& job, cudaStream_t stream) {
   if (job.K % 32 || job.K < 32 || job.K > 256 || job.V % kTileV) return cudaErrorInvalidValue;
-  if ((int64_t)job.nchains * job.G > 65535) return cudaErrorInvalidValue;
+  if (job_grid(job, job.V / kTileV).x == 0) return cudaErrorInvalidValue;
   return job.layout == 0 ? dispatch_r<0>(job, stream) : dispatch_r<1>(job, stream);
 }
 

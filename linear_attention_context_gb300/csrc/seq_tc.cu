@@ -386,7 +386,8 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
     g_qla_gt[gt_slot * 2] = now;
   }
 #endif
-  const int u = blockIdx.y;
+  int u, tile;
+  if (!unit_and_tile(j, u, tile)) return;
   const int chain = u / j.G;
   const int g = u - chain * j.G;
   int64_t cbase;  // the chain's first segment in the packed arrays
@@ -396,7 +397,7 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
   const int s_lo = g * j.L;
   const int n = min(j.L, S - s_lo);
   const int nsteps = n - 1 + (j.fin ? 1 : 0);
-  const int vbase = blockIdx.x * (TILES * VT);
+  const int vbase = tile * (TILES * VT);
   if (n <= 0) {  // a sequence without segments: its final state is its initial state
     if (j.fin) {
       float* F = j.fin + u * j.fin_unit_stride;
@@ -412,7 +413,7 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
   const bool fwd = j.direction == 0;
   auto seg_of = [&](int step) { return fwd ? s_lo + step : s_lo + n - 1 - step; };
 #ifdef QLA_TRACE
-  const bool tr = blockIdx.x == 0 && blockIdx.y == 0 &&
+  const bool tr = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&
                   ((threadIdx.x & 31) == 0 &&
                    (warp <= C::NI || warp == C::SPL_WARP0 || warp == C::SPL_WARP0 + 4 || warp == C::EPI_WARP0 ||
                     warp == C::WARPS - 1));
@@ -880,7 +881,7 @@ cudaError_t launch_k(const SeqJob& j, int release, unsigned int* status, uint64_
   auto kern = seq_tc_kernel<K, TILES, VT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid(j.V / (TILES * VT), j.nchains * j.G);
+  const dim3 grid = job_grid(j, j.V / (TILES * VT));
   e = launch_kernel(kern, grid, 32 * C::WARPS, C::SMEM, stream, j.pdl != 0, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

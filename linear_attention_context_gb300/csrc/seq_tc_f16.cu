@@ -289,7 +289,8 @@ __global__ void __launch_bounds__(32 * h16::WARPS, 1) seq_tc_f16_kernel(const __
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const SeqJob& j = p.job;
-  const int u = blockIdx.y;
+  int u, tile;
+  if (!unit_and_tile(j, u, tile)) return;
   const int chain = u / j.G;
   const int g = u - chain * j.G;
   int64_t cbase;  // the chain's first segment in the packed arrays
@@ -299,7 +300,7 @@ __global__ void __launch_bounds__(32 * h16::WARPS, 1) seq_tc_f16_kernel(const __
   const int s_lo = g * j.L;
   const int n = min(j.L, S - s_lo);
   const int nsteps = n - 1 + (j.fin ? 1 : 0);
-  const int vbase = blockIdx.x * VT;
+  const int vbase = tile * VT;
   if (n <= 0) {  // a sequence without segments: its final state is its initial state
     if (j.fin) {
       float* F = j.fin + u * j.fin_unit_stride;
@@ -315,7 +316,7 @@ __global__ void __launch_bounds__(32 * h16::WARPS, 1) seq_tc_f16_kernel(const __
   const bool fwd = j.direction == 0;
   auto seg_of = [&](int step) { return fwd ? s_lo + step : s_lo + n - 1 - step; };
 #ifdef QLA_TRACE
-  const bool tr = blockIdx.x == 0 && blockIdx.y == 0 && lane == 0 &&
+  const bool tr = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && lane == 0 &&
                   (warp <= NI || warp == SPL_WARP0 || warp == SPL_WARP0 + 4 || warp == EPI_WARP0 || warp == WARPS - 1);
   const int trc = warp == WARPS - 1 ? 1 : 0;
   (void)trc;
@@ -765,7 +766,7 @@ cudaError_t launch_seq_tc_f16(const SeqJob& j, int release, unsigned int* status
   if (!make_job_maps(j, VT, EC, &p.map_h, &p.map_out, &p.map_m)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(seq_tc_f16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid(j.V / VT, j.nchains * j.G);
+  const dim3 grid = job_grid(j, j.V / VT);
   e = launch_kernel(seq_tc_f16_kernel, grid, 32 * WARPS, SMEM, stream, j.pdl != 0, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

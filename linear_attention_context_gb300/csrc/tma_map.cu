@@ -44,7 +44,10 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 }
 
 bool tma_job_supported(const SeqJob& j) {
-  if ((int64_t)j.nchains * j.G > 65535) return false;
+  if (job_grid(j, j.V / 32).x == 0) return false;  // one CTA per 32-column tile of each unit
+  // Tensor-map row coordinates are 32-bit: every state's rows must be addressable.
+  const int64_t states = j.cu_seg ? j.nstates : (int64_t)j.nchains * j.S;
+  if (states * (int64_t)(j.K > j.V ? j.K : j.V) > 0x7fffffff) return false;
   // The tensor maps view H/out and M as 2-D arrays of all chains' states, so
   // chains must be packed back to back (H and out are absent in scan phase
   // 1a; variable-length jobs locate every chain and group through the

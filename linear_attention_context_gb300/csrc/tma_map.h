@@ -14,9 +14,11 @@ namespace qla {
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows,
               int swizzle);
 
-// Whether a tensor-core launch can take the job: at most 65535 units, and
-// chains packed back to back (the maps view all chains' states as one 2-D
-// array) unless the job locates them through variable-length offsets.
+// Whether a tensor-core launch can take the job: its units fit the grid (at
+// most 2^31 - 1, see job_grid), every state row has a 32-bit
+// tensor-map coordinate, and chains are packed back to back (the maps view
+// all chains' states as one 2-D array) unless the job locates them through
+// variable-length offsets.
 bool tma_job_supported(const SeqJob& j);
 
 // The three maps of a tensor-core launch with VT-column CTA tiles and

@@ -19,12 +19,16 @@ def state_errors(got, ref):
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
-    d = got - ref
-    ax = (-2, -1)
-    num = np.sqrt((d * d).sum(axis=ax))
-    den = np.sqrt((ref * ref).sum(axis=ax))
-    mref = np.abs(ref).max(axis=ax)
-    mabs = np.abs(d).max(axis=ax)
+    lead = got.shape[:-2]
+    # one row per state, so every reduction runs along contiguous memory
+    g = got.reshape(-1, got.shape[-2] * got.shape[-1])
+    r = ref.reshape(g.shape)
+    d = g - r
+    num = np.sqrt(np.einsum("ij,ij->i", d, d)).reshape(lead)
+    den = np.sqrt(np.einsum("ij,ij->i", r, r)).reshape(lead)
+    # max |x| as max(max x, -min x): no second large temporary
+    mref = np.maximum(r.max(axis=1), -r.min(axis=1)).reshape(lead)
+    mabs = np.maximum(d.max(axis=1), -d.min(axis=1)).reshape(lead)
     with np.errstate(divide="ignore", invalid="ignore"):
         rel = np.where(den > 0, num / np.where(den > 0, den, 1), np.where(num > 0, np.inf, 0.0))
         rmax = np.where(mref > 0, mabs / np.where(mref > 0, mref, 1), np.where(mabs > 0, np.inf, 0.0))

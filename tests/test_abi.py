@@ -70,6 +70,8 @@ def call(L, H=FAKE, M=FAKE + (1 << 32), h0=None, out=FAKE + (2 << 32), fin=None,
     (dict(layout=2), -1), (dict(direction=-1), -1),
     (dict(variant=3), -1), (dict(engine=9), -1), (dict(engine=4), -1), (dict(release=7), -1), (dict(group=-1), -1),
     (dict(K=48), -2), (dict(V=288), -2), (dict(K=16), -2), (dict(V=100), -2),
+    # one CTA per (chain, segment group, 32-column tile) must fit a 2^31 - 1 grid
+    (dict(B=1 << 16, heads=1 << 10, S=16), -2),
     (dict(H=FAKE + 4), -3), (dict(M=FAKE + (1 << 32) + 8), -3), (dict(out=FAKE + (2 << 32) + 12), -3),
     (dict(h0=FAKE + (3 << 32) + 2), -3), (dict(fin=FAKE + (4 << 32) + 1), -3),
     # overlaps: out partially over H; M over H; h_init inside M; final over out
@@ -97,6 +99,13 @@ def test_out_equal_to_H_passes_the_checks(L):
 def test_valid_call_without_gpu_reports_cuda_error(L):
     assert call(L) == -5
     assert "cuda" in L.qla_last_error().decode().lower()
+
+
+@no_gpu_only
+def test_more_chains_than_a_grid_y_dimension_pass_the_checks(L):
+    # 70,000 chains: the grid is one-dimensional, so only its 2^31 - 1 CTAs bound them
+    assert call(L, B=70, heads=1000, S=1) == -5
+    assert call_varlen(L, N=70000, heads=1) == -5
 
 
 @no_gpu_only
@@ -131,7 +140,7 @@ def call_varlen(L, H=FAKE, M=FAKE + (1 << 32), h0=None, out=FAKE + (2 << 32), fi
 @pytest.mark.parametrize("kw,status", [
     (dict(cu=None), -1), (dict(H=None), -1), (dict(M=None), -1), (dict(out=None), -1),
     (dict(N=0), -1), (dict(T=-1), -1), (dict(heads=0), -1), (dict(layout=3), -1), (dict(direction=2), -1),
-    (dict(engine=4), -1), (dict(K=48), -2), (dict(V=300), -2), (dict(N=70000, heads=1), -2),
+    (dict(engine=4), -1), (dict(K=48), -2), (dict(V=300), -2), (dict(N=1 << 30, heads=2), -2),
     (dict(cu=FAKE + (5 << 32) + 2), -3), (dict(H=FAKE + 8), -3),
     (dict(cu=FAKE + 64), -4), (dict(out=FAKE + 4096), -4), (dict(h0=FAKE + (1 << 32) + 16), -4),
 ])

@@ -104,6 +104,20 @@ def test_edge_shapes(shape, layout, direction, engine):
     assert_parity(fin2, rfin, what="edge final only")
 
 
+def test_more_chains_than_a_grid_y_dimension_holds():
+    """70,000 chains (B = 70, heads = 1000): more units than the 65,535 a
+    grid's y dimension takes, on the sequential variant and on the scan
+    (140,000 units of two groups), through the one-dimensional grid."""
+    c = qi.Case(B=70, heads=1000, S=2, K=32, V=32, seed=91, m_kind="householder", h_scale=0.5,
+                init_kind="gaussian")
+    H, M, h0 = qi.make_inputs(c, "kv")
+    ref, rfin = oracle.cp_correct(H, M, h0, "kv", "fwd", want_final=True)
+    for variant in ("seq", "scan"):
+        got, fin = run(H, M, h0, "kv", "fwd", variant=variant, final=True)
+        assert_parity(got, ref, what=f"70000 chains {variant}")
+        assert_parity(fin, rfin, what=f"70000 chains {variant} final")
+
+
 # Magnitudes far from 1: the fp16-pair engine scales its operands by powers of
 # two (fp16 alone holds 6e-8 .. 65504); the other engines compute in fp32.
 RANGES = [
