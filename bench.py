@@ -677,7 +677,8 @@ def run_configs(args):
             def body():
                 for _ in range(16):
                     for Hd, Md, h0d, out in sets:
-                        qla.cp_correct(Hd, Md, h0d, out, layout=layout, direction=direction, stream=stream)
+                        qla.cp_correct(Hd, Md, h0d, out, layout=layout, direction=direction, stream=stream,
+                                       engine=args.engine)
             with torch.cuda.stream(stream):
                 body()
                 g = torch.cuda.CUDAGraph()
@@ -700,7 +701,8 @@ def run_configs(args):
         b = algorithmic_bytes(c.B * c.heads, c.S, c.K, c.V, with_init=c.init_kind != "none")
         line = {"config": name, "B": c.B, "heads": c.heads, "K": c.K, "V": c.V, "S": c.S,
                 "us_per_call": {k: round(v, 3) for k, v in times.items()}, "mean_us": round(us, 3),
-                "engine": qla.resolve(c.B, c.heads, c.S, c.K, c.V)[1], "algorithmic_bytes": b,
+                "engine": args.engine if args.engine != "auto" else qla.resolve(c.B, c.heads, c.S, c.K, c.V)[1],
+                "algorithmic_bytes": b,
                 "hbm_gbs": round(b / (us * 1e-6) / 1e9, 1)}
         line["hbm_frac"] = round(b / (us * 1e-6) / 1e9 / peak, 4)
         line["peak"] = f"{peak} GB/s ({peak_source})"

@@ -13,10 +13,14 @@
 // propagation matrix through shared memory in 32-wide k chunks of A (A = M
 // going forward, M^T in reverse), keeps the state tile in shared memory, and
 // each of its 256 threads accumulates R x 4 outputs (R = K / 32 rows spaced 32
-// apart, 4 adjacent columns) in registers.  The chunks go through a two-stage
-// ring filled with cp.async one chunk ahead, across step boundaries too (M
-// does not depend on the state), so a chunk's global latency overlaps the
-// previous chunk's arithmetic.
+// apart, 4 adjacent columns) in registers.  The chunks go through a ring of
+// NST stages filled with cp.async NST - 1 chunks ahead, across step boundaries
+// too (M does not depend on the state), so a chunk's global latency overlaps
+// the arithmetic of the chunks before it.  NST is 8 for K <= 64, where a step
+// has only one or two chunks and their latency dominates (config of 1 head,
+// K = V = 64, S = 4: 8.92 -> 8.56 us per call), and 2 above: at K = 128 with
+// 32 heads five stages measured up to 9 % slower (the larger shared-memory
+// carve-out leaves less L1 to the 4-byte cp.async copies and the H loads).
 //
 // In-place (out == H): a thread reads its H_seg elements before it writes
 // out[seg] over the same addresses, and no other thread touches them.
@@ -52,14 +56,22 @@ __host__ __device__ constexpr int stage_floats() {
   return K * 33 > 32 * (K + 1) ? K * 33 : 32 * (K + 1);
 }
 
+// Ring stages for K (75 KB of shared memory at most, with the state tile).
+template <int K>
+__host__ __device__ constexpr int ring_stages() {
+  return K <= 64 ? 8 : 2;
+}
+
 template <int R, int LAYOUT>
 __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
   constexpr int K = R * 32;
   constexpr int CH = K / 32;  // chunks per step
   constexpr int SF = stage_floats<K>();
+  constexpr int NST = ring_stages<K>();  // ring stages
+  constexpr int D = NST - 1;             // chunks in flight ahead of the one in use
   extern __shared__ __align__(16) float smem[];
   float* Xs = smem;                 // [K][kXsLd]    state tile, kv view
-  float* As = smem + K * kXsLd;     // [2][SF]       chunk ring
+  float* As = smem + K * kXsLd;     // [NST][SF]     chunk ring
 
   const int t = threadIdx.x;
   // kv: 8 column groups across a warp, so float4 global accesses along v coalesce.
@@ -104,13 +116,13 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
   const int nsteps = n - 1 + (j.fin ? 1 : 0);
   const int total = nsteps > 0 ? nsteps * CH : 0;  // chunks over all steps
   auto seg_of = [&](int jj) { return fwd ? s_lo + jj : s_lo + n - 1 - jj; };
-  // Chunk c (step c / CH, k block c % CH) -> stage c & 1, one 4-byte cp.async
+  // Chunk c (step c / CH, k block c % CH) -> stage c % NST, one 4-byte cp.async
   // per element: forward A[m][kc + kk] = M[m][kc + kk], reverse A[m][kc + kk] =
   // M[kc + kk][m]; consecutive threads read consecutive global floats.
   auto issue_chunk = [&](int c) {
     const float* Ms = Mc + (int64_t)seg_of(c / CH) * K * K;
     const int kc = (c % CH) * 32;
-    float* dst = As + (c & 1) * SF;
+    float* dst = As + (c % NST) * SF;
     for (int e = t; e < 32 * K; e += kThreads) {
       if (fwd) {
         const int m = e >> 5, kk = e & 31;
@@ -121,8 +133,12 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
       }
     }
   };
-  if (total > 0) issue_chunk(0);
-  cp_async_commit();
+  // One commit group per chunk, empty past the last: D groups ahead of the loop.
+#pragma unroll
+  for (int c = 0; c < D; ++c) {
+    if (c < total) issue_chunk(c);
+    cp_async_commit();
+  }
 
   for (int jj = 0; jj < n; ++jj) {
     const int seg = seg_of(jj);
@@ -175,12 +191,12 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
 
     for (int kb = 0; kb < CH; ++kb) {
       const int c = jj * CH + kb;
-      __syncthreads();  // every thread is done with chunk c - 1, whose stage chunk c + 1 reuses; Xs written
-      if (c + 1 < total) issue_chunk(c + 1);
+      __syncthreads();  // every thread is done with chunk c - 1, whose stage chunk c + D reuses; Xs written
+      if (c + D < total) issue_chunk(c + D);
       cp_async_commit();
-      cp_async_wait<1>();  // this thread's copies of chunk c have landed
+      cp_async_wait<D>();  // this thread's copies of chunk c have landed
       __syncthreads();     // everyone's have
-      const float* A = As + (c & 1) * SF;
+      const float* A = As + (c % NST) * SF;
       const int kc = kb * 32;
 #pragma unroll 8
       for (int kk = 0; kk < 32; ++kk) {
@@ -217,7 +233,7 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
 template <int R, int LAYOUT>
 cudaError_t launch_one(const SeqJob& j, cudaStream_t stream) {
   constexpr int K = R * 32;
-  const size_t smem = sizeof(float) * ((size_t)K * kXsLd + 2 * (size_t)stage_floats<K>());
+  const size_t smem = sizeof(float) * ((size_t)K * kXsLd + (size_t)ring_stages<K>() * stage_floats<K>());
   auto kern = seq_simt_kernel<R, LAYOUT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
