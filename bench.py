@@ -479,9 +479,16 @@ def cpu_baseline(probs, budget_s=20.0):
         oracle.cp_correct(q["H"][:, :heads], q["M"][:, :heads], q["h0"][:, :heads], q["layout"], q["direction"])
     el = time.perf_counter() - t
     us_per_call = el / len(probs) * (HEADS / heads) * 1e6
+    # the same oracle on one thread: two heads of each call, scaled to a full call
+    t = time.perf_counter()
+    for q in probs:
+        oracle.cp_correct(q["H"][:, :2], q["M"][:, :2], q["h0"][:, :2], q["layout"], q["direction"], nthreads=1)
+    one = (time.perf_counter() - t) / len(probs) * (HEADS / 2) * 1e6
     return {"value": round(us_per_call, 1), "unit": "us", "cores": threads, "kind": "oracle",
             "sample": f"{len(probs)} calls x {heads} of {HEADS} heads (fp64 oracle, {threads} threads), "
-                      f"scaled to a full call"}
+                      f"scaled to a full call",
+            "single_thread": {"value": round(one, 1), "unit": "us",
+                              "sample": f"{len(probs)} calls x 2 of {HEADS} heads on one thread, scaled"}}
 
 
 def run_reference(args):
