@@ -12,9 +12,11 @@
 // group) for all of that unit's segments.  Per step it streams the
 // propagation matrix through shared memory in 32-wide k chunks of A (A = M
 // going forward, M^T in reverse), keeps the state tile in shared memory, and
-// each of its 256 threads accumulates R x 4 outputs (R = K / 32 rows spaced 32
-// apart, 4 adjacent columns) in registers.  The chunks go through a ring of
-// NST stages filled with cp.async NST - 1 chunks ahead, across step boundaries
+// each of its 256 threads accumulates R x 4 outputs (R = K / 32 consecutive
+// rows, 4 adjacent columns) in registers; the chunk is stored k-major, so per
+// k a thread reads its R values of A and its 4 of the state with vector loads.
+// The chunks go through a ring of NST stages filled with cp.async NST - 1
+// chunks ahead, across step boundaries
 // too (M does not depend on the state), so a chunk's global latency overlaps
 // the arithmetic of the chunks before it.  NST is 8 for K <= 64, where a step
 // has only one or two chunks and their latency dominates (config of 1 head,
@@ -33,10 +35,6 @@ constexpr int kThreads = 256;
 constexpr int kTileV = 32;
 constexpr int kXsLd = kTileV + 4;  // padded row of the state tile (bank spread, keeps float4 alignment)
 
-__device__ __forceinline__ int64_t state_index(int layout, int K, int V, int k, int v) {
-  return layout == 0 ? (int64_t)k * V + v : (int64_t)v * K + k;
-}
-
 __device__ __forceinline__ void cp_async4(float* dst, const float* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
                "l"(src)
@@ -48,12 +46,53 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Floats of one chunk stage: forward [K rows m][33] (row m of A, 32 k + pad),
-// reverse [32 rows k][K + 1] (row k of M = column of A, + pad).  Both pads keep
-// the compute's shared loads free of bank conflicts.
+// One chunk stage holds A[m][kc + kk] k-major, as [32 rows kk][K + 4]: the
+// forward copy transposes M's rows on the way in (element-wise cp.async), the
+// reverse one keeps M's rows.  A thread's R consecutive rows m of one kk are
+// then adjacent, so the compute reads them with vector loads; the 4-float pad
+// keeps those loads 16-byte aligned.
+template <int K>
+__host__ __device__ constexpr int stage_ld() {
+  return K + 4;
+}
 template <int K>
 __host__ __device__ constexpr int stage_floats() {
-  return K * 33 > 32 * (K + 1) ? K * 33 : 32 * (K + 1);
+  return 32 * stage_ld<K>();
+}
+
+// R consecutive floats from / to p (aligned to 4 R bytes): float4 pieces when
+// R is a multiple of 4, float2 when even, scalars otherwise.
+template <int R>
+__device__ __forceinline__ void load_run(const float* p, float (&a)[R]) {
+  if constexpr (R % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < R; i += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(p + i);
+      a[i] = v.x; a[i + 1] = v.y; a[i + 2] = v.z; a[i + 3] = v.w;
+    }
+  } else if constexpr (R % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < R; i += 2) {
+      const float2 v = *reinterpret_cast<const float2*>(p + i);
+      a[i] = v.x; a[i + 1] = v.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < R; ++i) a[i] = p[i];
+  }
+}
+template <int R>
+__device__ __forceinline__ void store_run(float* p, const float (&a)[R]) {
+  if constexpr (R % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < R; i += 4) *reinterpret_cast<float4*>(p + i) = make_float4(a[i], a[i + 1], a[i + 2], a[i + 3]);
+  } else if constexpr (R % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < R; i += 2) *reinterpret_cast<float2*>(p + i) = make_float2(a[i], a[i + 1]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < R; ++i) p[i] = a[i];
+  }
 }
 
 // Ring stages for K (75 KB of shared memory at most, with the state tile).
@@ -66,6 +105,7 @@ template <int R, int LAYOUT>
 __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
   constexpr int K = R * 32;
   constexpr int CH = K / 32;  // chunks per step
+  constexpr int SL = stage_ld<K>();
   constexpr int SF = stage_floats<K>();
   constexpr int NST = ring_stages<K>();  // ring stages
   constexpr int D = NST - 1;             // chunks in flight ahead of the one in use
@@ -73,11 +113,13 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
   float* Xs = smem;                 // [K][kXsLd]    state tile, kv view
   float* As = smem + K * kXsLd;     // [NST][SF]     chunk ring
 
+  // Thread t owns rows R rg .. R rg + R - 1 and columns 4 cg .. 4 cg + 3 of
+  // the 32-column tile: 8 column groups across a warp, so kv global accesses
+  // are float4 runs along v; vk ones are runs of R along k.
   const int t = threadIdx.x;
-  // kv: 8 column groups across a warp, so float4 global accesses along v coalesce.
-  // vk: 32 consecutive rows across a warp, so scalar global accesses along k coalesce.
-  const int cg = LAYOUT == 0 ? (t & 7) : (t >> 5);
-  const int rg = LAYOUT == 0 ? (t >> 3) : (t & 31);
+  const int cg = t & 7;
+  const int rg = t >> 3;
+  const int k0 = R * rg;
   const int V = j.V;
   int u, tile;
   if (!unit_and_tile(j, u, tile)) return;
@@ -98,38 +140,71 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
   float* Oc = j.out ? j.out + cbase * st : nullptr;
   const float* Mc = j.M + cbase * K * K;
 
-  float x[R][4];
+  // This thread's R x 4 block of a state (k-major in registers) from / to a
+  // [K][V] (kv) or [V][K] (vk) array.
+  auto load_block = [&](const float* src, float (&b)[R][4]) {
+    if (LAYOUT == 0) {
 #pragma unroll
-  for (int q = 0; q < R; ++q) {
-    const int k = rg + 32 * q;
+      for (int q = 0; q < R; ++q) {
+        const float4 v = *reinterpret_cast<const float4*>(src + (int64_t)(k0 + q) * V + v0);
+        b[q][0] = v.x; b[q][1] = v.y; b[q][2] = v.z; b[q][3] = v.w;
+      }
+    } else {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float val = 0.f;
-      if (j.init_mode == kInitPointer)
-        val = j.init[u * j.init_unit_stride + state_index(LAYOUT, K, V, k, v0 + e)];
-      else if (j.init_mode == kInitIdentity)
-        val = (k == v0 + e) ? 1.f : 0.f;
-      x[q][e] = val;
+      for (int e = 0; e < 4; ++e) {
+        float r[R];
+        load_run<R>(src + (int64_t)(v0 + e) * K + k0, r);
+#pragma unroll
+        for (int q = 0; q < R; ++q) b[q][e] = r[q];
+      }
     }
+  };
+  auto store_block = [&](float* dst, const float (&b)[R][4]) {
+    if (LAYOUT == 0) {
+#pragma unroll
+      for (int q = 0; q < R; ++q)
+        *reinterpret_cast<float4*>(dst + (int64_t)(k0 + q) * V + v0) = make_float4(b[q][0], b[q][1], b[q][2], b[q][3]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float r[R];
+#pragma unroll
+        for (int q = 0; q < R; ++q) r[q] = b[q][e];
+        store_run<R>(dst + (int64_t)(v0 + e) * K + k0, r);
+      }
+    }
+  };
+
+  float x[R][4];
+  if (j.init_mode == kInitPointer) {
+    load_block(j.init + u * j.init_unit_stride, x);
+  } else {
+#pragma unroll
+    for (int q = 0; q < R; ++q)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[q][e] = (j.init_mode == kInitIdentity && k0 + q == v0 + e) ? 1.f : 0.f;
   }
 
   const int nsteps = n - 1 + (j.fin ? 1 : 0);
   const int total = nsteps > 0 ? nsteps * CH : 0;  // chunks over all steps
   auto seg_of = [&](int jj) { return fwd ? s_lo + jj : s_lo + n - 1 - jj; };
-  // Chunk c (step c / CH, k block c % CH) -> stage c % NST, one 4-byte cp.async
-  // per element: forward A[m][kc + kk] = M[m][kc + kk], reverse A[m][kc + kk] =
-  // M[kc + kk][m]; consecutive threads read consecutive global floats.
+  // Chunk c (step c / CH, k block c % CH) -> stage c % NST as [kk][m], one
+  // 4-byte cp.async per element.  Reverse: A[m][kc + kk] = M[kc + kk][m], and
+  // consecutive threads take consecutive m.  Forward: A[m][kc + kk] =
+  // M[m][kc + kk], transposed on the way in; a warp takes 8 kk x 4 m, so it
+  // reads four 32-byte runs of M's rows and its shared writes, (K + 4) floats
+  // apart per kk, fall in 32 different banks.
   auto issue_chunk = [&](int c) {
     const float* Ms = Mc + (int64_t)seg_of(c / CH) * K * K;
     const int kc = (c % CH) * 32;
     float* dst = As + (c % NST) * SF;
     for (int e = t; e < 32 * K; e += kThreads) {
       if (fwd) {
-        const int m = e >> 5, kk = e & 31;
-        cp_async4(dst + m * 33 + kk, Ms + (int64_t)m * K + kc + kk);
+        const int kk = (e & 7) + 8 * ((e >> 5) & 3), m = ((e >> 3) & 3) + 4 * (e >> 7);
+        cp_async4(dst + kk * SL + m, Ms + (int64_t)m * K + kc + kk);
       } else {
         const int kk = e / K, m = e - kk * K;
-        cp_async4(dst + kk * (K + 1) + m, Ms + (int64_t)(kc + kk) * K + m);
+        cp_async4(dst + kk * SL + m, Ms + (int64_t)(kc + kk) * K + m);
       }
     }
   };
@@ -144,44 +219,21 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
     const int seg = seg_of(jj);
     const bool do_step = jj < nsteps;
     float h[R][4];
-#pragma unroll
-    for (int q = 0; q < R; ++q)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) h[q][e] = 0.f;
     if (do_step && Hc) {
-      const float* Hs = Hc + seg * st;
+      load_block(Hc + seg * st, h);
+    } else {
 #pragma unroll
-      for (int q = 0; q < R; ++q) {
-        const int k = rg + 32 * q;
-        if (LAYOUT == 0) {
-          const float4 hv = *reinterpret_cast<const float4*>(Hs + (int64_t)k * V + v0);
-          h[q][0] = hv.x; h[q][1] = hv.y; h[q][2] = hv.z; h[q][3] = hv.w;
-        } else {
+      for (int q = 0; q < R; ++q)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) h[q][e] = Hs[(int64_t)(v0 + e) * K + k];
-        }
-      }
+        for (int e = 0; e < 4; ++e) h[q][e] = 0.f;
     }
-    if (Oc) {
-      float* Os = Oc + seg * st;
-#pragma unroll
-      for (int q = 0; q < R; ++q) {
-        const int k = rg + 32 * q;
-        if (LAYOUT == 0) {
-          *reinterpret_cast<float4*>(Os + (int64_t)k * V + v0) = make_float4(x[q][0], x[q][1], x[q][2], x[q][3]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) Os[(int64_t)(v0 + e) * K + k] = x[q][e];
-        }
-      }
-    }
+    if (Oc) store_block(Oc + seg * st, x);
     if (!do_step) break;
 
     __syncthreads();  // the previous step's readers of Xs are done
 #pragma unroll
     for (int q = 0; q < R; ++q)
-      *reinterpret_cast<float4*>(Xs + (rg + 32 * q) * kXsLd + cg * 4) =
-          make_float4(x[q][0], x[q][1], x[q][2], x[q][3]);
+      *reinterpret_cast<float4*>(Xs + (k0 + q) * kXsLd + cg * 4) = make_float4(x[q][0], x[q][1], x[q][2], x[q][3]);
 
     float acc[R][4];
 #pragma unroll
@@ -196,18 +248,19 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
       cp_async_commit();
       cp_async_wait<D>();  // this thread's copies of chunk c have landed
       __syncthreads();     // everyone's have
-      const float* A = As + (c % NST) * SF;
+      const float* A = As + (c % NST) * SF + k0;
       const int kc = kb * 32;
 #pragma unroll 8
       for (int kk = 0; kk < 32; ++kk) {
         const float4 xv = *reinterpret_cast<const float4*>(Xs + (kc + kk) * kXsLd + cg * 4);
+        float a[R];
+        load_run<R>(A + kk * SL, a);  // A[k0 .. k0 + R - 1][kc + kk]
 #pragma unroll
         for (int q = 0; q < R; ++q) {
-          const float a = fwd ? A[(rg + 32 * q) * 33 + kk] : A[kk * (K + 1) + rg + 32 * q];
-          acc[q][0] = fmaf(a, xv.x, acc[q][0]);
-          acc[q][1] = fmaf(a, xv.y, acc[q][1]);
-          acc[q][2] = fmaf(a, xv.z, acc[q][2]);
-          acc[q][3] = fmaf(a, xv.w, acc[q][3]);
+          acc[q][0] = fmaf(a[q], xv.x, acc[q][0]);
+          acc[q][1] = fmaf(a[q], xv.y, acc[q][1]);
+          acc[q][2] = fmaf(a[q], xv.z, acc[q][2]);
+          acc[q][3] = fmaf(a[q], xv.w, acc[q][3]);
         }
       }
     }
@@ -219,15 +272,7 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
   cp_async_wait<0>();  // no copy may land after the CTA is gone
   griddep_launch_dependents();
 
-  if (j.fin) {
-    float* F = j.fin + u * j.fin_unit_stride;
-#pragma unroll
-    for (int q = 0; q < R; ++q) {
-      const int k = rg + 32 * q;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) F[state_index(LAYOUT, K, V, k, v0 + e)] = x[q][e];
-    }
-  }
+  if (j.fin) store_block(j.fin + u * j.fin_unit_stride, x);
 }
 
 template <int R, int LAYOUT>
