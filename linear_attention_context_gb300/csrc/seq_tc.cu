@@ -479,6 +479,38 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
     ctl->abort = 0;
     fence_mbar_init();
   }
+  // The first step's loads need no TMEM and no other thread: the producer
+  // thread issues them before the set-up barrier, so their DRAM latency runs
+  // under the TMEM allocation and the barrier.  These are the first uses of
+  // their slots (no empty wait); the producer loop continues after them.
+  int pre_m = 0;   // M chunks of step 0 already issued (ring stages 0 ..)
+  bool pre_h = false;
+  if (threadIdx.x == 0 && nsteps > 0) {
+    const int64_t mrow0 = (cbase + seg_of(0)) * K;
+    pre_m = C::CPS < C::NM ? C::CPS : C::NM;
+    for (int c = 0; c < pre_m; ++c) {
+      mbar_arrive_expect_tx(&ctl->m_full[c], kChunkBytes);
+      const int kc = c / C::HALVES, h = c % C::HALVES;
+      uint8_t* dst = smem + C::OFF_M + c * kChunkBytes;
+      if (fwd)
+        tma_load_2d(dst, &p.map_m, 32 * kc, (int32_t)(mrow0 + 128 * h), &ctl->m_full[c]);
+      else
+        tma_load_2d(dst, &p.map_m, 128 * h, (int32_t)(mrow0 + 32 * kc), &ctl->m_full[c]);
+    }
+    if (p.has_h) {
+      const int64_t hrow0 = (cbase + seg_of(0)) * (j.layout == 0 ? K : j.V);
+      for (int tl = 0; tl < TILES; ++tl) {
+        mbar_arrive_expect_tx(&ctl->h_full[tl][0], C::TILE);
+        uint8_t* dst = smem + C::OFF_H + (tl * 2) * C::TILE;
+        const int v0 = vbase + tl * VT;
+        if (j.layout == 0)
+          tma_load_2d(dst, &p.map_h, v0, (int32_t)hrow0, &ctl->h_full[tl][0]);
+        else
+          tma_load_2d(dst, &p.map_h, 0, (int32_t)(hrow0 + v0), &ctl->h_full[tl][0]);
+      }
+      pre_h = true;
+    }
+  }
   if (warp == 1) {
     tmem_alloc(&ctl->tmem_base, kTmemCols);
     tmem_relinquish();
@@ -493,8 +525,10 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t mit = 0;
+      uint32_t mit = (uint32_t)pre_m;
       int hissued[TILES] = {};
+      if (pre_h)
+        for (int tl = 0; tl < TILES; ++tl) hissued[tl] = 1;
       bool ok = true;
       const int hrows = j.layout == 0 ? K : j.V;  // rows of one state in the 2-D view of H
       for (int step = 0; step < nsteps && ok; ++step) {
@@ -518,7 +552,7 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
           QLA_TR(0, step, 0, 0);
         };
         auto load_m = [&]() {
-          for (int c = 0; c < C::CPS && ok; ++c, ++mit) {
+          for (int c = step == 0 ? pre_m : 0; c < C::CPS && ok; ++c, ++mit) {
             const int stage = mit % C::NM;
             if (!(ok = mbar_wait(&ctl->m_empty[stage], ((mit / C::NM) & 1) ^ 1, wc))) break;
             QLA_TR(0, step, 1, c);
@@ -536,7 +570,7 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
         // slots, so their H tile goes first.
         if (step == 0) {
           load_m();
-          if (ok) load_h();
+          if (ok && !pre_h) load_h();
         } else {
           load_h();
           if (ok) load_m();
@@ -739,8 +773,8 @@ __global__ void __launch_bounds__(32 * Cfg<K, TILES, VT>::WARPS, 1) seq_tc_kerne
     auto drain_add = [&](int h, float (&acc)[EC]) {
       float a[EC], b[EC];
       const uint32_t base = tmem + lane_off + (uint32_t)((tl * C::HALVES + h) * C::NQ * VT + c0);
-#pragma unroll
       static_assert(C::NQ % 2 == 0, "chains are drained in pairs");
+#pragma unroll
       for (int q = 0; q < C::NQ; q += 2) {
         tmem_ld<EC>(base + q * VT, a);
         tmem_ld<EC>(base + (q + 1) * VT, b);
