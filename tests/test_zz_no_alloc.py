@@ -5,10 +5,11 @@ runs with a fixed device-memory budget handed out at start-up, and
 latency-bound code that cannot afford the device synchronisation cudaMalloc
 can cause.  It keeps the scan's scratch in a fixed array inside the library.
 
-These tests call it through the C ABI and compare it with the allocating scan
-(qla_cp_correct_ex with QLA_VARIANT_SCAN) within the parity tolerance the other
-GPU tests use, on two calls in a row that share the array, and check that a
-shape needing more scratch than the array holds is refused before anything
+These tests call it through the C ABI and compare it with the fp64 oracle and
+with the allocating scan (qla_cp_correct_ex with QLA_VARIANT_SCAN) within the
+parity tolerance the other GPU tests use, on two calls in a row that share the
+array; they cover a single segment (no scan phases) and check that a shape
+needing more scratch than the array holds is refused before anything
 launches.  The file is named so that pytest collects it last.
 """
 import ctypes
@@ -17,6 +18,7 @@ import numpy as np
 import pytest
 
 import linear_attention_context_gb300 as qla
+import oracle
 import qla_inputs as qi
 from qla_check import assert_parity
 
@@ -56,7 +58,11 @@ def _call_alloc_scan(Hd, Md, h0d, out, fin, c, layout, direction, group=0):
         DIR[direction], 2, 0, 0, group, _stream())
 
 
-def test_static_scan_matches_allocating_scan_on_two_calls():
+def _host(t):
+    return t.cpu().numpy().astype(np.float64)
+
+
+def test_static_scan_matches_oracle_and_allocating_scan_on_two_calls():
     import torch
     cases = [(qi.sweep_case(heads=4, S=32), "kv", "fwd"), (qi.sweep_case(heads=4, S=32).with_(seed=9), "vk", "rev")]
     for c, _, _ in cases:
@@ -75,13 +81,35 @@ def test_static_scan_matches_allocating_scan_on_two_calls():
         static_out.append((out, fin))
     torch.cuda.synchronize()
     for (c, layout, direction, Hd, Md, h0d, fin_shape), (out, fin) in zip(prepared, static_out):
-        ref = torch.empty_like(Hd)
-        rfin = torch.empty(fin_shape, device=Hd.device)
-        rc = _call_alloc_scan(Hd, Md, h0d, ref, rfin, c, layout, direction)
+        H, M, h0 = qi.make_inputs(c, layout)
+        ref, rfin = oracle.cp_correct(H, M, h0, layout, direction, want_final=True)
+        assert_parity(_host(out), ref, what=f"static scan vs oracle {layout} {direction}")
+        assert_parity(_host(fin), rfin, what=f"static scan final vs oracle {layout} {direction}")
+        aref = torch.empty_like(Hd)
+        afin = torch.empty(fin_shape, device=Hd.device)
+        rc = _call_alloc_scan(Hd, Md, h0d, aref, afin, c, layout, direction)
         assert rc == 0, qla.last_error()
         torch.cuda.synchronize()
-        assert_parity(out.cpu().numpy(), ref.cpu().numpy(), what=f"static scan {layout} {direction}")
-        assert_parity(fin.cpu().numpy(), rfin.cpu().numpy(), what=f"static scan final {layout} {direction}")
+        assert_parity(_host(out), _host(aref), what=f"static scan vs allocating scan {layout} {direction}")
+        assert_parity(_host(fin), _host(afin), what=f"static scan final vs allocating scan {layout} {direction}")
+
+
+def test_static_entry_with_one_segment():
+    """S = 1 has no scan phases: out[0] is h_init and the final state one step."""
+    import torch
+    c = qi.sweep_case(heads=4, S=1)
+    for layout, direction in (("kv", "fwd"), ("vk", "rev")):
+        Hd, Md, h0d, fin_shape = _device_case(c, layout)
+        H, M, h0 = qi.make_inputs(c, layout)
+        ref, rfin = oracle.cp_correct(H, M, h0, layout, direction, want_final=True)
+        for _ in range(2):
+            out = torch.full_like(Hd, float("nan"))
+            fin = torch.full(fin_shape, float("nan"), device=Hd.device)
+            rc = _call_static(Hd, Md, h0d, out, fin, c, layout, direction)
+            assert rc == 0, qla.last_error()
+            torch.cuda.synchronize()
+            assert_parity(_host(out), ref, what=f"static S=1 {layout} {direction}")
+            assert_parity(_host(fin), rfin, what=f"static S=1 final {layout} {direction}")
 
 
 def test_static_scan_refuses_shapes_beyond_its_scratch():
