@@ -89,19 +89,23 @@ enum {
 
 /* Which kernel engine runs the sequential pass. */
 enum {
-  QLA_ENGINE_AUTO = 0,    /* tensor-core engine where the shape allows, else SIMT */
+  QLA_ENGINE_AUTO = 0,    /* 3xTF32 engine where the shape and chain length allow, else SIMT */
   QLA_ENGINE_SIMT = 1,    /* plain FFMA kernel, no TMA: any supported K, V */
   QLA_ENGINE_TC_F16 = 2,  /* the same pipeline with tcgen05 kind::f16 MMAs on power-of-two-scaled
                              fp16 hi/lo operand pairs (22 significant bits, as 3xTF32): K = 128 only */
   QLA_ENGINE_TC = 3       /* warp-specialised TMA/mbarrier pipeline, tcgen05 3xTF32 propagate */
 };
-/* Accuracy on long chains: the tensor core accumulates in fp32 rounding toward
- * zero, so with norm-preserving M (no decay) the two tensor-core engines lose
- * about 4e-8 of the state's norm per step, coherently: worst per-state relative
- * L2 error 6.4e-6 at 128 steps, 1.3e-5 at 256 and 2.6e-5 at 512 (K = V = 128).
- * The SIMT engine rounds to nearest and stays near 3e-6 at 512 steps.  Decaying
- * M damps the drift; for chains of a few hundred undecayed steps that need
- * 1e-5, ask for QLA_ENGINE_SIMT. */
+/* Accuracy on long chains and the automatic engine choice.  The tensor core
+ * accumulates in fp32 rounding toward zero, so with norm-preserving M (no
+ * decay) the two tensor-core engines shrink the state coherently, about 4.4e-8
+ * of its norm per step at K = 128 and 1.4e-7 at K = 256: the worst per-state
+ * relative L2 error passes 1e-5 near 200 steps (K = 128) and 64 steps
+ * (K = 256).  QLA_ENGINE_AUTO therefore takes the 3xTF32 engine only for
+ * chains of at most 160 segments (K = 128) or 48 segments (K = 256) and the
+ * FFMA engine, which rounds to nearest (about 3e-6 at 512 steps), for longer
+ * ones, in both variants; with variable lengths the bound is max_segments (T
+ * for the sequential variant).  An engine asked for explicitly is used as
+ * asked, whatever the chain length. */
 
 /* How a consumer releases a double-buffer slot it has read with ordinary
  * shared-memory loads, before the TMA producer may overwrite it (section
@@ -171,7 +175,8 @@ QLA_API int qla_cp_correct_varlen(const float* H, const float* M, const float* h
  * qla_cp_correct_varlen with a variant choice.  The scan variant needs the
  * groups' size on the host without reading the device offsets, so the caller
  * passes `max_segments`, an upper bound on every sequence's segment count
- * (1 .. T; 0 means T; ignored by the sequential variant).  Every chain is cut
+ * (1 .. T; 0 means T; the sequential variant uses it only for the automatic
+ * engine choice).  Every chain is cut
  * into G groups of L consecutive segments, G = scan_group (0: automatic from
  * max_segments) and L = ceil(max_segments / G); groups past a sequence's end
  * are empty (their aggregates are the identity and zero).  A sequence longer

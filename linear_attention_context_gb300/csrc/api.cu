@@ -206,8 +206,20 @@ bool known_engine(int engine) {
          engine == QLA_ENGINE_TC_F16;
 }
 
+// Longest chain the automatic choice gives to the tensor-core engine.  The
+// tensor core accumulates in fp32 rounding toward zero; with norm-preserving
+// M the states shrink coherently by about 4.4e-8 per step at K = 128 (four
+// accumulations per chain and step) and 1.4e-7 at K = 256 (sixteen), so the
+// worst per-state relative L2 error reaches 1e-5 near 200 and 64 steps
+// (measured on GB300: 8.0e-6 at S = 160, K = 128; 7.8e-6 at S = 48, K = 256).
+// Longer chains go to the FFMA engine, which rounds to nearest (3.3e-6 at
+// S = 512).  The scan regroups the same products and drifts the same way, so
+// the limit applies to the whole chain there too.
+int tc_auto_max_segments(int K) { return K <= 128 ? 160 : 48; }
+
 int resolve_engine(const Shape& s, int engine) {
-  if (engine == QLA_ENGINE_AUTO) return tc_supports(s.K, s.V) ? QLA_ENGINE_TC : QLA_ENGINE_SIMT;
+  if (engine == QLA_ENGINE_AUTO)
+    return (tc_supports(s.K, s.V) && s.S <= tc_auto_max_segments(s.K)) ? QLA_ENGINE_TC : QLA_ENGINE_SIMT;
   return engine;
 }
 

@@ -37,21 +37,42 @@ def test_workloads(name, layout, direction, engine):
     assert_parity(fin, rfin, what=f"{name} final")
 
 
-@pytest.mark.parametrize("engine", ["auto"] + [e for e in ENGINES if e != "simt"])
-@pytest.mark.parametrize("direction", DIRS)
-def test_large_workload_sampled(direction, engine):
-    """B=4, 64 heads, K=V=256, S=32 at full size on the GPU; the oracle checks
-    a sample of chains (first, last, and two in between)."""
+@pytest.fixture(scope="module")
+def large_inputs():
     c = qi.WORKLOADS["c3"]
-    skip_unsupported(engine, c.K, c.V)
     H, M, h0 = qi.make_inputs(c, "kv")
-    got, _ = run(H, M, h0, "kv", direction, engine=engine)
+    return c, H, M, h0
+
+
+def run_f32(H, M, h0, layout, direction, engine):
+    """As gpu_util.run, but keeps the result in fp32 (the large workload's
+    outputs are 2 GB in fp32)."""
+    import torch
+    import linear_attention_context_gb300 as qla
+    from gpu_util import to_dev
+    out = qla.cp_correct(to_dev(H), to_dev(M), to_dev(h0), layout=layout, direction=direction, engine=engine)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+@pytest.mark.parametrize("direction", DIRS)
+def test_large_workload_every_chain(large_inputs, direction):
+    """B=4, 64 heads, K=V=256, S=32 at full size: every one of the 256 chains
+    of every engine that takes K=256 (the automatic choice, 3xTF32 and FFMA)
+    against the oracle, state by state.  The oracle runs once per block of
+    chains and serves all engines."""
+    c, H, M, h0 = large_inputs
+    engines = [e for e in ("auto", "tc", "simt") if e == "auto" or (e in ENGINES and engine_supports(e, c.K, c.V))]
+    got = {e: run_f32(H, M, h0, "kv", direction, e) for e in engines}
     n = c.chains
-    for ch in sorted({0, n // 3, (2 * n) // 3, n - 1}):
-        b, h = divmod(ch, c.heads)
-        sl = (slice(b, b + 1), slice(h, h + 1))
-        ref, _ = oracle.cp_correct(H[sl], M[sl], h0[sl], "kv", direction)
-        assert_parity(got[sl], ref, what=f"c3 chain {ch} {direction} {engine}")
+    flat = lambda a: a.reshape((1, n) + a.shape[2:])  # noqa: E731  chains in (b, h) order
+    Hf, Mf, h0f = flat(H), flat(M), flat(h0)
+    step = 32
+    for c0 in range(0, n, step):
+        sl = (slice(None), slice(c0, min(n, c0 + step)))
+        ref, _ = oracle.cp_correct(Hf[sl], Mf[sl], h0f[sl], "kv", direction)
+        for e in engines:
+            assert_parity(flat(got[e])[sl], ref, what=f"c3 chains {c0}..{c0 + step - 1} {direction} {e}")
 
 
 @pytest.mark.parametrize("direction", DIRS)
@@ -317,3 +338,55 @@ def test_ffma_engine_on_a_very_long_chain():
     ref, _ = oracle.cp_correct(H, M, h0, "vk", "fwd")
     got, _ = run(H, M, h0, "vk", "fwd", engine="simt", variant="seq")
     assert_parity(got, ref, what="S=512 orthogonal simt")
+
+
+@pytest.mark.parametrize("layout,direction", [("kv", "fwd"), ("vk", "rev"), ("vk", "fwd"), ("kv", "rev")])
+def test_plain_entry_point_through_the_c_abi(layout, direction):
+    """qla_cp_correct, the entry point with the library's default choices,
+    called directly through ctypes on the 32-head workload (and in place)."""
+    import ctypes
+
+    import torch
+
+    import linear_attention_context_gb300 as qla
+    from gpu_util import to_dev
+    c = qi.WORKLOADS["c1" if direction == "fwd" else "c2"]
+    H, M, h0 = qi.make_inputs(c, layout)
+    ref, _ = oracle.cp_correct(H, M, h0, layout, direction)
+    Hd, Md, h0d = to_dev(H), to_dev(M), to_dev(h0)
+    out = torch.full_like(Hd, float("nan"))
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    lay, dirn = qla.LAYOUTS[layout], qla.DIRECTIONS[direction]
+    rc = qla.lib().qla_cp_correct(p(Hd), p(Md), p(h0d), p(out), c.B, c.heads, c.S, c.K, c.V, lay, dirn, stream)
+    assert rc == 0, qla.last_error()
+    torch.cuda.synchronize()
+    assert_parity(out.cpu().numpy().astype(np.float64), ref, what=f"qla_cp_correct {layout} {direction}")
+    # in place (out == H), and a NULL h_init meaning zeros
+    rc = qla.lib().qla_cp_correct(p(Hd), p(Md), None, p(Hd), c.B, c.heads, c.S, c.K, c.V, lay, dirn, stream)
+    assert rc == 0, qla.last_error()
+    torch.cuda.synchronize()
+    ref0, _ = oracle.cp_correct(H, M, None, layout, direction)
+    assert_parity(Hd.cpu().numpy().astype(np.float64), ref0, what=f"qla_cp_correct in place {layout} {direction}")
+
+
+@pytest.mark.parametrize("K,S", [(128, 160), (128, 256), (128, 512), (256, 48), (256, 64), (256, 128)])
+def test_automatic_choice_keeps_the_bar_on_long_undecayed_chains(K, S):
+    """Orthogonal M without decay is the worst case for the tensor core's
+    round-toward-zero accumulation (a coherent shrink every step).  The
+    automatic engine takes the 3xTF32 engine up to 160 segments at K = 128
+    and 48 at K = 256 and the FFMA engine beyond; either way the results stay
+    inside the bar, in both variants and both directions."""
+    import linear_attention_context_gb300 as qla
+    limit = 160 if K == 128 else 48
+    _, engine = qla.resolve(1, 2, S, K, 64, "kv")
+    assert engine == ("tc" if S <= limit else "simt")
+    c = qi.Case(B=1, heads=2, S=S, K=K, V=64, seed=11, m_kind="orthogonal", m_scale=1.0, h_scale=0.1,
+                init_kind="gaussian", init_scale=0.1)
+    H, M, h0 = qi.make_inputs(c, "kv")
+    for direction in DIRS:
+        ref, rfin = oracle.cp_correct(H, M, h0, "kv", direction, want_final=True)
+        for variant in ("auto", "seq", "scan"):
+            got, fin = run(H, M, h0, "kv", direction, engine="auto", variant=variant, final=True)
+            assert_parity(got, ref, what=f"auto engine K={K} S={S} {direction} {variant}")
+            assert_parity(fin, rfin, what=f"auto engine final K={K} S={S} {direction} {variant}")
