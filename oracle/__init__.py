@@ -1,9 +1,11 @@
-"""fp64 oracle for the CP state-correction pass -- TEST INFRASTRUCTURE ONLY.
+"""fp64 oracle for the CP state-correction pass and for the per-segment local
+pass that produces its inputs -- TEST INFRASTRUCTURE ONLY.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
 leg may import this package.  The library's CUDA path never calls it and shares
-no code with it.  The arithmetic lives in ``qla_oracle.c``; this module only
-marshals numpy arrays through ctypes.
+no code with it.  The arithmetic lives in ``qla_oracle.c`` (the correction) and
+``qla_local_oracle.c`` (the local pass); this module only marshals numpy arrays
+through ctypes.
 """
 from __future__ import annotations
 
@@ -31,6 +33,10 @@ def _lib(variant: str = ""):
         lib.qla_oracle_cp_correct.argtypes = [f32p, f32p, f32p, f64p, f64p, ctypes.c_int64,
                                               ci, ci, ci, ci, ci, ci]
         lib.qla_oracle_cp_correct.restype = ci
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        lib.qla_oracle_local_pass.argtypes = [u16p, u16p, f32p, f32p, f64p, f64p, ctypes.c_int64,
+                                              ci, ci, ci, ci, ci, ci]
+        lib.qla_oracle_local_pass.restype = ci
         _LIBS[variant] = lib
     return _LIBS[variant]
 
@@ -114,3 +120,32 @@ def cp_correct_varlen(H, M, h_init, cu_seg, layout="kv", direction="fwd"):
         out[:, s0:s1] = o[0]
         fin[n] = f[0]
     return out, fin
+
+
+def local_pass(k, v, beta, g, S, layout="kv", want_H=True, want_M=True, nthreads=0, variant=""):
+    """Per-segment local state H_i and propagation matrix M_i (gated delta
+    rule, token by token, fp64); see qla_local_oracle.c.
+
+    k: [B, heads, T, K] and v: [B, heads, T, V] bf16 bit patterns (uint16 or
+    int16 arrays); beta, g: [B, heads, T] float32; T = S * L.  Returns (H, M):
+    H [B, heads, S, K, V] (kv) or [B, heads, S, V, K] (vk), M [B, heads, S, K, K],
+    fp64 (None where not wanted)."""
+    k = np.ascontiguousarray(k).view(np.uint16)
+    v = np.ascontiguousarray(v).view(np.uint16)
+    beta = _f32(beta)
+    g = _f32(g)
+    B, heads, T, K = k.shape
+    V = v.shape[3]
+    assert v.shape[:3] == (B, heads, T) and beta.shape == (B, heads, T) and g.shape == (B, heads, T)
+    assert S >= 1 and T % S == 0, (T, S)
+    lay = {"kv": 0, "vk": 1}[layout]
+    st = (K, V) if layout == "kv" else (V, K)
+    H = np.empty((B, heads, S) + st, np.float64) if want_H else None
+    M = np.empty((B, heads, S, K, K), np.float64) if want_M else None
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    f32p = ctypes.POINTER(ctypes.c_float)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    p = lambda a, t: None if a is None else a.ctypes.data_as(t)  # noqa: E731
+    _lib(variant).qla_oracle_local_pass(p(k, u16p), p(v, u16p), p(beta, f32p), p(g, f32p), p(H, f64p),
+                                        p(M, f64p), B * heads, T, S, K, V, lay, nthreads)
+    return H, M

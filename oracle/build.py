@@ -9,10 +9,13 @@ def library_path(variant: str = ""):
     return os.path.join(HERE, "_lib", f"libqla_oracle{variant}.so")
 
 
+SOURCES = ("qla_oracle.c", "qla_local_oracle.c")
+
+
 def build_command(defines=(), variant: str = ""):
-    src = os.path.join(HERE, "qla_oracle.c")
+    srcs = [os.path.join(HERE, s) for s in SOURCES]
     return (["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off"]
-            + [f"-D{d}" for d in defines] + [src, "-o", library_path(variant)])
+            + [f"-D{d}" for d in defines] + srcs + ["-o", library_path(variant), "-lm"])
 
 
 def build(defines=(), variant: str = ""):

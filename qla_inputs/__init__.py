@@ -27,6 +27,10 @@ from . import build as _build
 TENSOR_H = 1
 TENSOR_M = 2
 TENSOR_INIT = 3
+TENSOR_KEY = 4
+TENSOR_VALUE = 5
+TENSOR_BETA = 6
+TENSOR_GATE = 7
 
 _LIB = None
 
@@ -45,8 +49,13 @@ def _lib():
         lib.qla_gen_orthogonal.argtypes = [f32p, i64, cint, u64, u64, i64, dbl]
         lib.qla_gen_signed_perm.argtypes = [f32p, i64, cint, u64, u64, i64]
         lib.qla_gen_small_int.argtypes = [f32p, i64, i64, u64, u64, i64, cint]
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        lib.qla_gen_unit_bf16.argtypes = [u16p, i64, cint, u64, u64, i64]
+        lib.qla_gen_gaussian_bf16.argtypes = [u16p, i64, i64, u64, u64, i64, dbl]
+        lib.qla_gen_uniform.argtypes = [f32p, i64, i64, u64, u64, i64, dbl, dbl, cint]
         for fn in ("qla_gen_gaussian", "qla_gen_householder", "qla_gen_orthogonal",
-                   "qla_gen_signed_perm", "qla_gen_small_int"):
+                   "qla_gen_signed_perm", "qla_gen_small_int", "qla_gen_unit_bf16",
+                   "qla_gen_gaussian_bf16", "qla_gen_uniform"):
             getattr(lib, fn).restype = None
         _LIB = lib
     return _LIB
@@ -225,3 +234,106 @@ def make_varlen_inputs(lengths, heads, K, V, seed, layout="kv", m_kind="househol
     M = M.reshape(heads, T, K, K)
     h0 = gaussian(N * heads, KV, seed, TENSOR_INIT, init_scale).reshape((N, heads) + st) if with_init else None
     return H, M, h0, cu
+
+
+# ---------------------------------------------------------------- local pass inputs
+#
+# Token-level inputs of the per-segment local pass (gated delta rule):
+#   k     [B][heads][T][K] bf16 (stored as int16 bit patterns): unit Gaussian directions
+#   v     [B][heads][T][V] bf16: N(0,1) * v_scale
+#   beta  [B][heads][T] fp32: U(beta_lo, beta_hi)
+#   g     [B][heads][T] fp32: log of U(alpha_lo, alpha_hi), a log-space decay
+# A k or v block is one token (chain * T + t); a beta or g block is one chain.
+
+def _u16_ptr(a: np.ndarray):
+    assert a.dtype == np.uint16 and a.flags.c_contiguous
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16))
+
+
+def unit_bf16(nblocks, dim, seed, tensor_id, block0=0):
+    out = np.empty((int(nblocks), dim), np.uint16)
+    if out.size:
+        _lib().qla_gen_unit_bf16(_u16_ptr(out), nblocks, dim, seed, tensor_id, block0)
+    return out
+
+
+def gaussian_bf16(nblocks, block_elems, seed, tensor_id, scale=1.0, block0=0):
+    out = np.empty((int(nblocks), int(block_elems)), np.uint16)
+    if out.size:
+        _lib().qla_gen_gaussian_bf16(_u16_ptr(out), nblocks, block_elems, seed, tensor_id, block0, scale)
+    return out
+
+
+def uniform(nblocks, block_elems, seed, tensor_id, lo, hi, log_space=False, block0=0):
+    out = np.empty((int(nblocks), int(block_elems)), np.float32)
+    if out.size:
+        _lib().qla_gen_uniform(_ptr(out), nblocks, block_elems, seed, tensor_id, block0, lo, hi, int(log_space))
+    return out
+
+
+def bf16_to_f32(a):
+    """Exact fp32 values of bf16 bit patterns (int16 or uint16 arrays)."""
+    return (np.asarray(a).view(np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def f32_to_bf16(x):
+    """bf16 bit patterns (int16) of fp32 values, rounded to nearest even."""
+    u = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16).view(np.int16)
+
+
+@dataclass(frozen=True)
+class LocalCase:
+    """One synthetic local-pass problem: T tokens per chain in S segments."""
+    B: int
+    heads: int
+    T: int
+    S: int
+    K: int
+    V: int
+    seed: int
+    beta_lo: float = 0.0
+    beta_hi: float = 1.0
+    alpha_lo: float = 0.9
+    alpha_hi: float = 1.0
+    v_scale: float = 1.0
+
+    @property
+    def chains(self):
+        return self.B * self.heads
+
+    @property
+    def L(self):
+        return self.T // self.S
+
+    def with_(self, **kw):
+        return replace(self, **kw)
+
+
+def make_local_inputs(c: LocalCase, unit0: int = 0):
+    """Returns (k, v, beta, g): k, v int16 bf16 bit patterns [B, heads, T, K|V];
+    beta, g float32 [B, heads, T].  ``unit0`` is this problem's first chain
+    within a larger job of the same case (as for make_inputs)."""
+    assert c.S >= 1 and c.T % c.S == 0
+    n = c.chains
+    k = unit_bf16(n * c.T, c.K, c.seed, TENSOR_KEY, block0=unit0 * c.T)
+    v = gaussian_bf16(n * c.T, c.V, c.seed, TENSOR_VALUE, c.v_scale, block0=unit0 * c.T)
+    beta = uniform(n, c.T, c.seed, TENSOR_BETA, c.beta_lo, c.beta_hi, block0=unit0)
+    g = uniform(n, c.T, c.seed, TENSOR_GATE, c.alpha_lo, c.alpha_hi, log_space=True, block0=unit0)
+    sh = (c.B, c.heads, c.T)
+    return (k.view(np.int16).reshape(sh + (c.K,)), v.view(np.int16).reshape(sh + (c.V,)), beta.reshape(sh),
+            g.reshape(sh))
+
+
+# Local-pass workloads.  The pages give no token-level distributions; these
+# keep each segment's propagation matrix well inside fp32's range and far from
+# zero: a small single-head case with strong writes and decays, and the
+# 32-head case of the correction workload (32K tokens in 8 segments of 4K,
+# K = V = 128) with moderate writes (beta below 0.1) and decays near 1.
+LOCAL_WORKLOADS = {
+    "l0": LocalCase(B=1, heads=1, T=256, S=4, K=64, V=64, seed=20, beta_lo=0.0, beta_hi=1.0, alpha_lo=0.9,
+                    alpha_hi=1.0),
+    "l1": LocalCase(B=1, heads=32, T=32768, S=8, K=128, V=128, seed=21, beta_lo=0.0, beta_hi=0.1,
+                    alpha_lo=0.999, alpha_hi=1.0),
+}

@@ -175,3 +175,68 @@ void qla_gen_small_int(float* out, int64_t nblocks, int64_t block_elems, uint64_
     for (int64_t e = 0; e < block_elems; ++e) o[e] = (float)((int64_t)(rng_next(&r) % span) - maxabs);
   }
 }
+
+/* ------------------------------------------------------------------ local pass inputs
+ * Token-level inputs of the per-segment local pass: keys and values in bf16
+ * (bit patterns), write strengths and log-space decays in fp32. */
+
+/* bf16 bit pattern of x: rounded to fp32, then to bf16 with ties to even. */
+static uint16_t to_bf16(double x) {
+  float f = (float)x;
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+/* Blocks of `dim` values: a Gaussian vector scaled to unit length, in bf16. */
+void qla_gen_unit_bf16(uint16_t* out, int64_t nblocks, int dim, uint64_t seed, uint64_t tensor_id,
+                       int64_t block0) {
+#pragma omp parallel
+  {
+    double* tmp = (double*)malloc(sizeof(double) * (size_t)dim);
+#pragma omp for schedule(static)
+    for (int64_t b = 0; b < nblocks; ++b) {
+      qla_rng r = stream_for(seed, tensor_id, block0 + b);
+      fill_gauss(&r, tmp, dim);
+      double nrm = 0.0;
+      for (int e = 0; e < dim; ++e) nrm += tmp[e] * tmp[e];
+      nrm = sqrt(nrm);
+      uint16_t* o = out + b * (int64_t)dim;
+      for (int e = 0; e < dim; ++e) o[e] = to_bf16(tmp[e] / nrm);
+    }
+    free(tmp);
+  }
+}
+
+/* Blocks of block_elems values ~ N(0,1) * scale, in bf16. */
+void qla_gen_gaussian_bf16(uint16_t* out, int64_t nblocks, int64_t block_elems, uint64_t seed,
+                           uint64_t tensor_id, int64_t block0, double scale) {
+#pragma omp parallel
+  {
+    double* tmp = (double*)malloc(sizeof(double) * (size_t)block_elems);
+#pragma omp for schedule(static)
+    for (int64_t b = 0; b < nblocks; ++b) {
+      qla_rng r = stream_for(seed, tensor_id, block0 + b);
+      fill_gauss(&r, tmp, block_elems);
+      uint16_t* o = out + b * block_elems;
+      for (int64_t e = 0; e < block_elems; ++e) o[e] = to_bf16(tmp[e] * scale);
+    }
+    free(tmp);
+  }
+}
+
+/* Blocks of block_elems values ~ U(lo, hi); with `log_space` set, the natural
+ * logarithm of such a draw (a log-space decay), rounded to fp32 once. */
+void qla_gen_uniform(float* out, int64_t nblocks, int64_t block_elems, uint64_t seed, uint64_t tensor_id,
+                     int64_t block0, double lo, double hi, int log_space) {
+#pragma omp parallel for schedule(static)
+  for (int64_t b = 0; b < nblocks; ++b) {
+    qla_rng r = stream_for(seed, tensor_id, block0 + b);
+    float* o = out + b * block_elems;
+    for (int64_t e = 0; e < block_elems; ++e) {
+      const double x = lo + (hi - lo) * rng_uniform(&r);
+      o[e] = (float)(log_space ? log(x) : x);
+    }
+  }
+}

@@ -139,3 +139,42 @@ def read_golden(path):
             rows = [[float(x) for x in r.split()] for r in rhs.split(";")]
             vals[name] = np.array(rows, np.float64)
     return vals
+
+
+def bf16_bits_to_f64(a):
+    """Exact values of bf16 bit patterns (int16 or uint16 arrays)."""
+    return (np.asarray(a).view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def local_products(k, v, beta, g, S, layout="kv"):
+    """Brute force for the local pass: every token's transition formed as a
+    dense matrix, A_t = a_t (I - b_t k_t k_t^T) with a_t = exp(g_t), and per
+    segment M = A_last ... A_first, H = sum_t (A_last ... A_{t+1}) b_t k_t v_t^T
+    (kv view; transposed for vk).  Returns (H, M) in fp64."""
+    kf = bf16_bits_to_f64(k)
+    vf = bf16_bits_to_f64(v)
+    B, nh, T, K = kf.shape
+    V = vf.shape[-1]
+    L = T // S
+    H = np.zeros((B, nh, S, K, V))
+    M = np.zeros((B, nh, S, K, K))
+    for b in range(B):
+        for n in range(nh):
+            for i in range(S):
+                seg = range(i * L, (i + 1) * L)
+                A = [np.exp(np.float64(g[b, n, t])) * (np.eye(K) - np.float64(beta[b, n, t]) *
+                                                        np.outer(kf[b, n, t], kf[b, n, t])) for t in seg]
+                Mi = np.eye(K)
+                for At in A:
+                    Mi = At @ Mi
+                Hi = np.zeros((K, V))
+                for j, t in enumerate(seg):
+                    P = np.eye(K)
+                    for At in A[j + 1:]:
+                        P = At @ P
+                    Hi += P @ (np.float64(beta[b, n, t]) * np.outer(kf[b, n, t], vf[b, n, t]))
+                M[b, n, i] = Mi
+                H[b, n, i] = Hi
+    if layout == "vk":
+        H = np.swapaxes(H, -1, -2)
+    return H, M
