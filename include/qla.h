@@ -303,6 +303,44 @@ QLA_API int qla_cp_correct_scan_static(const float* H, const float* M, const flo
                                        float* final_state, int B, int heads, int S, int K, int V, int layout,
                                        int direction, int engine, int release, int scan_group, void* stream);
 
+/*
+ * The per-segment local pass that produces H and M for the correction.
+ * Antarx Memos, "一次 TileLang Warp Specialization 数值错误的定位与修复", section
+ * "从版本升级后的数值偏差开始", names each segment's local state ("ht") and
+ * propagation matrix ("mt") but not how they are computed; this library reads
+ * them as the gated delta rule (Yang, Kautz, Hatamizadeh, "Gated Delta
+ * Networks", ICLR 2025), token by token in the kv view:
+ *
+ *     X_t = a_t (I - b_t k_t k_t^T) X_{t-1} + b_t k_t v_t^T,   a_t = exp(g_t),
+ *
+ * and for segment i (tokens i*L .. i*L + L - 1, L = T / S):
+ *     H_i = that recurrence's state after the segment, from X = 0,
+ *     M_i = A_last ... A_first,   A_t = a_t (I - b_t k_t k_t^T),
+ * so that the state after the segment is M_i X_enter + H_i, the forward
+ * recurrence qla_cp_correct composes (the reverse pass needs the segments'
+ * local gradients, which this pass does not compute).
+ *
+ * Memory (DEVICE pointers owned by the caller, contiguous, row-major):
+ *     k     [B][heads][T][K]  bf16 (16-bit patterns), 16-byte aligned
+ *     v     [B][heads][T][V]  bf16, 16-byte aligned
+ *     beta  [B][heads][T]     fp32 write strengths, 4-byte aligned
+ *     g     [B][heads][T]     fp32 log-space decays, 4-byte aligned
+ *     H     [B][heads][S][K][V] (kv) or [B][heads][S][V][K] (vk), fp32, or NULL
+ *     M     [B][heads][S][K][K] fp32, or NULL (not both NULL); 16-byte aligned
+ * exactly the H and M arguments of qla_cp_correct.  T must be a multiple of S;
+ * K and V multiples of 32 in [32, 256].  H and M may not overlap each other or
+ * the inputs (QLA_ERR_ALIAS).  Decays are applied as a running scale kept in
+ * fp64 (no fp32 compounding); a single token whose g_t is below about -80
+ * empties the state (exp underflows), as in exact arithmetic to fp32 range.
+ * Asynchronous on `stream`.  With the dependent-launch switch on
+ * (qla_set_dependent_launch) the kernel is itself a programmatic dependent,
+ * and it lets the next kernel on the stream launch at once: a correction
+ * enqueued right after it starts its set-up early and reads H and M only
+ * after this kernel has completed.
+ */
+QLA_API int qla_local_pass(const void* k, const void* v, const float* beta, const float* g, float* H, float* M,
+                           int B, int heads, int T, int S, int K, int V, int layout, void* stream);
+
 /* ABI version of this header (major * 100 + minor). */
 QLA_API int qla_version(void);
 

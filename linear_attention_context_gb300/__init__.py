@@ -34,7 +34,7 @@ STATUS = {0: "QLA_OK", -1: "QLA_ERR_INVALID_ARG", -2: "QLA_ERR_UNSUPPORTED", -3:
 EXPORTS = ("qla_cp_correct", "qla_cp_correct_ex", "qla_cp_correct_varlen", "qla_cp_correct_varlen_ex",
            "qla_scan_workspace_bytes", "qla_set_variant", "qla_set_dependent_launch",
            "qla_resolve", "qla_status_string", "qla_last_error", "qla_device_status", "qla_selftest_stalled_wait",
-           "qla_selftest_dependent_producer", "qla_cp_correct_scan_static", "qla_version")
+           "qla_selftest_dependent_producer", "qla_cp_correct_scan_static", "qla_local_pass", "qla_version")
 
 # Bytes of scratch the allocation-free scan entry point holds (QLA_SCAN_STATIC_BYTES).
 SCAN_STATIC_BYTES = 8 << 20
@@ -91,6 +91,8 @@ def lib():
         L.qla_selftest_stalled_wait.restype = ci
         L.qla_cp_correct_scan_static.argtypes = [vp, vp, vp, vp, vp] + [ci] * 10 + [vp]
         L.qla_cp_correct_scan_static.restype = ci
+        L.qla_local_pass.argtypes = [vp] * 6 + [ci] * 7 + [vp]
+        L.qla_local_pass.restype = ci
         L.qla_version.argtypes = []
         L.qla_version.restype = ci
         _LIB = L
@@ -222,6 +224,47 @@ def cp_correct_varlen(H, M, cu_seg, h_init=None, out=None, *, layout="kv", direc
                                             int(max_segments), int(scan_group), _stream_handle(stream))
     check(rc)
     return out
+
+
+def local_pass(k, v, beta, g, S, H=None, M=None, *, layout="kv", want_H=True, want_M=True, stream=None):
+    """Per-segment local states H and propagation matrices M (the inputs of
+    cp_correct) from token-level inputs, by the gated delta rule (include/qla.h,
+    qla_local_pass).
+
+    k: [B, heads, T, K] and v: [B, heads, T, V] CUDA tensors of dtype bfloat16
+    (or int16 holding bf16 bit patterns); beta, g: [B, heads, T] float32 (write
+    strengths, log-space decays); T a multiple of S.  H ([B, heads, S, K, V] kv
+    or [B, heads, S, V, K] vk) and M ([B, heads, S, K, K]) float32 are
+    allocated when not given.  Returns (H, M), None for a part not wanted."""
+    import torch
+    if layout not in LAYOUTS:
+        raise ValueError(f"layout {layout!r}")
+    if k.dim() != 4 or v.dim() != 4:
+        raise ValueError("k and v must be [B, heads, T, K] and [B, heads, T, V]")
+    B, nh, T, K = k.shape
+    V = v.shape[3]
+    dev = k.device
+    if dev.type != "cuda":
+        raise ValueError("k must be a CUDA tensor")
+    for name, t in (("k", k), ("v", v)):
+        if t.dtype not in (torch.bfloat16, torch.int16) or t.device != dev or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bfloat16 (or int16) tensor on {dev}")
+    if tuple(v.shape[:3]) != (B, nh, T):
+        raise ValueError(f"v must be {(B, nh, T, V)}, got {tuple(v.shape)}")
+    _check_tensor("beta", beta, dev, (B, nh, T))
+    _check_tensor("g", g, dev, (B, nh, T))
+    st = (K, V) if layout == "kv" else (V, K)
+    if want_H and H is None:
+        H = torch.empty((B, nh, S) + st, dtype=torch.float32, device=dev)
+    if want_M and M is None:
+        M = torch.empty((B, nh, S, K, K), dtype=torch.float32, device=dev)
+    _check_tensor("H", H, dev, (B, nh, S) + st)
+    _check_tensor("M", M, dev, (B, nh, S, K, K))
+    with torch.cuda.device(dev):
+        rc = lib().qla_local_pass(_ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(H), _ptr(M), B, nh, T, S, K, V,
+                                  LAYOUTS[layout], _stream_handle(stream))
+    check(rc)
+    return H, M
 
 
 def set_variant(variant: str):

@@ -703,6 +703,63 @@ int qla_cp_correct_varlen_ex(const float* H, const float* M, const float* h_init
   return run_scan_varlen(j, s, eng, scan_group, d, cs);
 }
 
+int qla_local_pass(const void* k, const void* v, const float* beta, const float* g, float* H, float* M, int B,
+                   int heads, int T, int S, int K, int V, int layout, void* stream) {
+  t_last_error.clear();
+  if (B < 1 || heads < 1 || S < 1 || T < 1 || K < 1 || V < 1)
+    return fail(QLA_ERR_INVALID_ARG, "B, heads, T, S, K, V must be >= 1 (got %d, %d, %d, %d, %d, %d)", B, heads, T,
+                S, K, V);
+  if (T % S) return fail(QLA_ERR_INVALID_ARG, "T (%d) must be a multiple of S (%d)", T, S);
+  if (layout != QLA_LAYOUT_KV && layout != QLA_LAYOUT_VK)
+    return fail(QLA_ERR_INVALID_ARG, "layout must be QLA_LAYOUT_KV or QLA_LAYOUT_VK (got %d)", layout);
+  if (!k || !v || !beta || !g) return fail(QLA_ERR_INVALID_ARG, "k, v, beta and g must not be NULL");
+  if (!H && !M) return fail(QLA_ERR_INVALID_ARG, "H and M are both NULL: nothing to compute");
+  if (K % 32 || K > 256 || V % 32 || V > 256)
+    return fail(QLA_ERR_UNSUPPORTED, "K and V must be multiples of 32 in [32, 256] (got K=%d, V=%d)", K, V);
+  const int64_t chains = (int64_t)B * heads;
+  if (chains * S > 0x7fffffff) return fail(QLA_ERR_UNSUPPORTED, "B*heads*S must be below 2^31");
+  if ((double)chains * T * std::max(K, V) >= 4.6e18) return fail(QLA_ERR_INVALID_ARG, "problem too large");
+  const void* p16[] = {k, v, H, M};
+  const char* n16[] = {"k", "v", "H", "M"};
+  for (int i = 0; i < 4; ++i)
+    if (p16[i] && (reinterpret_cast<uintptr_t>(p16[i]) & 15))
+      return fail(QLA_ERR_ALIGNMENT, "%s is not 16-byte aligned", n16[i]);
+  if ((reinterpret_cast<uintptr_t>(beta) | reinterpret_cast<uintptr_t>(g)) & 3)
+    return fail(QLA_ERR_ALIGNMENT, "beta and g must be 4-byte aligned");
+  Range r[6];
+  int n = 0;
+  r[n++] = {(uintptr_t)k, (uintptr_t)k + (uintptr_t)(chains * T * K * 2), "k"};
+  r[n++] = {(uintptr_t)v, (uintptr_t)v + (uintptr_t)(chains * T * V * 2), "v"};
+  r[n++] = {(uintptr_t)beta, (uintptr_t)beta + (uintptr_t)(chains * T * 4), "beta"};
+  r[n++] = {(uintptr_t)g, (uintptr_t)g + (uintptr_t)(chains * T * 4), "g"};
+  if (H) r[n++] = {(uintptr_t)H, (uintptr_t)H + (uintptr_t)(chains * S * K * V * 4), "H"};
+  if (M) r[n++] = {(uintptr_t)M, (uintptr_t)M + (uintptr_t)(chains * S * K * K * 4), "M"};
+  for (int a = 4; a < n; ++a)  // outputs against everything before them
+    for (int b = 0; b < a; ++b)
+      if (overlap(r[a], r[b])) return fail(QLA_ERR_ALIAS, "%s and %s overlap", r[a].name, r[b].name);
+  DeviceInfo* d = nullptr;
+  int st = current_device(&d);
+  if (st != QLA_OK) return st;
+  LocalJob j{};
+  j.k = static_cast<const uint16_t*>(k);
+  j.v = static_cast<const uint16_t*>(v);
+  j.beta = beta;
+  j.g = g;
+  j.H = H;
+  j.M = M;
+  j.nchains = (int)chains;
+  j.T = T;
+  j.S = S;
+  j.L = T / S;
+  j.K = K;
+  j.V = V;
+  j.layout = layout;
+  j.pdl = dependent_launch();
+  const cudaError_t e = launch_local_simt(j, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return QLA_OK;
+}
+
 int qla_device_status(int* flags) {
   t_last_error.clear();
   DeviceInfo* d = nullptr;

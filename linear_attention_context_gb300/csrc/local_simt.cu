@@ -1,0 +1,291 @@
+// Per-segment local pass: the inputs (H_i, M_i) of the context-parallel state
+// correction, computed from token-level keys, values, write strengths and
+// decays.  Antarx Memos, "一次 TileLang Warp Specialization 数值错误的定位与修复：
+// 从双缓冲竞争到 membar", section "从版本升级后的数值偏差开始", names the two
+// per-segment quantities (the local state "ht" and the propagation matrix
+// "mt") without defining them; the reading implemented here is the token
+// recurrence of the gated delta rule (Yang, Kautz, Hatamizadeh, "Gated Delta
+// Networks: Improving Mamba2 with Delta Rule", ICLR 2025) in the kv view:
+//
+//     X_t = a_t (I - b_t k_t k_t^T) X_{t-1} + b_t k_t v_t^T,   a_t = exp(g_t)
+//
+// and for each segment of L tokens H = the state after its tokens from zero,
+// M = A_last ... A_first with A_t = a_t (I - b_t k_t k_t^T), so that the state
+// leaving a segment is M X_enter + H -- the recurrence the correction composes.
+//
+// Work split.  The columns of Y = [H | M] (V columns of the local state, K of
+// the propagation matrix, which starts at the identity) evolve independently
+// under the same left multiplications, so each warp owns a block of columns of
+// one segment for the whole segment: a lane holds R rows x 2 columns in
+// registers and G = K / R lanes share a column pair (the dot product k^T Y is
+// a partial sum per lane, then a shuffle reduction over those G lanes).  Per
+// token and lane: 2R FMAs for the dot products and 2R for the update; every
+// key value read from shared memory (a broadcast) feeds two FMAs.  No
+// synchronisation between tokens.
+//
+// Decay as a scale.  Y = s Yhat with s = exp(sum of g since a reference
+// token), so the update is Yhat += k c^T with c = b (v / s - d), d = k^T Yhat:
+// the decays never multiply the state element by element, so their fp32
+// roundings do not compound over the segment.  The running log-decay sum is
+// kept in fp64 by the staging warp; 1 / s per token comes from it in fp32 (exp
+// of the high part, corrected to first order by the low part).  When the sum
+// has moved more than 16 away from the reference at some token, the state is
+// rescaled by s once, before that token's update, and the reference moves there.
+//
+// Staging.  Tokens go through shared memory in tiles of kTT: keys and values
+// widened from bf16 to fp32, write strengths, 1 / s and the rescale factors.
+// The CTA waits at a barrier while a tile is staged (the staging is a few
+// percent of the tile's arithmetic, and the SM's other CTAs keep computing).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qla_internal.h"
+
+namespace qla {
+namespace {
+
+constexpr int kLocalWarps = 2;
+constexpr int kLocalThreads = 32 * kLocalWarps;
+constexpr int kTT = 32;              // tokens per staged tile (one per lane of the staging warp)
+constexpr double kRescaleLog = 16.0;  // rescale when |log s| would exceed this
+
+struct LocalParams {
+  LocalJob j;
+  int col_begin;     // first column of Y = [H | M] computed (0, or V when H is not wanted)
+  int col_end;       // one past the last (V when M is not wanted, else V + K)
+  int cols_per_cta;  // columns of Y per CTA
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Widens n rows of `width` bf16 values (contiguous in global memory, 16-byte
+// aligned) to fp32 rows in shared memory, 8 values per thread step.
+__device__ __forceinline__ void stage_bf16_rows(const uint16_t* __restrict__ src, float* dst, int n, int width) {
+  const int total = n * width / 8;
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  float4* d4 = reinterpret_cast<float4*>(dst);
+  for (int i = threadIdx.x; i < total; i += kLocalThreads) {
+    const uint4 w = __ldg(s4 + i);
+    d4[2 * i] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+    d4[2 * i + 1] = make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+  }
+}
+
+// exp(x) for an fp64 x: exp of the fp32 high part times (1 + the low part).
+__device__ __forceinline__ float exp_split(double x) {
+  const float hi = (float)x;
+  const float lo = (float)(x - (double)hi);
+  return expf(hi) * (1.0f + lo);
+}
+
+template <int R, int G>
+__global__ void __launch_bounds__(kLocalThreads) local_pass_kernel(const LocalParams p) {
+  constexpr int CW = 32 / G;  // column pairs per warp
+  const LocalJob& j = p.j;
+  const int K = j.K, V = j.V, L = j.L;
+  const int64_t unit = blockIdx.z == 0 ? (int64_t)blockIdx.y : (int64_t)blockIdx.z * gridDim.y + blockIdx.y;
+  if (unit >= (int64_t)j.nchains * j.S) return;
+  const int64_t chain = unit / j.S;
+  const int seg = (int)(unit - chain * j.S);
+
+  extern __shared__ __align__(16) float smem[];
+  float* ks = smem;               // [kTT][K]
+  float* vs = ks + kTT * K;       // [kTT][V]
+  float* bs = vs + kTT * V;       // [kTT] write strength
+  float* inv_s = bs + kTT;        // [kTT] 1 / s for the token's update
+  float* fac_s = inv_s + kTT;     // [kTT] rescale factor before the token's update (1 = none)
+  float* s_end = fac_s + kTT;     // [1] s after the segment's last token
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int part = lane / CW;  // which block of R rows
+  const int q = lane - part * CW;
+  const int row0 = part * R;
+  const int cta_c0 = p.col_begin + (int)blockIdx.x * p.cols_per_cta;
+  const int gc = cta_c0 + warp * (2 * CW) + 2 * q;  // this lane's first column of Y (the second is gc + 1)
+  const bool live = gc < p.col_end;
+  const bool is_h = gc < V;
+  const int mc = gc - V;             // its column of M when !is_h
+  const bool need_v = cta_c0 < V;    // the CTA holds a column of H
+
+  float y0[R], y1[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    y0[r] = (!is_h && row0 + r == mc) ? 1.0f : 0.0f;
+    y1[r] = (!is_h && row0 + r == mc + 1) ? 1.0f : 0.0f;
+  }
+
+  // Let a dependent kernel (the correction) launch now; it reads H and M only
+  // after its griddepcontrol.wait, i.e. after this grid has completed.
+  griddep_launch_dependents();
+  griddep_wait();
+
+  const int64_t tok0 = chain * j.T + (int64_t)seg * L;
+  double gsum = 0.0, gref = 0.0;  // staging warp: log-decay after the previous tile, and the reference
+  for (int t0 = 0; t0 < L; t0 += kTT) {
+    const int n = min(kTT, L - t0);
+    __syncthreads();  // every warp is done with the previous tile
+    stage_bf16_rows(j.k + (tok0 + t0) * K, ks, n, K);
+    if (need_v) stage_bf16_rows(j.v + (tok0 + t0) * V, vs, n, V);
+    if (warp == 0) {
+      // lane i <-> token t0 + i: inclusive prefix sum of the log-decays, fp64
+      double G = lane < n ? (double)__ldg(j.g + tok0 + t0 + lane) : 0.0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, G, o);
+        if (lane >= o) G += y;
+      }
+      G += gsum;
+      // Reference moves: the first token whose sum is more than kRescaleLog
+      // from the reference rescales the state before its update and becomes
+      // the reference; tokens before it keep the old one.
+      double ref = gref;
+      bool done = lane >= n;
+      float fac = 1.0f, inv = 1.0f;
+      for (;;) {
+        const unsigned far = __ballot_sync(0xffffffffu, !done && fabs(G - ref) > kRescaleLog);
+        if (!far) break;
+        const int f = __ffs(far) - 1;
+        const double Gf = __shfl_sync(0xffffffffu, G, f);
+        if (!done && lane < f) {
+          inv = exp_split(ref - G);
+          done = true;
+        }
+        if (lane == f) {
+          fac = exp_split(Gf - ref);
+          inv = 1.0f;
+          done = true;
+        }
+        ref = Gf;
+      }
+      if (!done) inv = exp_split(ref - G);
+      if (lane < n) {
+        bs[lane] = __ldg(j.beta + tok0 + t0 + lane);
+        inv_s[lane] = inv;
+        fac_s[lane] = fac;
+      }
+      if (lane == n - 1) s_end[0] = exp_split(G - ref);
+      gsum = __shfl_sync(0xffffffffu, G, n - 1);
+      gref = ref;
+    }
+    __syncthreads();
+
+    for (int i = 0; i < n; ++i) {
+      const float fac = fac_s[i];
+      if (fac != 1.0f) {  // same for every thread of the CTA
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          y0[r] *= fac;
+          y1[r] *= fac;
+        }
+      }
+      const float* kr = ks + i * K + row0;
+      float d0a = 0.f, d0b = 0.f, d1a = 0.f, d1b = 0.f;
+#pragma unroll
+      for (int r = 0; r < R; r += 4) {
+        const float4 kk = *reinterpret_cast<const float4*>(kr + r);
+        d0a = fmaf(kk.x, y0[r], d0a);
+        d1a = fmaf(kk.x, y1[r], d1a);
+        d0b = fmaf(kk.y, y0[r + 1], d0b);
+        d1b = fmaf(kk.y, y1[r + 1], d1b);
+        d0a = fmaf(kk.z, y0[r + 2], d0a);
+        d1a = fmaf(kk.z, y1[r + 2], d1a);
+        d0b = fmaf(kk.w, y0[r + 3], d0b);
+        d1b = fmaf(kk.w, y1[r + 3], d1b);
+      }
+      float d0 = d0a + d0b, d1 = d1a + d1b;
+#pragma unroll
+      for (int m = CW; m < 32; m <<= 1) {
+        d0 += __shfl_xor_sync(0xffffffffu, d0, m);
+        d1 += __shfl_xor_sync(0xffffffffu, d1, m);
+      }
+      float v0 = 0.f, v1 = 0.f;
+      if (is_h && live) {
+        const float2 vv = *reinterpret_cast<const float2*>(vs + i * V + gc);
+        v0 = vv.x;
+        v1 = vv.y;
+      }
+      const float b = bs[i], inv = inv_s[i];
+      const float c0 = b * fmaf(v0, inv, -d0);
+      const float c1 = b * fmaf(v1, inv, -d1);
+#pragma unroll
+      for (int r = 0; r < R; r += 4) {
+        const float4 kk = *reinterpret_cast<const float4*>(kr + r);
+        y0[r] = fmaf(kk.x, c0, y0[r]);
+        y1[r] = fmaf(kk.x, c1, y1[r]);
+        y0[r + 1] = fmaf(kk.y, c0, y0[r + 1]);
+        y1[r + 1] = fmaf(kk.y, c1, y1[r + 1]);
+        y0[r + 2] = fmaf(kk.z, c0, y0[r + 2]);
+        y1[r + 2] = fmaf(kk.z, c1, y1[r + 2]);
+        y0[r + 3] = fmaf(kk.w, c0, y0[r + 3]);
+        y1[r + 3] = fmaf(kk.w, c1, y1[r + 3]);
+      }
+    }
+  }
+  if (!live) return;
+  const float s = s_end[0];
+  if (is_h) {
+    float* h = j.H + unit * (int64_t)K * V;
+    if (j.layout == 0) {  // kv: H[k][v]
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        *reinterpret_cast<float2*>(h + (int64_t)(row0 + r) * V + gc) = make_float2(y0[r] * s, y1[r] * s);
+    } else {  // vk: H[v][k]
+      float* h0 = h + (int64_t)gc * K + row0;
+      float* h1 = h0 + K;
+#pragma unroll
+      for (int r = 0; r < R; r += 4) {
+        *reinterpret_cast<float4*>(h0 + r) = make_float4(y0[r] * s, y0[r + 1] * s, y0[r + 2] * s, y0[r + 3] * s);
+        *reinterpret_cast<float4*>(h1 + r) = make_float4(y1[r] * s, y1[r + 1] * s, y1[r + 2] * s, y1[r + 3] * s);
+      }
+    }
+  } else {
+    float* m = j.M + unit * (int64_t)K * K;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      *reinterpret_cast<float2*>(m + (int64_t)(row0 + r) * K + mc) = make_float2(y0[r] * s, y1[r] * s);
+  }
+}
+
+template <int R, int G>
+cudaError_t launch_rg(const LocalJob& j, cudaStream_t stream) {
+  LocalParams p{};
+  p.j = j;
+  p.col_begin = j.H ? 0 : j.V;
+  p.col_end = j.M ? j.V + j.K : j.V;
+  p.cols_per_cta = kLocalWarps * 64 / G;
+  const int64_t units = (int64_t)j.nchains * j.S;
+  const int xblocks = (p.col_end - p.col_begin + p.cols_per_cta - 1) / p.cols_per_cta;
+  dim3 grid(xblocks, 1, 1);
+  if (units <= 65535) {
+    grid.y = (unsigned)units;
+  } else {
+    grid.y = 65535u;
+    grid.z = (unsigned)((units + 65534) / 65535);
+  }
+  const size_t smem = sizeof(float) * (size_t)(kTT * (j.K + j.V) + 3 * kTT + 4);
+  cudaError_t e = cudaFuncSetAttribute(local_pass_kernel<R, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(local_pass_kernel<R, G>, grid, kLocalThreads, smem, stream, j.pdl != 0, p);
+}
+
+}  // namespace
+
+// Rows per lane R and lanes per column pair G for a key dimension K (a
+// multiple of 32 up to 256): G is the smallest power of two with K / G <= 64.
+cudaError_t launch_local_simt(const LocalJob& j, cudaStream_t stream) {
+  switch (j.K) {
+    case 32: return launch_rg<32, 1>(j, stream);
+    case 64: return launch_rg<64, 1>(j, stream);
+    case 96: return launch_rg<48, 2>(j, stream);
+    case 128: return launch_rg<64, 2>(j, stream);
+    case 160: return launch_rg<40, 4>(j, stream);
+    case 192: return launch_rg<48, 4>(j, stream);
+    case 224: return launch_rg<56, 4>(j, stream);
+    case 256: return launch_rg<64, 4>(j, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace qla

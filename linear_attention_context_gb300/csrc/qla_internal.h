@@ -145,6 +145,21 @@ bool tc_f16_supports(int K, int V);
 cudaError_t launch_seq_tc_f16(const SeqJob& job, int release, unsigned int* status, uint64_t limit_ns,
                               int stall_test, cudaStream_t stream);
 
+// One launch of the per-segment local pass (local_simt.cu): for every chain
+// and segment of L = T / S tokens, H = the segment's gated-delta-rule state
+// from zero and M = the product of its token transitions.
+struct LocalJob {
+  const uint16_t* k;  // [nchains][T][K] bf16 bit patterns
+  const uint16_t* v;  // [nchains][T][V] bf16 bit patterns
+  const float* beta;  // [nchains][T]
+  const float* g;     // [nchains][T] log-space decays
+  float* H;           // [nchains][S][K][V] (kv) or [..][V][K] (vk), or nullptr
+  float* M;           // [nchains][S][K][K], or nullptr
+  int nchains, T, S, L, K, V, layout;
+  int pdl;            // launch as a programmatic dependent of the stream's previous kernel
+};
+cudaError_t launch_local_simt(const LocalJob& job, cudaStream_t stream);
+
 // Bound on every device-side wait of the pipelined engines.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 

@@ -206,3 +206,29 @@ def test_dependent_producer_checks(L, src, dst, nbytes, delay, status):
     vp = ctypes.c_void_p
     assert L.qla_selftest_dependent_producer(None if src is None else vp(src), None if dst is None else vp(dst),
                                              nbytes, delay, None) == status
+
+
+def call_local(L, k=FAKE, v=FAKE + (1 << 32), beta=FAKE + (2 << 32), g=FAKE + (3 << 32), H=FAKE + (4 << 32),
+               M=FAKE + (5 << 32), B=1, heads=2, T=64, S=4, K=64, V=64, layout=0):
+    vp = ctypes.c_void_p
+    return L.qla_local_pass(vp(k), vp(v), vp(beta), vp(g), vp(H), vp(M), B, heads, T, S, K, V, layout, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(k=None), -1), (dict(v=None), -1), (dict(beta=None), -1), (dict(g=None), -1), (dict(H=None, M=None), -1),
+    (dict(T=66), -1), (dict(S=0), -1), (dict(T=0), -1), (dict(B=0), -1), (dict(layout=2), -1),
+    (dict(K=48), -2), (dict(V=288), -2), (dict(B=1 << 20, heads=1 << 10, T=1 << 12, S=1 << 12), -2),
+    (dict(k=FAKE + 8), -3), (dict(v=FAKE + (1 << 32) + 2), -3), (dict(H=FAKE + (4 << 32) + 4), -3),
+    (dict(M=FAKE + (5 << 32) + 8), -3), (dict(beta=FAKE + (2 << 32) + 2), -3), (dict(g=FAKE + (3 << 32) + 1), -3),
+    # outputs over an input, or over each other
+    (dict(H=FAKE + 64), -4), (dict(M=FAKE + (3 << 32) + 16), -4), (dict(M=FAKE + (4 << 32) + 4096), -4),
+])
+def test_local_pass_argument_checks(L, kw, status):
+    assert call_local(L, **kw) == status
+    assert L.qla_last_error().decode() != ""
+
+
+@no_gpu_only
+def test_local_pass_valid_call_without_gpu(L):
+    assert call_local(L) == -5
+    assert call_local(L, H=None) == -5 and call_local(L, M=None) == -5
