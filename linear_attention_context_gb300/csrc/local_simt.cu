@@ -34,8 +34,8 @@
 //
 // Staging.  Tokens go through shared memory in tiles of kTT: keys and values
 // widened from bf16 to fp32, write strengths, 1 / s and the rescale factors.
-// The CTA waits at a barrier while a tile is staged (the staging is a few
-// percent of the tile's arithmetic, and the SM's other CTAs keep computing).
+// The next tile's raw inputs are copied in (cp.async) while the current tile
+// computes; widening them is a shared-to-shared pass at the tile's start.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -59,19 +59,6 @@ struct LocalParams {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Widens n rows of `width` bf16 values (contiguous in global memory, 16-byte
-// aligned) to fp32 rows in shared memory, 8 values per thread step.
-__device__ __forceinline__ void stage_bf16_rows(const uint16_t* __restrict__ src, float* dst, int n, int width) {
-  const int total = n * width / 8;
-  const uint4* s4 = reinterpret_cast<const uint4*>(src);
-  float4* d4 = reinterpret_cast<float4*>(dst);
-  for (int i = threadIdx.x; i < total; i += kLocalThreads) {
-    const uint4 w = __ldg(s4 + i);
-    d4[2 * i] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
-    d4[2 * i + 1] = make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
-  }
-}
-
 // exp(x) for an fp64 x: exp of the fp32 high part times (1 + the low part).
 __device__ __forceinline__ float exp_split(double x) {
   const float hi = (float)x;
@@ -79,8 +66,55 @@ __device__ __forceinline__ float exp_split(double x) {
   return expf(hi) * (1.0f + lo);
 }
 
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Issues the copies of a tile's raw inputs (bf16 keys and values, fp32 write
+// strengths and log-decays) into shared memory.
+__device__ __forceinline__ void issue_tile(const LocalJob& j, int64_t tok, int n, bool need_v, uint16_t* kraw,
+                                           uint16_t* vraw, float* braw, float* graw) {
+  const int kc = n * j.K / 8, vc = need_v ? n * j.V / 8 : 0;
+  const uint4* ks = reinterpret_cast<const uint4*>(j.k + tok * j.K);
+  const uint4* vs = reinterpret_cast<const uint4*>(j.v + tok * j.V);
+  for (int i = threadIdx.x; i < kc; i += kLocalThreads) cp_async16(reinterpret_cast<uint4*>(kraw) + i, ks + i);
+  for (int i = threadIdx.x; i < vc; i += kLocalThreads) cp_async16(reinterpret_cast<uint4*>(vraw) + i, vs + i);
+  if (threadIdx.x < n) cp_async4(braw + threadIdx.x, j.beta + tok + threadIdx.x);
+  else if (threadIdx.x >= 32 && threadIdx.x - 32 < n) cp_async4(graw + threadIdx.x - 32, j.g + tok + threadIdx.x - 32);
+  cp_async_commit();
+}
+
+// Widens n rows of `width` bf16 values to fp32, shared memory to shared memory.
+__device__ __forceinline__ void widen_rows(const uint16_t* src, float* dst, int n, int width) {
+  const int total = n * width / 8;
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  float4* d4 = reinterpret_cast<float4*>(dst);
+  for (int i = threadIdx.x; i < total; i += kLocalThreads) {
+    const uint4 w = s4[i];
+    d4[2 * i] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+    d4[2 * i + 1] = make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+  }
+}
+
+// Reduces a lane's partial dot products over the G lanes sharing its columns.
+template <int CW>
+__device__ __forceinline__ void reduce_parts(float& d0, float& d1) {
+#pragma unroll
+  for (int m = CW; m < 32; m <<= 1) {
+    d0 += __shfl_xor_sync(0xffffffffu, d0, m);
+    d1 += __shfl_xor_sync(0xffffffffu, d1, m);
+  }
+}
+
 template <int R, int G>
-__global__ void __launch_bounds__(kLocalThreads) local_pass_kernel(const LocalParams p) {
+__global__ void __launch_bounds__(kLocalThreads, 6) local_pass_kernel(const LocalParams p) {
   constexpr int CW = 32 / G;  // column pairs per warp
   const LocalJob& j = p.j;
   const int K = j.K, V = j.V, L = j.L;
@@ -90,12 +124,16 @@ __global__ void __launch_bounds__(kLocalThreads) local_pass_kernel(const LocalPa
   const int seg = (int)(unit - chain * j.S);
 
   extern __shared__ __align__(16) float smem[];
-  float* ks = smem;               // [kTT][K]
-  float* vs = ks + kTT * K;       // [kTT][V]
+  float* ks = smem;               // [kTT][K] keys, fp32
+  float* vs = ks + kTT * K;       // [kTT][V] values, fp32
   float* bs = vs + kTT * V;       // [kTT] write strength
   float* inv_s = bs + kTT;        // [kTT] 1 / s for the token's update
-  float* fac_s = inv_s + kTT;     // [kTT] rescale factor before the token's update (1 = none)
-  float* s_end = fac_s + kTT;     // [1] s after the segment's last token
+  float* fac_s = inv_s + kTT;     // [kTT] rescale factor after the previous token (1 = none)
+  float* s_end = fac_s + kTT;     // [4] s after the segment's last token
+  float* braw = s_end + 4;        // [kTT] next tile's write strengths, as loaded
+  float* graw = braw + kTT;       // [kTT] next tile's log-decays, as loaded
+  uint16_t* kraw = reinterpret_cast<uint16_t*>(graw + kTT);  // [kTT][K] next tile's keys, bf16
+  uint16_t* vraw = kraw + kTT * K;                           // [kTT][V] next tile's values, bf16
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int part = lane / CW;  // which block of R rows
@@ -121,21 +159,23 @@ __global__ void __launch_bounds__(kLocalThreads) local_pass_kernel(const LocalPa
   griddep_wait();
 
   const int64_t tok0 = chain * j.T + (int64_t)seg * L;
+  issue_tile(j, tok0, min(kTT, L), need_v, kraw, vraw, braw, graw);
   double gsum = 0.0, gref = 0.0;  // staging warp: log-decay after the previous tile, and the reference
   for (int t0 = 0; t0 < L; t0 += kTT) {
     const int n = min(kTT, L - t0);
-    __syncthreads();  // every warp is done with the previous tile
-    stage_bf16_rows(j.k + (tok0 + t0) * K, ks, n, K);
-    if (need_v) stage_bf16_rows(j.v + (tok0 + t0) * V, vs, n, V);
+    cp_async_wait_all();
+    __syncthreads();  // this tile's raw inputs have landed; every warp is done with the previous tile
+    widen_rows(kraw, ks, n, K);
+    if (need_v) widen_rows(vraw, vs, n, V);
     if (warp == 0) {
       // lane i <-> token t0 + i: inclusive prefix sum of the log-decays, fp64
-      double G = lane < n ? (double)__ldg(j.g + tok0 + t0 + lane) : 0.0;
+      double Gs = lane < n ? (double)graw[lane] : 0.0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, G, o);
-        if (lane >= o) G += y;
+        const double y = __shfl_up_sync(0xffffffffu, Gs, o);
+        if (lane >= o) Gs += y;
       }
-      G += gsum;
+      Gs += gsum;
       // Reference moves: the first token whose sum is more than kRescaleLog
       // from the reference rescales the state before its update and becomes
       // the reference; tokens before it keep the old one.
@@ -143,12 +183,12 @@ __global__ void __launch_bounds__(kLocalThreads) local_pass_kernel(const LocalPa
       bool done = lane >= n;
       float fac = 1.0f, inv = 1.0f;
       for (;;) {
-        const unsigned far = __ballot_sync(0xffffffffu, !done && fabs(G - ref) > kRescaleLog);
+        const unsigned far = __ballot_sync(0xffffffffu, !done && fabs(Gs - ref) > kRescaleLog);
         if (!far) break;
         const int f = __ffs(far) - 1;
-        const double Gf = __shfl_sync(0xffffffffu, G, f);
+        const double Gf = __shfl_sync(0xffffffffu, Gs, f);
         if (!done && lane < f) {
-          inv = exp_split(ref - G);
+          inv = exp_split(ref - Gs);
           done = true;
         }
         if (lane == f) {
@@ -158,20 +198,24 @@ __global__ void __launch_bounds__(kLocalThreads) local_pass_kernel(const LocalPa
         }
         ref = Gf;
       }
-      if (!done) inv = exp_split(ref - G);
+      if (!done) inv = exp_split(ref - Gs);
       if (lane < n) {
-        bs[lane] = __ldg(j.beta + tok0 + t0 + lane);
+        bs[lane] = braw[lane];
         inv_s[lane] = inv;
         fac_s[lane] = fac;
       }
-      if (lane == n - 1) s_end[0] = exp_split(G - ref);
-      gsum = __shfl_sync(0xffffffffu, G, n - 1);
+      if (lane == n - 1) s_end[0] = exp_split(Gs - ref);
+      gsum = __shfl_sync(0xffffffffu, Gs, n - 1);
       gref = ref;
     }
-    __syncthreads();
+    __syncthreads();  // the widened tile is ready and the raw buffers are free
+    if (t0 + kTT < L) issue_tile(j, tok0 + t0 + kTT, min(kTT, L - t0 - kTT), need_v, kraw, vraw, braw, graw);
 
-    for (int i = 0; i < n; ++i) {
-      const float fac = fac_s[i];
+    // Token i's update and token i + 1's dot products share one pass over the
+    // registers: d_{i+1} = k_{i+1}^T (Yhat + k_i c_i^T).
+    float d0, d1;
+    {
+      const float fac = fac_s[0];
       if (fac != 1.0f) {  // same for every thread of the CTA
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -179,26 +223,25 @@ __global__ void __launch_bounds__(kLocalThreads) local_pass_kernel(const LocalPa
           y1[r] *= fac;
         }
       }
-      const float* kr = ks + i * K + row0;
-      float d0a = 0.f, d0b = 0.f, d1a = 0.f, d1b = 0.f;
+      const float* kn = ks + row0;
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
 #pragma unroll
       for (int r = 0; r < R; r += 4) {
-        const float4 kk = *reinterpret_cast<const float4*>(kr + r);
-        d0a = fmaf(kk.x, y0[r], d0a);
-        d1a = fmaf(kk.x, y1[r], d1a);
-        d0b = fmaf(kk.y, y0[r + 1], d0b);
-        d1b = fmaf(kk.y, y1[r + 1], d1b);
-        d0a = fmaf(kk.z, y0[r + 2], d0a);
-        d1a = fmaf(kk.z, y1[r + 2], d1a);
-        d0b = fmaf(kk.w, y0[r + 3], d0b);
-        d1b = fmaf(kk.w, y1[r + 3], d1b);
+        const float4 kk = *reinterpret_cast<const float4*>(kn + r);
+        a0 = fmaf(kk.x, y0[r], a0);
+        b0 = fmaf(kk.x, y1[r], b0);
+        a1 = fmaf(kk.y, y0[r + 1], a1);
+        b1 = fmaf(kk.y, y1[r + 1], b1);
+        a2 = fmaf(kk.z, y0[r + 2], a2);
+        b2 = fmaf(kk.z, y1[r + 2], b2);
+        a3 = fmaf(kk.w, y0[r + 3], a3);
+        b3 = fmaf(kk.w, y1[r + 3], b3);
       }
-      float d0 = d0a + d0b, d1 = d1a + d1b;
-#pragma unroll
-      for (int m = CW; m < 32; m <<= 1) {
-        d0 += __shfl_xor_sync(0xffffffffu, d0, m);
-        d1 += __shfl_xor_sync(0xffffffffu, d1, m);
-      }
+      d0 = (a0 + a1) + (a2 + a3);
+      d1 = (b0 + b1) + (b2 + b3);
+      reduce_parts<CW>(d0, d1);
+    }
+    for (int i = 0; i < n; ++i) {
       float v0 = 0.f, v1 = 0.f;
       if (is_h && live) {
         const float2 vv = *reinterpret_cast<const float2*>(vs + i * V + gc);
@@ -208,17 +251,57 @@ __global__ void __launch_bounds__(kLocalThreads) local_pass_kernel(const LocalPa
       const float b = bs[i], inv = inv_s[i];
       const float c0 = b * fmaf(v0, inv, -d0);
       const float c1 = b * fmaf(v1, inv, -d1);
+      const float* kc = ks + i * K + row0;
+      if (i + 1 < n) {
+        const float* kn = kc + K;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
 #pragma unroll
-      for (int r = 0; r < R; r += 4) {
-        const float4 kk = *reinterpret_cast<const float4*>(kr + r);
-        y0[r] = fmaf(kk.x, c0, y0[r]);
-        y1[r] = fmaf(kk.x, c1, y1[r]);
-        y0[r + 1] = fmaf(kk.y, c0, y0[r + 1]);
-        y1[r + 1] = fmaf(kk.y, c1, y1[r + 1]);
-        y0[r + 2] = fmaf(kk.z, c0, y0[r + 2]);
-        y1[r + 2] = fmaf(kk.z, c1, y1[r + 2]);
-        y0[r + 3] = fmaf(kk.w, c0, y0[r + 3]);
-        y1[r + 3] = fmaf(kk.w, c1, y1[r + 3]);
+        for (int r = 0; r < R; r += 4) {
+          const float4 kk = *reinterpret_cast<const float4*>(kc + r);
+          const float4 kq = *reinterpret_cast<const float4*>(kn + r);
+          y0[r] = fmaf(kk.x, c0, y0[r]);
+          y1[r] = fmaf(kk.x, c1, y1[r]);
+          y0[r + 1] = fmaf(kk.y, c0, y0[r + 1]);
+          y1[r + 1] = fmaf(kk.y, c1, y1[r + 1]);
+          y0[r + 2] = fmaf(kk.z, c0, y0[r + 2]);
+          y1[r + 2] = fmaf(kk.z, c1, y1[r + 2]);
+          y0[r + 3] = fmaf(kk.w, c0, y0[r + 3]);
+          y1[r + 3] = fmaf(kk.w, c1, y1[r + 3]);
+          a0 = fmaf(kq.x, y0[r], a0);
+          b0 = fmaf(kq.x, y1[r], b0);
+          a1 = fmaf(kq.y, y0[r + 1], a1);
+          b1 = fmaf(kq.y, y1[r + 1], b1);
+          a2 = fmaf(kq.z, y0[r + 2], a2);
+          b2 = fmaf(kq.z, y1[r + 2], b2);
+          a3 = fmaf(kq.w, y0[r + 3], a3);
+          b3 = fmaf(kq.w, y1[r + 3], b3);
+        }
+        d0 = (a0 + a1) + (a2 + a3);
+        d1 = (b0 + b1) + (b2 + b3);
+        reduce_parts<CW>(d0, d1);
+        const float fac = fac_s[i + 1];
+        if (fac != 1.0f) {  // rescale before token i + 1: its dot products scale alike
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            y0[r] *= fac;
+            y1[r] *= fac;
+          }
+          d0 *= fac;
+          d1 *= fac;
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < R; r += 4) {
+          const float4 kk = *reinterpret_cast<const float4*>(kc + r);
+          y0[r] = fmaf(kk.x, c0, y0[r]);
+          y1[r] = fmaf(kk.x, c1, y1[r]);
+          y0[r + 1] = fmaf(kk.y, c0, y0[r + 1]);
+          y1[r + 1] = fmaf(kk.y, c1, y1[r + 1]);
+          y0[r + 2] = fmaf(kk.z, c0, y0[r + 2]);
+          y1[r + 2] = fmaf(kk.z, c1, y1[r + 2]);
+          y0[r + 3] = fmaf(kk.w, c0, y0[r + 3]);
+          y1[r + 3] = fmaf(kk.w, c1, y1[r + 3]);
+        }
       }
     }
   }
@@ -263,7 +346,9 @@ cudaError_t launch_rg(const LocalJob& j, cudaStream_t stream) {
     grid.y = 65535u;
     grid.z = (unsigned)((units + 65534) / 65535);
   }
-  const size_t smem = sizeof(float) * (size_t)(kTT * (j.K + j.V) + 3 * kTT + 4);
+  // fp32 tile, per-token scalars, raw next tile (bf16 keys and values, fp32 scalars)
+  const size_t smem = sizeof(float) * (size_t)(kTT * (j.K + j.V) + 3 * kTT + 4 + 2 * kTT) +
+                      sizeof(uint16_t) * (size_t)kTT * (j.K + j.V);
   cudaError_t e = cudaFuncSetAttribute(local_pass_kernel<R, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
