@@ -39,6 +39,11 @@ WORKLOAD = ("CP state correction, B=1, 32 heads, K=V=128, S=8 (32K tokens / 4K p
             "step = fwd kv + fwd vk (Householder M) + rev kv + rev vk (0.99*orthogonal M)")
 
 
+# GB300's nominal HBM3e bandwidth, for the fraction against the datasheet figure
+# beside the one against the measured copy bandwidth.
+NOMINAL_HBM_GBS = 8000.0
+
+
 def algorithmic_bytes(chains, S_, K_, V_, with_init=True):
     """Bytes one call must move: H and M of the S-1 segments it visits, every
     output state, and h_init."""
@@ -436,6 +441,7 @@ def run_ours(args):
                        "parallelism": f"replicas x{world} (no collective)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4),
+                         "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4), "nominal_peak": NOMINAL_HBM_GBS,
                          "traffic": args.traffic if args.traffic is not None else (kernel_traffic() if eng == "tc" else None),
                          "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                                         if peak_kind == "measured" else "fallback 6.8 TB/s",
@@ -756,6 +762,103 @@ def run_large(args):
               flush=True)
 
 
+def local_flops(chains, T, K_, V_):
+    """FFMA flops of the local pass: per token and column of [H | M], a dot
+    product and an update over the K rows."""
+    return 4 * chains * T * K_ * (K_ + V_)
+
+
+def run_local(args):
+    """The per-segment local pass that produces (H_i, M_i) from token-level
+    inputs (gated delta rule), on 32 heads x 32K tokens in 8 segments of 4K,
+    K = V = 128: its time against the FFMA ceiling, then the local pass and the
+    forward correction chained on one stream (the correction launched as a
+    programmatic dependent), replayed in a CUDA graph.  The inputs (537 MB of
+    bf16 keys and values) exceed L2.  One head of the outputs is checked
+    against the fp64 oracle.  One JSON line; not the headline metric."""
+    import numpy as np
+    import torch
+
+    import linear_attention_context_gb300 as qla
+    import oracle
+    import qla_inputs as qi
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream(dev)
+    c = qi.LOCAL_WORKLOADS["l1"]
+    k, v, b, g = qi.make_local_inputs(c)
+    dk, dv, db, dg = (torch.from_numpy(np.ascontiguousarray(a)).to(dev) for a in (k, v, b, g))
+    H = torch.empty((c.B, c.heads, c.S, c.K, c.V), device=dev)
+    M = torch.empty((c.B, c.heads, c.S, c.K, c.K), device=dev)
+    out = torch.empty_like(H)
+    h0 = torch.zeros((c.B, c.heads, c.K, c.V), device=dev)
+    peaks = compute_peaks(dev) if not args.skip_peaks else None
+    ffma = peaks["ffma_tflops"] if peaks else 80.5
+
+    def timed(fn, reps):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                fn()
+        stream.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                gr.replay()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                gr.replay()
+            e1.record(stream)
+        stream.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    def local():
+        qla.local_pass(dk, dv, db, dg, c.S, H, M, stream=stream)
+
+    def chained():
+        qla.local_pass(dk, dv, db, dg, c.S, H, M, stream=stream)
+        qla.cp_correct(H, M, h0, out, variant="seq", stream=stream)
+
+    us_local = timed(local, args.sweep_reps)
+    qla.set_dependent_launch(True)
+    try:
+        us_pair = timed(chained, args.sweep_reps)
+    finally:
+        qla.set_dependent_launch(False)
+    # check one head of H, M and the corrected states against the oracle
+    sl = (slice(0, 1), slice(0, 1))
+    Hr, Mr = oracle.local_pass(k[sl], v[sl], b[sl], g[sl], c.S)
+    ref, _ = oracle.cp_correct(Hr.astype(np.float32), Mr.astype(np.float32), np.zeros((1, 1, c.K, c.V), np.float32),
+                               "kv", "fwd")
+    err = {}
+    for name, got, r in (("H", H, Hr), ("M", M, Mr), ("out", out, ref)):
+        gg = got[0:1, 0:1].cpu().numpy().astype(np.float64)
+        d = (gg - r).reshape(c.S, -1)
+        err[name] = float(np.max(np.linalg.norm(d, axis=1) / np.maximum(np.linalg.norm(r.reshape(c.S, -1), axis=1),
+                                                                           1e-300)))
+    if max(err.values()) > 1e-5:
+        raise SystemExit(f"local pass outside the parity bar: {err}")
+    flops = local_flops(c.chains, c.T, c.K, c.V)
+    rate = flops / (us_local * 1e-6) / 1e12
+    line = {"local_pass": {"workload": f"B=1, {c.heads} heads, {c.T} tokens in {c.S} segments of {c.L}, "
+                                       f"K=V={c.K}, bf16 keys/values, fp32 states", "layout": "kv"},
+            "us_per_call": round(us_local, 1),
+            "roofline": {"bound": "alu", "achieved": round(rate, 2), "peak": ffma, "unit": "TFLOP/s",
+                         "frac": round(rate / ffma, 4), "flops_per_call": flops,
+                         "peak_source": "FFMA: SMs x 128 FMA/clk x 2 x max SM clock"},
+            "chained_with_correction_us": round(us_pair, 1),
+            "correction_share_us": round(us_pair - us_local, 1),
+            "max_rel_l2_one_head": {k_: float(f"{v_:.3e}") for k_, v_ in err.items()},
+            "input_bytes": int(k.nbytes + v.nbytes + b.nbytes + g.nbytes)}
+    print(json.dumps(line), flush=True)
+    if qla.device_status() != 0:
+        raise SystemExit("device status word set during the local-pass timings")
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -778,6 +881,7 @@ def main():
     ap.add_argument("--large", action="store_true", help="time the 4 x 64-head K=V=256 S=32 workload")
     ap.add_argument("--varlen", action="store_true", help="time variable-length calls, sequential vs scan")
     ap.add_argument("--configs", action="store_true", help="time configs 0-2 one at a time")
+    ap.add_argument("--local", action="store_true", help="time the per-segment local pass and its chain into the correction")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -787,6 +891,8 @@ def main():
         run_large(args)
     elif args.varlen:
         run_varlen(args)
+    elif args.local:
+        run_local(args)
     elif args.configs:
         run_configs(args)
     else:
