@@ -859,6 +859,60 @@ def run_local(args):
         raise SystemExit("device status word set during the local-pass timings")
 
 
+def run_accuracy(args):
+    """Worst per-state error against the fp64 oracle, config by config, with
+    the library's automatic choices (configs 0-3 in full; config 4 at its
+    sweep points, both layouts and directions).  One JSON line per case."""
+    import numpy as np
+    import torch
+
+    import linear_attention_context_gb300 as qla
+    import oracle
+    import qla_inputs as qi
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+
+    def worst(got, ref):
+        g = got.reshape(-1, got.shape[-2] * got.shape[-1]).astype(np.float64)
+        r = ref.reshape(g.shape)
+        d = g - r
+        rel = np.linalg.norm(d, axis=1) / np.maximum(np.linalg.norm(r, axis=1), 1e-300)
+        rmax = np.abs(d).max(axis=1) / np.maximum(np.abs(r).max(axis=1), 1e-300)
+        return float(rel.max()), float(rmax.max())
+
+    def case(name, c, layout, direction):
+        H, M, h0 = qi.make_inputs(c, layout)
+        Hd, Md = torch.from_numpy(H).to(dev), torch.from_numpy(M).to(dev)
+        h0d = None if h0 is None else torch.from_numpy(h0).to(dev)
+        out = qla.cp_correct(Hd, Md, h0d, layout=layout, direction=direction)
+        torch.cuda.synchronize()
+        got = out.cpu().numpy()
+        del out, Hd, Md
+        rel = rmax = 0.0
+        n = c.chains
+        flat = lambda a: a.reshape((1, n) + a.shape[2:])  # noqa: E731
+        for c0 in range(0, n, 32):  # the oracle in blocks of chains
+            sl = (slice(None), slice(c0, min(n, c0 + 32)))
+            ref, _ = oracle.cp_correct(flat(H)[sl], flat(M)[sl], None if h0 is None else flat(h0)[sl], layout,
+                                       direction)
+            a, b = worst(flat(got)[sl], ref)
+            rel, rmax = max(rel, a), max(rmax, b)
+        v, e = qla.resolve(c.B, c.heads, c.S, c.K, c.V, layout)
+        print(json.dumps({"accuracy": name, "B": c.B, "heads": c.heads, "K": c.K, "V": c.V, "S": c.S,
+                          "layout": layout, "direction": direction, "variant": v, "engine": e,
+                          "worst_rel_l2": float(f"{rel:.3e}"), "worst_rel_max": float(f"{rmax:.3e}")}), flush=True)
+
+    for name, combos in (("c0", [("kv", "fwd")]), ("c1", [("kv", "fwd"), ("vk", "fwd")]),
+                         ("c2", [("kv", "rev"), ("vk", "rev")]), ("c3", [("kv", "fwd"), ("kv", "rev")])):
+        for layout, direction in combos:
+            case(name, qi.WORKLOADS[name], layout, direction)
+    for heads in qi.SWEEP_HEADS:
+        for S_ in qi.SWEEP_S:
+            for layout in ("kv", "vk"):
+                for direction in ("fwd", "rev"):
+                    case("c4", qi.sweep_case(heads, S_), layout, direction)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -882,6 +936,7 @@ def main():
     ap.add_argument("--varlen", action="store_true", help="time variable-length calls, sequential vs scan")
     ap.add_argument("--configs", action="store_true", help="time configs 0-2 one at a time")
     ap.add_argument("--local", action="store_true", help="time the per-segment local pass and its chain into the correction")
+    ap.add_argument("--accuracy", action="store_true", help="worst per-state error against the oracle, per config")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -893,6 +948,8 @@ def main():
         run_varlen(args)
     elif args.local:
         run_local(args)
+    elif args.accuracy:
+        run_accuracy(args)
     elif args.configs:
         run_configs(args)
     else:

@@ -91,13 +91,12 @@ enum {
 enum {
   QLA_ENGINE_AUTO = 0,    /* 3xTF32 engine where the shape and chain length allow, else SIMT */
   QLA_ENGINE_SIMT = 1,    /* plain FFMA kernel, no TMA: any supported K, V */
-  QLA_ENGINE_TC_F16 = 2,  /* the same pipeline with tcgen05 kind::f16 MMAs on power-of-two-scaled
-                             fp16 hi/lo operand pairs (22 significant bits, as 3xTF32): K = 128 only */
+  /* (value 2 is not used: it is rejected with QLA_ERR_INVALID_ARG) */
   QLA_ENGINE_TC = 3       /* warp-specialised TMA/mbarrier pipeline, tcgen05 3xTF32 propagate */
 };
 /* Accuracy on long chains and the automatic engine choice.  The tensor core
  * accumulates in fp32 rounding toward zero, so with norm-preserving M (no
- * decay) the two tensor-core engines shrink the state coherently, about 4.4e-8
+ * decay) the tensor-core engine shrinks the state coherently, about 4.4e-8
  * of its norm per step at K = 128 and 1.4e-7 at K = 256: the worst per-state
  * relative L2 error passes 1e-5 near 200 steps (K = 128) and 64 steps
  * (K = 256).  QLA_ENGINE_AUTO therefore takes the 3xTF32 engine only for
@@ -245,9 +244,9 @@ QLA_API const char* qla_last_error(void);
 QLA_API int qla_device_status(int* flags);
 
 /*
- * Self-test of the bounded waits: launches a warp-specialised pipeline
- * (engine QLA_ENGINE_TC or QLA_ENGINE_TC_F16; any other value is
- * QLA_ERR_INVALID_ARG) on a tiny problem in a mode where one consumer waits
+ * Self-test of the bounded waits: launches the warp-specialised pipeline
+ * (engine QLA_ENGINE_TC; any other value is QLA_ERR_INVALID_ARG) on a tiny
+ * problem in a mode where one consumer waits
  * on a barrier that nothing arrives on.  The wait gives up after
  * `wait_limit_us` microseconds, the kernel records QLA_ERR_TIMEOUT in the
  * device status word, drains and returns.  The buffers are as for

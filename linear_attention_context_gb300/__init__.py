@@ -23,7 +23,7 @@ from . import _build
 LAYOUTS = {"kv": 0, "vk": 1}
 DIRECTIONS = {"fwd": 0, "rev": 1}
 VARIANTS = {"auto": 0, "seq": 1, "scan": 2}
-ENGINES = {"auto": 0, "simt": 1, "tc_f16": 2, "tc": 3}
+ENGINES = {"auto": 0, "simt": 1, "tc": 3}
 RELEASES = {"membar": 0, "proxy": 1, "delay": 2, "none": 3}
 
 QLA_OK = 0

@@ -202,8 +202,7 @@ int auto_groups(int S) {
 }
 
 bool known_engine(int engine) {
-  return engine == QLA_ENGINE_AUTO || engine == QLA_ENGINE_SIMT || engine == QLA_ENGINE_TC ||
-         engine == QLA_ENGINE_TC_F16;
+  return engine == QLA_ENGINE_AUTO || engine == QLA_ENGINE_SIMT || engine == QLA_ENGINE_TC;
 }
 
 // Longest chain the automatic choice gives to the tensor-core engine.  The
@@ -225,7 +224,6 @@ int resolve_engine(const Shape& s, int engine) {
 
 // The engine a scan phase runs on: phase 1a's V' = K may differ from V.
 int engine_for(const SeqJob& j, int engine) {
-  if (engine == QLA_ENGINE_TC_F16 && !tc_f16_supports(j.K, j.V)) engine = QLA_ENGINE_TC;
   if (engine == QLA_ENGINE_TC && !tc_supports(j.K, j.V)) return QLA_ENGINE_SIMT;
   return engine;
 }
@@ -299,11 +297,6 @@ int launch_seq(const SeqJob& job, int engine, int release, const DeviceInfo* d, 
       if (!tc_supports(j.K, j.V))
         return fail(QLA_ERR_UNSUPPORTED, "the tensor-core engine takes K in {128, 256} (got K=%d, V=%d)", j.K, j.V);
       e = launch_seq_tc(j, release, d->status_word, kWaitLimitNs, 0, stream);
-      break;
-    case QLA_ENGINE_TC_F16:
-      if (!tc_f16_supports(j.K, j.V))
-        return fail(QLA_ERR_UNSUPPORTED, "the fp16-pair tensor-core engine takes K = 128 (got K=%d, V=%d)", j.K, j.V);
-      e = launch_seq_tc_f16(j, release, d->status_word, kWaitLimitNs, 0, stream);
       break;
     default:
       return fail(QLA_ERR_UNSUPPORTED, "engine %d is not available in this build", engine);
@@ -787,16 +780,15 @@ int qla_selftest_stalled_wait(const float* H, const float* M, float* out, int S,
   if (S < 2) return fail(QLA_ERR_INVALID_ARG, "the stalled-wait self-test needs S >= 2");
   if (wait_limit_us < 1 || wait_limit_us > 10000000)
     return fail(QLA_ERR_INVALID_ARG, "wait_limit_us must be in [1, 10^7]");
-  if (engine != QLA_ENGINE_TC && engine != QLA_ENGINE_TC_F16)
-    return fail(QLA_ERR_INVALID_ARG, "the stalled-wait self-test takes a pipelined engine (got %d)", engine);
+  if (engine != QLA_ENGINE_TC)
+    return fail(QLA_ERR_INVALID_ARG, "the stalled-wait self-test takes the pipelined engine (got %d)", engine);
   DeviceInfo* d = nullptr;
   if ((st = current_device(&d)) != QLA_OK) return st;
   const uint64_t limit = (uint64_t)wait_limit_us * 1000ull;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   SeqJob j = plain_job(H, M, nullptr, out, nullptr, s);
   j.status = d->status_word;
-  cudaError_t e = engine == QLA_ENGINE_TC ? launch_seq_tc(j, QLA_RELEASE_MEMBAR, d->status_word, limit, 1, cs)
-                                          : launch_seq_tc_f16(j, QLA_RELEASE_MEMBAR, d->status_word, limit, 1, cs);
+  cudaError_t e = launch_seq_tc(j, QLA_RELEASE_MEMBAR, d->status_word, limit, 1, cs);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return QLA_OK;
 }

@@ -224,24 +224,6 @@ __device__ __forceinline__ void mma_tf32_ts_c(uint32_t d_tmem, uint32_t a_tmem, 
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem descriptor], kind::f16 (A and B fp16, D fp32),
-// one CTA; descriptor in two 32-bit halves, accumulate flag a compile-time
-// constant.
-template <bool ACC>
-__device__ __forceinline__ void mma_f16_ts_c(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
-                                             uint32_t idesc) {
-  asm volatile(
-      "{\n"
-      " .reg .pred p;\n"
-      " .reg .b64 bd;\n"
-      " setp.ne.b32 p, %5, 0;\n"
-      " mov.b64 bd, {%2, %3};\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n"
-      "}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(ACC ? 1 : 0)
-      : "memory");
-}
-
 // 16-byte shared store at a 32-bit shared address plus a compile-time offset.
 template <uint32_t OFF>
 __device__ __forceinline__ void sts128(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -360,29 +342,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)2 << 61;
   return d;
-}
-
-// Shared-memory matrix descriptor for an MN-major 16-bit operand in the
-// 64-byte swizzle layout: each k row holds 32 consecutive N elements (64
-// bytes), rows 64 B apart, 8-row (512-byte) atoms with the 16-byte pieces of
-// row r exchanged by (r / 2) % 4.  An operand of N = 32 is one atom wide, so
-// the only stride used is the one between 8-row groups along k; `lbo` and
-// `sbo` both carry it.  [61,64) layout 4 = 64-byte swizzle.
-__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)4 << 61;
-  return d;
-}
-
-// Instruction descriptor, kind::f16: D fp32 (bits [4,6) = 1), A and B fp16
-// (format 0 at [7,10) and [10,13)), A K-major, B K-major or MN-major (bit 16),
-// N >> 3 at bits [17,23), M >> 4 at bits [24,29).
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (b_mn_major ? (1u << 16) : 0u) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Instruction descriptor, kind::tf32: D fp32 (bits [4,6) = 1), A and B tf32

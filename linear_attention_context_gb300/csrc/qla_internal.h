@@ -138,13 +138,6 @@ bool tc_supports(int K, int V);
 cudaError_t launch_seq_tc(const SeqJob& job, int release, unsigned int* status, uint64_t limit_ns,
                           int stall_test, cudaStream_t stream);
 
-// seq_tc_f16.cu: the same pipeline with kind::f16 MMAs on power-of-two-scaled
-// fp16 hi/lo operand pairs.  K = 128, V a multiple of 32; other arguments as
-// launch_seq_tc.
-bool tc_f16_supports(int K, int V);
-cudaError_t launch_seq_tc_f16(const SeqJob& job, int release, unsigned int* status, uint64_t limit_ns,
-                              int stall_test, cudaStream_t stream);
-
 // One launch of the per-segment local pass (local_simt.cu): for every chain
 // and segment of L = T / S tokens, H = the segment's gated-delta-rule state
 // from zero and M = the product of its token transitions.

@@ -6,9 +6,9 @@ import os
 
 import numpy as np
 
-# Engines under test.  The tensor-core engines take the shapes listed in
-# tc_supports() / tc_f16_supports(); the FFMA engine takes every supported shape.
-BUILT_ENGINES = ("simt", "tc", "tc_f16")
+# Engines under test.  The tensor-core engine takes the shapes listed in
+# tc_supports(); the FFMA engine takes every supported shape.
+BUILT_ENGINES = ("simt", "tc")
 
 
 def engines_under_test():
@@ -21,8 +21,6 @@ def engines_under_test():
 def engine_supports(engine, K, V):
     if engine == "tc":
         return K in (128, 256) and V % 32 == 0
-    if engine == "tc_f16":
-        return K == 128 and V % 32 == 0
     return True
 
 

@@ -68,7 +68,8 @@ def call(L, H=FAKE, M=FAKE + (1 << 32), h0=None, out=FAKE + (2 << 32), fin=None,
     (dict(H=None), -1), (dict(M=None), -1), (dict(out=None), -1),
     (dict(B=0), -1), (dict(heads=-1), -1), (dict(S=0), -1), (dict(K=0), -1),
     (dict(layout=2), -1), (dict(direction=-1), -1),
-    (dict(variant=3), -1), (dict(engine=9), -1), (dict(engine=4), -1), (dict(release=7), -1), (dict(group=-1), -1),
+    (dict(variant=3), -1), (dict(engine=9), -1), (dict(engine=4), -1), (dict(engine=2), -1), (dict(release=7), -1),
+    (dict(group=-1), -1),
     (dict(K=48), -2), (dict(V=288), -2), (dict(K=16), -2), (dict(V=100), -2),
     # one CTA per (chain, segment group, 32-column tile) must fit a 2^31 - 1 grid
     (dict(B=1 << 16, heads=1 << 10, S=16), -2),
@@ -153,6 +154,7 @@ def test_stalled_wait_selftest_argument_checks(L):
     H, M, out = vp(FAKE), vp(FAKE + (1 << 32)), vp(FAKE + (2 << 32))
     assert L.qla_selftest_stalled_wait(H, M, out, 3, 1000, 1, None) == -1    # FFMA engine has no pipeline
     assert L.qla_selftest_stalled_wait(H, M, out, 3, 1000, 0, None) == -1    # automatic choice is not an engine
+    assert L.qla_selftest_stalled_wait(H, M, out, 3, 1000, 2, None) == -1    # no engine 2
     assert L.qla_selftest_stalled_wait(H, M, out, 1, 1000, 3, None) == -1    # needs S >= 2
     assert L.qla_selftest_stalled_wait(H, M, out, 3, 0, 3, None) == -1       # limit outside [1, 10^7]
 
