@@ -40,6 +40,11 @@ __device__ __forceinline__ void cp_async4(float* dst, const float* src) {
                "l"(src)
                : "memory");
 }
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -275,6 +280,209 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
   if (j.fin) store_block(j.fin + u * j.fin_unit_stride, x);
 }
 
+// ---------------------------------------------------------------- k-split form (K <= 128)
+//
+// The same recurrence with the contraction split four ways: 2K threads in
+// four k-groups of K/2; a thread of k-group g computes an 8-row x 8-column
+// block of sum over k in [g K/4, (g+1) K/4) of A[m][k] X[k][v], so every value
+// it reads from shared memory feeds four FMAs (the R x 4 tiles above feed two;
+// at K = 128 those make the shared-memory reads, not the FMAs, the bound).
+// The four partial blocks meet in shared memory once per step, where the
+// thread that owns an output (a row and 16 columns) adds them and H.  A step's
+// whole A (K x K, k-major) is copied in with cp.async during the step before.
+constexpr int kKG = 4;          // k-groups
+constexpr int kPld = kTileV + 4;  // padded row of a partial block and of the state tile
+
+template <int K>
+__host__ __device__ constexpr int ks_threads() {
+  return 2 * K;
+}
+template <int K>
+__host__ __device__ constexpr int ks_ald() {
+  return K + 4;  // padded row (one k) of the A copy
+}
+template <int K>
+__host__ __device__ constexpr size_t ks_smem_floats() {
+  // state tile [K][kPld] + two A copies [K][K + 4] + partials [kKG][K][kPld]
+  return (size_t)K * kPld + 2 * (size_t)K * ks_ald<K>() + (size_t)kKG * K * kPld;
+}
+
+template <int K, int LAYOUT>
+__global__ void __launch_bounds__(2 * K) seq_simt_ksplit_kernel(const SeqJob j) {
+  constexpr int NT = ks_threads<K>();
+  constexpr int KR = K / kKG;    // k per group
+  constexpr int AL = ks_ald<K>();
+  extern __shared__ __align__(16) float smem[];
+  float* Xs = smem;                      // [K][kPld]   state tile, kv view
+  float* As0 = Xs + K * kPld;            // [2][K][AL]  A copies, As[k][m] = A[m][k]
+  float* Ps = As0 + 2 * K * AL;          // [kKG][K][kPld] partial blocks
+
+  const int t = threadIdx.x;
+  const int kg = t / (K / 2);            // k-group
+  const int w = t - kg * (K / 2);
+  const int rb = w >> 2, cb = w & 3;     // 8-row block, 8-column block
+  // owner of outputs: one row and 16 columns (kv: lanes pair up along a row;
+  // vk: lanes run down a column, so global accesses are runs along k)
+  const int orow = LAYOUT == 0 ? (t >> 1) : (t % K);
+  const int oc0 = LAYOUT == 0 ? (t & 1) * 16 : (t / K) * 16;
+  const int V = j.V;
+  int u, tile;
+  if (!unit_and_tile(j, u, tile)) return;
+  const int vt = tile * kTileV;          // the tile's first column
+  const int chain = u / j.G;
+  const int g = u - chain * j.G;
+  int64_t cbase;
+  int S;
+  griddep_wait();  // (before the first global access: the offsets may be the previous kernel's output)
+  if (!chain_span(j, chain, cbase, S)) return;
+  const int s_lo = g * j.L;
+  const int n = min(j.L, S - s_lo);
+  const int64_t st = (int64_t)K * V;
+  const bool fwd = j.direction == 0;
+  const float* Hc = j.H ? j.H + cbase * st : nullptr;
+  float* Oc = j.out ? j.out + cbase * st : nullptr;
+  const float* Mc = j.M + cbase * K * K;
+
+  // this thread's owned outputs of a [K][V] (kv) or [V][K] (vk) state
+  auto load_own = [&](const float* src, float (&b)[16]) {
+    if (LAYOUT == 0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = *reinterpret_cast<const float4*>(src + (int64_t)orow * V + vt + oc0 + 4 * q);
+        b[4 * q] = v.x; b[4 * q + 1] = v.y; b[4 * q + 2] = v.z; b[4 * q + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) b[c] = src[(int64_t)(vt + oc0 + c) * K + orow];
+    }
+  };
+  auto store_own = [&](float* dst, const float (&b)[16]) {
+    if (LAYOUT == 0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<float4*>(dst + (int64_t)orow * V + vt + oc0 + 4 * q) =
+            make_float4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) dst[(int64_t)(vt + oc0 + c) * K + orow] = b[c];
+    }
+  };
+  auto put_state = [&](const float (&b)[16]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<float4*>(Xs + orow * kPld + oc0 + 4 * q) =
+          make_float4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
+  };
+
+  float x[16];
+  if (j.init_mode == kInitPointer) {
+    load_own(j.init + u * j.init_unit_stride, x);
+  } else {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) x[c] = (j.init_mode == kInitIdentity && orow == vt + oc0 + c) ? 1.f : 0.f;
+  }
+  const int nsteps = n - 1 + (j.fin ? 1 : 0);
+  auto seg_of = [&](int jj) { return fwd ? s_lo + jj : s_lo + n - 1 - jj; };
+  // A of step jj into copy jj & 1 as [k][m]: reverse A = M^T, so As[k][m] =
+  // M[k][m] (16-byte copies of M's rows); forward A = M, As[k][m] = M[m][k],
+  // transposed on the way in with 4-byte copies (a warp takes 8 k x 4 m, so
+  // it reads 32-byte runs of M's rows and its shared writes spread over banks).
+  auto issue_a = [&](int jj) {
+    const float* Ms = Mc + (int64_t)seg_of(jj) * K * K;
+    float* dst = As0 + (jj & 1) * K * AL;
+    if (fwd) {
+      for (int e = t; e < K * K; e += NT) {
+        const int k = (e & 7) + 8 * ((e >> 5) % (K / 8)), m = ((e >> 3) & 3) + 4 * (e / (4 * K));
+        cp_async4(dst + k * AL + m, Ms + (int64_t)m * K + k);
+      }
+    } else {
+      for (int e = t; e < K * K / 4; e += NT) {
+        const int k = e / (K / 4), m4 = e - k * (K / 4);
+        cp_async16(dst + k * AL + 4 * m4, Ms + (int64_t)k * K + 4 * m4);
+      }
+    }
+    cp_async_commit();
+  };
+  if (nsteps > 0) issue_a(0);
+
+  for (int jj = 0; jj < n; ++jj) {
+    const int seg = seg_of(jj);
+    const bool do_step = jj < nsteps;
+    // In place (out == H): each thread reads its H_seg elements before it
+    // writes out[seg] over the same addresses; no other thread touches them.
+    float h[16];
+    if (do_step && Hc) {
+      load_own(Hc + seg * st, h);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) h[c] = 0.f;
+    }
+    if (Oc) store_own(Oc + seg * st, x);
+    if (!do_step) break;
+    put_state(x);
+    cp_async_wait<0>();  // this thread's copies of step jj's A have landed
+    __syncthreads();     // everyone's, and the state tile is written; step jj-1 is done with copy (jj+1)&1
+    if (jj + 1 < nsteps) issue_a(jj + 1);
+
+    float acc[8][8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+    const float* A = As0 + (jj & 1) * K * AL + kg * KR * AL + rb * 8;
+    const float* X = Xs + kg * KR * kPld + cb * 8;
+#pragma unroll 4
+    for (int k = 0; k < KR; ++k) {
+      const float4 a0 = *reinterpret_cast<const float4*>(A + k * AL);
+      const float4 a1 = *reinterpret_cast<const float4*>(A + k * AL + 4);
+      const float4 x0 = *reinterpret_cast<const float4*>(X + k * kPld);
+      const float4 x1 = *reinterpret_cast<const float4*>(X + k * kPld + 4);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av[r], xv[c], acc[r][c]);
+    }
+    // partial blocks -> shared memory; the owners add them (k-groups in order) and H
+    float* P = Ps + kg * K * kPld + (rb * 8) * kPld + cb * 8;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      *reinterpret_cast<float4*>(P + r * kPld) = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+      *reinterpret_cast<float4*>(P + r * kPld + 4) = make_float4(acc[r][4], acc[r][5], acc[r][6], acc[r][7]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float4 sum = *reinterpret_cast<const float4*>(Ps + orow * kPld + oc0 + 4 * q);
+#pragma unroll
+      for (int gg = 1; gg < kKG; ++gg) {
+        const float4 p = *reinterpret_cast<const float4*>(Ps + gg * K * kPld + orow * kPld + oc0 + 4 * q);
+        sum.x += p.x; sum.y += p.y; sum.z += p.z; sum.w += p.w;
+      }
+      x[4 * q] = sum.x + h[4 * q];
+      x[4 * q + 1] = sum.y + h[4 * q + 1];
+      x[4 * q + 2] = sum.z + h[4 * q + 2];
+      x[4 * q + 3] = sum.w + h[4 * q + 3];
+    }
+    __syncthreads();  // every owner has read the partials before the next step writes them
+  }
+  cp_async_wait<0>();  // no copy may land after the CTA is gone
+  griddep_launch_dependents();
+  if (j.fin) store_own(j.fin + u * j.fin_unit_stride, x);
+}
+
+template <int K, int LAYOUT>
+cudaError_t launch_ksplit(const SeqJob& j, cudaStream_t stream) {
+  const size_t smem = sizeof(float) * ks_smem_floats<K>();
+  auto kern = seq_simt_ksplit_kernel<K, LAYOUT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid = job_grid(j, j.V / kTileV);
+  e = launch_kernel(kern, grid, ks_threads<K>(), smem, stream, j.pdl != 0, j);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 template <int R, int LAYOUT>
 cudaError_t launch_one(const SeqJob& j, cudaStream_t stream) {
   constexpr int K = R * 32;
@@ -290,10 +498,10 @@ cudaError_t launch_one(const SeqJob& j, cudaStream_t stream) {
 template <int LAYOUT>
 cudaError_t dispatch_r(const SeqJob& j, cudaStream_t s) {
   switch (j.K / 32) {
-    case 1: return launch_one<1, LAYOUT>(j, s);
-    case 2: return launch_one<2, LAYOUT>(j, s);
-    case 3: return launch_one<3, LAYOUT>(j, s);
-    case 4: return launch_one<4, LAYOUT>(j, s);
+    case 1: return launch_ksplit<32, LAYOUT>(j, s);
+    case 2: return launch_ksplit<64, LAYOUT>(j, s);
+    case 3: return launch_ksplit<96, LAYOUT>(j, s);
+    case 4: return launch_ksplit<128, LAYOUT>(j, s);
     case 5: return launch_one<5, LAYOUT>(j, s);
     case 6: return launch_one<6, LAYOUT>(j, s);
     case 7: return launch_one<7, LAYOUT>(j, s);
