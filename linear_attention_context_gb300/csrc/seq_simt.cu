@@ -291,7 +291,16 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
 // thread that owns an output (a row and 16 columns) adds them and H.  A step's
 // whole A (K x K, k-major) is copied in with cp.async during the step before.
 constexpr int kKG = 4;          // k-groups
-constexpr int kPld = kTileV + 4;  // padded row of a partial block and of the state tile
+constexpr int kPld = kTileV + 4;  // padded row of the state tile
+
+// Partial blocks are [kKG][K][kPld] (padded rows, so consecutive rows start in
+// different banks) with the two 16-byte groups of each pair swapped in odd
+// 8-row blocks: a warp's writes (8-row blocks of 8 columns, two row blocks
+// per quarter-warp) and the owners' reads (one row, 16 columns) then fall in
+// distinct banks.
+__device__ __forceinline__ int pidx(int row, int col) {
+  return row * kPld + ((((col >> 2) ^ (row >> 3)) & 1) | ((col >> 2) & 6)) * 4 + (col & 3);
+}
 
 template <int K>
 __host__ __device__ constexpr int ks_threads() {
@@ -315,7 +324,7 @@ __global__ void __launch_bounds__(2 * K) seq_simt_ksplit_kernel(const SeqJob j) 
   extern __shared__ __align__(16) float smem[];
   float* Xs = smem;                      // [K][kPld]   state tile, kv view
   float* As0 = Xs + K * kPld;            // [2][K][AL]  A copies, As[k][m] = A[m][k]
-  float* Ps = As0 + 2 * K * AL;          // [kKG][K][kPld] partial blocks
+  float* Ps = As0 + 2 * K * AL;          // [kKG][K][kPld] partial blocks (pidx)
 
   const int t = threadIdx.x;
   const int kg = t / (K / 2);            // k-group
@@ -445,19 +454,21 @@ __global__ void __launch_bounds__(2 * K) seq_simt_ksplit_kernel(const SeqJob j) 
         for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av[r], xv[c], acc[r][c]);
     }
     // partial blocks -> shared memory; the owners add them (k-groups in order) and H
-    float* P = Ps + kg * K * kPld + (rb * 8) * kPld + cb * 8;
+    float* P = Ps + kg * K * kPld;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-      *reinterpret_cast<float4*>(P + r * kPld) = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-      *reinterpret_cast<float4*>(P + r * kPld + 4) = make_float4(acc[r][4], acc[r][5], acc[r][6], acc[r][7]);
+      *reinterpret_cast<float4*>(P + pidx(rb * 8 + r, cb * 8)) = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+      *reinterpret_cast<float4*>(P + pidx(rb * 8 + r, cb * 8 + 4)) =
+          make_float4(acc[r][4], acc[r][5], acc[r][6], acc[r][7]);
     }
     __syncthreads();
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      float4 sum = *reinterpret_cast<const float4*>(Ps + orow * kPld + oc0 + 4 * q);
+      const int pi = pidx(orow, oc0 + 4 * q);
+      float4 sum = *reinterpret_cast<const float4*>(Ps + pi);
 #pragma unroll
       for (int gg = 1; gg < kKG; ++gg) {
-        const float4 p = *reinterpret_cast<const float4*>(Ps + gg * K * kPld + orow * kPld + oc0 + 4 * q);
+        const float4 p = *reinterpret_cast<const float4*>(Ps + gg * K * kPld + pi);
         sum.x += p.x; sum.y += p.y; sum.z += p.z; sum.w += p.w;
       }
       x[4 * q] = sum.x + h[4 * q];
