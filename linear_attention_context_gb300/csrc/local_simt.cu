@@ -16,11 +16,11 @@
 // Work split.  The columns of Y = [H | M] (V columns of the local state, K of
 // the propagation matrix, which starts at the identity) evolve independently
 // under the same left multiplications, so each warp owns a block of columns of
-// one segment for the whole segment: a lane holds R rows x 2 columns in
-// registers and G = K / R lanes share a column pair (the dot product k^T Y is
+// one segment for the whole segment: a lane holds R rows x NC columns in
+// registers and G = K / R lanes share a column group (the dot product k^T Y is
 // a partial sum per lane, then a shuffle reduction over those G lanes).  Per
-// token and lane: 2R FMAs for the dot products and 2R for the update; every
-// key value read from shared memory (a broadcast) feeds two FMAs.  No
+// token and lane: NC R FMAs for the dot products and NC R for the update;
+// every key value read from shared memory (a broadcast) feeds NC FMAs.  No
 // synchronisation between tokens.
 //
 // Decay as a scale.  Y = s Yhat with s = exp(sum of g since a reference
@@ -104,18 +104,55 @@ __device__ __forceinline__ void widen_rows(const uint16_t* src, float* dst, int 
 }
 
 // Reduces a lane's partial dot products over the G lanes sharing its columns.
-template <int CW>
-__device__ __forceinline__ void reduce_parts(float& d0, float& d1) {
+template <int CW, int NC>
+__device__ __forceinline__ void reduce_parts(float (&d)[NC]) {
 #pragma unroll
-  for (int m = CW; m < 32; m <<= 1) {
-    d0 += __shfl_xor_sync(0xffffffffu, d0, m);
-    d1 += __shfl_xor_sync(0xffffffffu, d1, m);
+  for (int m = CW; m < 32; m <<= 1)
+#pragma unroll
+    for (int c = 0; c < NC; ++c) d[c] += __shfl_xor_sync(0xffffffffu, d[c], m);
+}
+
+// One pass over the registers: optionally Yhat += k_i c^T (token i's update),
+// then optionally d = k_n^T Yhat (the next token's dot products, partial over
+// this lane's rows); each key value read feeds NC FMAs per use.
+template <int R, int NC, bool UPD, bool DOT>
+__device__ __forceinline__ void token_pass(float (&y)[NC][R], const float* kc, const float (&cc)[NC],
+                                           const float* kn, float (&d)[NC]) {
+  float a[NC][2];
+#pragma unroll
+  for (int c = 0; c < NC; ++c) a[c][0] = a[c][1] = 0.f;
+#pragma unroll
+  for (int r = 0; r < R; r += 4) {
+    if constexpr (UPD) {
+      const float4 kk = *reinterpret_cast<const float4*>(kc + r);
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        y[c][r] = fmaf(kk.x, cc[c], y[c][r]);
+        y[c][r + 1] = fmaf(kk.y, cc[c], y[c][r + 1]);
+        y[c][r + 2] = fmaf(kk.z, cc[c], y[c][r + 2]);
+        y[c][r + 3] = fmaf(kk.w, cc[c], y[c][r + 3]);
+      }
+    }
+    if constexpr (DOT) {
+      const float4 kq = *reinterpret_cast<const float4*>(kn + r);
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        a[c][0] = fmaf(kq.x, y[c][r], a[c][0]);
+        a[c][1] = fmaf(kq.y, y[c][r + 1], a[c][1]);
+        a[c][0] = fmaf(kq.z, y[c][r + 2], a[c][0]);
+        a[c][1] = fmaf(kq.w, y[c][r + 3], a[c][1]);
+      }
+    }
+  }
+  if constexpr (DOT) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) d[c] = a[c][0] + a[c][1];
   }
 }
 
-template <int R, int G>
+template <int R, int G, int NC>
 __global__ void __launch_bounds__(kLocalThreads, 6) local_pass_kernel(const LocalParams p) {
-  constexpr int CW = 32 / G;  // column pairs per warp
+  constexpr int CW = 32 / G;  // column groups (of NC columns) per warp
   const LocalJob& j = p.j;
   const int K = j.K, V = j.V, L = j.L;
   const int64_t unit = blockIdx.z == 0 ? (int64_t)blockIdx.y : (int64_t)blockIdx.z * gridDim.y + blockIdx.y;
@@ -140,18 +177,17 @@ __global__ void __launch_bounds__(kLocalThreads, 6) local_pass_kernel(const Loca
   const int q = lane - part * CW;
   const int row0 = part * R;
   const int cta_c0 = p.col_begin + (int)blockIdx.x * p.cols_per_cta;
-  const int gc = cta_c0 + warp * (2 * CW) + 2 * q;  // this lane's first column of Y (the second is gc + 1)
+  const int gc = cta_c0 + warp * (NC * CW) + NC * q;  // this lane's first column of Y (then gc + 1 .. gc + NC - 1)
   const bool live = gc < p.col_end;
-  const bool is_h = gc < V;
-  const int mc = gc - V;             // its column of M when !is_h
+  const bool is_h = gc < V;          // NC divides V: a lane's columns are all of H or all of M
+  const int mc = gc - V;             // its first column of M when !is_h
   const bool need_v = cta_c0 < V;    // the CTA holds a column of H
 
-  float y0[R], y1[R];
+  float y[NC][R];
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    y0[r] = (!is_h && row0 + r == mc) ? 1.0f : 0.0f;
-    y1[r] = (!is_h && row0 + r == mc + 1) ? 1.0f : 0.0f;
-  }
+  for (int c = 0; c < NC; ++c)
+#pragma unroll
+    for (int r = 0; r < R; ++r) y[c][r] = (!is_h && row0 + r == mc + c) ? 1.0f : 0.0f;
 
   // Let a dependent kernel (the correction) launch now; it reads H and M only
   // after its griddepcontrol.wait, i.e. after this grid has completed.
@@ -172,8 +208,8 @@ __global__ void __launch_bounds__(kLocalThreads, 6) local_pass_kernel(const Loca
       double Gs = lane < n ? (double)graw[lane] : 0.0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, Gs, o);
-        if (lane >= o) Gs += y;
+        const double yv = __shfl_up_sync(0xffffffffu, Gs, o);
+        if (lane >= o) Gs += yv;
       }
       Gs += gsum;
       // Reference moves: the first token whose sum is more than kRescaleLog
@@ -213,95 +249,51 @@ __global__ void __launch_bounds__(kLocalThreads, 6) local_pass_kernel(const Loca
 
     // Token i's update and token i + 1's dot products share one pass over the
     // registers: d_{i+1} = k_{i+1}^T (Yhat + k_i c_i^T).
-    float d0, d1;
+    float d[NC];
+    float cz[NC] = {};
     {
       const float fac = fac_s[0];
       if (fac != 1.0f) {  // same for every thread of the CTA
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          y0[r] *= fac;
-          y1[r] *= fac;
-        }
-      }
-      const float* kn = ks + row0;
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
+        for (int c = 0; c < NC; ++c)
 #pragma unroll
-      for (int r = 0; r < R; r += 4) {
-        const float4 kk = *reinterpret_cast<const float4*>(kn + r);
-        a0 = fmaf(kk.x, y0[r], a0);
-        b0 = fmaf(kk.x, y1[r], b0);
-        a1 = fmaf(kk.y, y0[r + 1], a1);
-        b1 = fmaf(kk.y, y1[r + 1], b1);
-        a2 = fmaf(kk.z, y0[r + 2], a2);
-        b2 = fmaf(kk.z, y1[r + 2], b2);
-        a3 = fmaf(kk.w, y0[r + 3], a3);
-        b3 = fmaf(kk.w, y1[r + 3], b3);
+          for (int r = 0; r < R; ++r) y[c][r] *= fac;
       }
-      d0 = (a0 + a1) + (a2 + a3);
-      d1 = (b0 + b1) + (b2 + b3);
-      reduce_parts<CW>(d0, d1);
+      token_pass<R, NC, false, true>(y, nullptr, cz, ks + row0, d);
+      reduce_parts<CW, NC>(d);
     }
     for (int i = 0; i < n; ++i) {
-      float v0 = 0.f, v1 = 0.f;
+      float v[NC];
+#pragma unroll
+      for (int c = 0; c < NC; ++c) v[c] = 0.f;
       if (is_h && live) {
-        const float2 vv = *reinterpret_cast<const float2*>(vs + i * V + gc);
-        v0 = vv.x;
-        v1 = vv.y;
+        if constexpr (NC == 4) {
+          const float4 vv = *reinterpret_cast<const float4*>(vs + i * V + gc);
+          v[0] = vv.x; v[1] = vv.y; v[2] = vv.z; v[3] = vv.w;
+        } else {
+#pragma unroll
+          for (int c = 0; c < NC; ++c) v[c] = vs[i * V + gc + c];
+        }
       }
       const float b = bs[i], inv = inv_s[i];
-      const float c0 = b * fmaf(v0, inv, -d0);
-      const float c1 = b * fmaf(v1, inv, -d1);
+      float cc[NC];
+#pragma unroll
+      for (int c = 0; c < NC; ++c) cc[c] = b * fmaf(v[c], inv, -d[c]);
       const float* kc = ks + i * K + row0;
       if (i + 1 < n) {
-        const float* kn = kc + K;
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
-#pragma unroll
-        for (int r = 0; r < R; r += 4) {
-          const float4 kk = *reinterpret_cast<const float4*>(kc + r);
-          const float4 kq = *reinterpret_cast<const float4*>(kn + r);
-          y0[r] = fmaf(kk.x, c0, y0[r]);
-          y1[r] = fmaf(kk.x, c1, y1[r]);
-          y0[r + 1] = fmaf(kk.y, c0, y0[r + 1]);
-          y1[r + 1] = fmaf(kk.y, c1, y1[r + 1]);
-          y0[r + 2] = fmaf(kk.z, c0, y0[r + 2]);
-          y1[r + 2] = fmaf(kk.z, c1, y1[r + 2]);
-          y0[r + 3] = fmaf(kk.w, c0, y0[r + 3]);
-          y1[r + 3] = fmaf(kk.w, c1, y1[r + 3]);
-          a0 = fmaf(kq.x, y0[r], a0);
-          b0 = fmaf(kq.x, y1[r], b0);
-          a1 = fmaf(kq.y, y0[r + 1], a1);
-          b1 = fmaf(kq.y, y1[r + 1], b1);
-          a2 = fmaf(kq.z, y0[r + 2], a2);
-          b2 = fmaf(kq.z, y1[r + 2], b2);
-          a3 = fmaf(kq.w, y0[r + 3], a3);
-          b3 = fmaf(kq.w, y1[r + 3], b3);
-        }
-        d0 = (a0 + a1) + (a2 + a3);
-        d1 = (b0 + b1) + (b2 + b3);
-        reduce_parts<CW>(d0, d1);
+        token_pass<R, NC, true, true>(y, kc, cc, kc + K, d);
+        reduce_parts<CW, NC>(d);
         const float fac = fac_s[i + 1];
         if (fac != 1.0f) {  // rescale before token i + 1: its dot products scale alike
 #pragma unroll
-          for (int r = 0; r < R; ++r) {
-            y0[r] *= fac;
-            y1[r] *= fac;
+          for (int c = 0; c < NC; ++c) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) y[c][r] *= fac;
+            d[c] *= fac;
           }
-          d0 *= fac;
-          d1 *= fac;
         }
       } else {
-#pragma unroll
-        for (int r = 0; r < R; r += 4) {
-          const float4 kk = *reinterpret_cast<const float4*>(kc + r);
-          y0[r] = fmaf(kk.x, c0, y0[r]);
-          y1[r] = fmaf(kk.x, c1, y1[r]);
-          y0[r + 1] = fmaf(kk.y, c0, y0[r + 1]);
-          y1[r + 1] = fmaf(kk.y, c1, y1[r + 1]);
-          y0[r + 2] = fmaf(kk.z, c0, y0[r + 2]);
-          y1[r + 2] = fmaf(kk.z, c1, y1[r + 2]);
-          y0[r + 3] = fmaf(kk.w, c0, y0[r + 3]);
-          y1[r + 3] = fmaf(kk.w, c1, y1[r + 3]);
-        }
+        token_pass<R, NC, true, false>(y, kc, cc, nullptr, d);
       }
     }
   }
@@ -309,34 +301,45 @@ __global__ void __launch_bounds__(kLocalThreads, 6) local_pass_kernel(const Loca
   const float s = s_end[0];
   if (is_h) {
     float* h = j.H + unit * (int64_t)K * V;
-    if (j.layout == 0) {  // kv: H[k][v]
+    if (j.layout == 0) {  // kv: H[k][v], NC consecutive columns per row
 #pragma unroll
-      for (int r = 0; r < R; ++r)
-        *reinterpret_cast<float2*>(h + (int64_t)(row0 + r) * V + gc) = make_float2(y0[r] * s, y1[r] * s);
-    } else {  // vk: H[v][k]
-      float* h0 = h + (int64_t)gc * K + row0;
-      float* h1 = h0 + K;
+      for (int r = 0; r < R; ++r) {
+        float* dst = h + (int64_t)(row0 + r) * V + gc;
+        if constexpr (NC == 4)
+          *reinterpret_cast<float4*>(dst) = make_float4(y[0][r] * s, y[1][r] * s, y[2][r] * s, y[3][r] * s);
+        else
+          *reinterpret_cast<float2*>(dst) = make_float2(y[0][r] * s, y[1][r] * s);
+      }
+    } else {  // vk: H[v][k], R consecutive rows per column
 #pragma unroll
-      for (int r = 0; r < R; r += 4) {
-        *reinterpret_cast<float4*>(h0 + r) = make_float4(y0[r] * s, y0[r + 1] * s, y0[r + 2] * s, y0[r + 3] * s);
-        *reinterpret_cast<float4*>(h1 + r) = make_float4(y1[r] * s, y1[r + 1] * s, y1[r + 2] * s, y1[r + 3] * s);
+      for (int c = 0; c < NC; ++c) {
+        float* dst = h + (int64_t)(gc + c) * K + row0;
+#pragma unroll
+        for (int r = 0; r < R; r += 4)
+          *reinterpret_cast<float4*>(dst + r) =
+              make_float4(y[c][r] * s, y[c][r + 1] * s, y[c][r + 2] * s, y[c][r + 3] * s);
       }
     }
   } else {
     float* m = j.M + unit * (int64_t)K * K;
 #pragma unroll
-    for (int r = 0; r < R; ++r)
-      *reinterpret_cast<float2*>(m + (int64_t)(row0 + r) * K + mc) = make_float2(y0[r] * s, y1[r] * s);
+    for (int r = 0; r < R; ++r) {
+      float* dst = m + (int64_t)(row0 + r) * K + mc;
+      if constexpr (NC == 4)
+        *reinterpret_cast<float4*>(dst) = make_float4(y[0][r] * s, y[1][r] * s, y[2][r] * s, y[3][r] * s);
+      else
+        *reinterpret_cast<float2*>(dst) = make_float2(y[0][r] * s, y[1][r] * s);
+    }
   }
 }
 
-template <int R, int G>
+template <int R, int G, int NC>
 cudaError_t launch_rg(const LocalJob& j, cudaStream_t stream) {
   LocalParams p{};
   p.j = j;
   p.col_begin = j.H ? 0 : j.V;
   p.col_end = j.M ? j.V + j.K : j.V;
-  p.cols_per_cta = kLocalWarps * 64 / G;
+  p.cols_per_cta = kLocalWarps * NC * (32 / G);
   const int64_t units = (int64_t)j.nchains * j.S;
   const int xblocks = (p.col_end - p.col_begin + p.cols_per_cta - 1) / p.cols_per_cta;
   dim3 grid(xblocks, 1, 1);
@@ -349,26 +352,28 @@ cudaError_t launch_rg(const LocalJob& j, cudaStream_t stream) {
   // fp32 tile, per-token scalars, raw next tile (bf16 keys and values, fp32 scalars)
   const size_t smem = sizeof(float) * (size_t)(kTT * (j.K + j.V) + 3 * kTT + 4 + 2 * kTT) +
                       sizeof(uint16_t) * (size_t)kTT * (j.K + j.V);
-  cudaError_t e = cudaFuncSetAttribute(local_pass_kernel<R, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(local_pass_kernel<R, G, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel(local_pass_kernel<R, G>, grid, kLocalThreads, smem, stream, j.pdl != 0, p);
+  return launch_kernel(local_pass_kernel<R, G, NC>, grid, kLocalThreads, smem, stream, j.pdl != 0, p);
 }
 
 }  // namespace
 
-// Rows per lane R and lanes per column pair G for a key dimension K (a
-// multiple of 32 up to 256): G is the smallest power of two with K / G <= 64.
+// Rows per lane R, lanes per column group G and columns per lane NC for a key
+// dimension K (a multiple of 32 up to 256): four columns of 32 or fewer rows
+// up to K = 128 (each key value read feeds four FMAs per use), two columns of
+// at most 64 rows above.
 cudaError_t launch_local_simt(const LocalJob& j, cudaStream_t stream) {
   switch (j.K) {
-    case 32: return launch_rg<32, 1>(j, stream);
-    case 64: return launch_rg<64, 1>(j, stream);
-    case 96: return launch_rg<48, 2>(j, stream);
-    case 128: return launch_rg<64, 2>(j, stream);
-    case 160: return launch_rg<40, 4>(j, stream);
-    case 192: return launch_rg<48, 4>(j, stream);
-    case 224: return launch_rg<56, 4>(j, stream);
-    case 256: return launch_rg<64, 4>(j, stream);
+    case 32: return launch_rg<32, 1, 4>(j, stream);
+    case 64: return launch_rg<32, 2, 4>(j, stream);
+    case 96: return launch_rg<24, 4, 4>(j, stream);
+    case 128: return launch_rg<32, 4, 4>(j, stream);
+    case 160: return launch_rg<40, 4, 2>(j, stream);
+    case 192: return launch_rg<48, 4, 2>(j, stream);
+    case 224: return launch_rg<56, 4, 2>(j, stream);
+    case 256: return launch_rg<64, 4, 2>(j, stream);
     default: return cudaErrorInvalidValue;
   }
 }
