@@ -340,6 +340,26 @@ QLA_API int qla_cp_correct_scan_static(const float* H, const float* M, const flo
 QLA_API int qla_local_pass(const void* k, const void* v, const float* beta, const float* g, float* H, float* M,
                            int B, int heads, int T, int S, int K, int V, int layout, void* stream);
 
+/*
+ * qla_local_pass with the sub-segment split chosen by the caller.  All of a
+ * pass's CTAs run the same number of tokens, so when they exceed what the SMs
+ * hold at once, the last partial wave costs a whole segment's time on a few
+ * SMs.  With split = F > 1 each segment is run as F sub-segments of L / F
+ * tokens (shorter units, more waves), and the F sub-segments' maps are then
+ * composed per segment by the correction kernels: M_i = the product of the
+ * sub-segment M's, H_i = their recurrence from zero (the same affine
+ * composition the correction applies across segments).  The results equal
+ * split = 1 up to rounding.  The sub-segments' H and M take
+ * B*heads*S*F*(K*K + K*V)*4 bytes of device scratch from the stream-ordered
+ * allocator (cudaMallocAsync on `stream`, returned the same way).
+ *   split  0: automatic (the F in {1, 2, 4, 8, 16} that minimises the
+ *          estimated time, from the launch's occupancy on this device);
+ *          otherwise F, which must divide L = T / S.
+ * qla_local_pass is split = 0.
+ */
+QLA_API int qla_local_pass_ex(const void* k, const void* v, const float* beta, const float* g, float* H, float* M,
+                              int B, int heads, int T, int S, int K, int V, int layout, int split, void* stream);
+
 /* ABI version of this header (major * 100 + minor). */
 QLA_API int qla_version(void);
 

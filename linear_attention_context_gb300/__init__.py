@@ -34,7 +34,8 @@ STATUS = {0: "QLA_OK", -1: "QLA_ERR_INVALID_ARG", -2: "QLA_ERR_UNSUPPORTED", -3:
 EXPORTS = ("qla_cp_correct", "qla_cp_correct_ex", "qla_cp_correct_varlen", "qla_cp_correct_varlen_ex",
            "qla_scan_workspace_bytes", "qla_set_variant", "qla_set_dependent_launch",
            "qla_resolve", "qla_status_string", "qla_last_error", "qla_device_status", "qla_selftest_stalled_wait",
-           "qla_selftest_dependent_producer", "qla_cp_correct_scan_static", "qla_local_pass", "qla_version")
+           "qla_selftest_dependent_producer", "qla_cp_correct_scan_static", "qla_local_pass", "qla_local_pass_ex",
+           "qla_version")
 
 # Bytes of scratch the allocation-free scan entry point holds (QLA_SCAN_STATIC_BYTES).
 SCAN_STATIC_BYTES = 8 << 20
@@ -93,6 +94,8 @@ def lib():
         L.qla_cp_correct_scan_static.restype = ci
         L.qla_local_pass.argtypes = [vp] * 6 + [ci] * 7 + [vp]
         L.qla_local_pass.restype = ci
+        L.qla_local_pass_ex.argtypes = [vp] * 6 + [ci] * 8 + [vp]
+        L.qla_local_pass_ex.restype = ci
         L.qla_version.argtypes = []
         L.qla_version.restype = ci
         _LIB = L
@@ -226,7 +229,7 @@ def cp_correct_varlen(H, M, cu_seg, h_init=None, out=None, *, layout="kv", direc
     return out
 
 
-def local_pass(k, v, beta, g, S, H=None, M=None, *, layout="kv", want_H=True, want_M=True, stream=None):
+def local_pass(k, v, beta, g, S, H=None, M=None, *, layout="kv", want_H=True, want_M=True, split=0, stream=None):
     """Per-segment local states H and propagation matrices M (the inputs of
     cp_correct) from token-level inputs, by the gated delta rule (include/qla.h,
     qla_local_pass).
@@ -235,7 +238,9 @@ def local_pass(k, v, beta, g, S, H=None, M=None, *, layout="kv", want_H=True, wa
     (or int16 holding bf16 bit patterns); beta, g: [B, heads, T] float32 (write
     strengths, log-space decays); T a multiple of S.  H ([B, heads, S, K, V] kv
     or [B, heads, S, V, K] vk) and M ([B, heads, S, K, K]) float32 are
-    allocated when not given.  Returns (H, M), None for a part not wanted."""
+    allocated when not given.  ``split``: sub-segments per segment (0 =
+    automatic; see qla_local_pass_ex).  Returns (H, M), None for a part not
+    wanted."""
     import torch
     if layout not in LAYOUTS:
         raise ValueError(f"layout {layout!r}")
@@ -261,8 +266,8 @@ def local_pass(k, v, beta, g, S, H=None, M=None, *, layout="kv", want_H=True, wa
     _check_tensor("H", H, dev, (B, nh, S) + st)
     _check_tensor("M", M, dev, (B, nh, S, K, K))
     with torch.cuda.device(dev):
-        rc = lib().qla_local_pass(_ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(H), _ptr(M), B, nh, T, S, K, V,
-                                  LAYOUTS[layout], _stream_handle(stream))
+        rc = lib().qla_local_pass_ex(_ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(H), _ptr(M), B, nh, T, S, K, V,
+                                     LAYOUTS[layout], int(split), _stream_handle(stream))
     check(rc)
     return H, M
 

@@ -463,6 +463,113 @@ int run_scan(const float* H, const float* M, const float* h_init, float* out, fl
   return run_scan_alloc(plain_job(H, M, h_init, out, fin, s), s, engine, release, group, d, stream);
 }
 
+// ---------------------------------------------------------------- local pass split
+//
+// A local pass's CTAs all run the same number of tokens, so when they exceed
+// what the SMs hold at once the last partial wave costs a whole segment's
+// time on a few SMs.  Splitting each segment into F sub-segments makes the
+// units F times shorter (more, shorter waves); the F sub-segments' maps are
+// then composed per segment by the correction kernels: M_seg = the product of
+// the sub-segment M's (from the identity) and H_seg = their recurrence from
+// zero, exactly the scan's first phase with groups of F.
+
+// Relative cost of one composition step per wave of its CTAs, in tokens of a
+// local-pass wave (both measured on GB300 at K = V = 128: a correction step
+// ~1.6 us, a local-pass token per wave ~0.5 us; rounded up for set-up).
+constexpr double kComposeStepTokens = 4.0;
+
+int local_auto_split(const LocalJob& j, const DeviceInfo* d, int* F) {
+  *F = 1;
+  if (d->sm_count < 1) return QLA_OK;
+  double best = 0.0;
+  for (int f = 1; f <= 16; f *= 2) {
+    if (j.L % f || j.L / f < 64) break;
+    LocalJob t = j;
+    t.S = j.S * f;
+    t.L = j.L / f;
+    // the split always computes the sub-segments' M (H only if H is wanted);
+    // the pointer only sets the column count of the query
+    if (f > 1 && !t.M) t.M = reinterpret_cast<float*>(16);
+    int64_t ctas = 0;
+    int per_sm = 0;
+    const cudaError_t e = local_grid_info(t, &ctas, &per_sm);
+    if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+    if (per_sm < 1) per_sm = 1;
+    const int64_t slots = (int64_t)per_sm * d->sm_count;
+    const double waves = (double)((ctas + slots - 1) / slots);
+    double cost = waves * t.L;
+    if (f > 1) {  // composition: f steps over (H, M) column tiles, one CTA per SM
+      const int64_t ccta = j.nchains * (int64_t)j.S * ((j.V + j.K + 31) / 32);
+      cost += f * kComposeStepTokens * (double)((ccta + d->sm_count - 1) / d->sm_count);
+    }
+    if (f == 1 || cost < best) {
+      best = cost;
+      *F = f;
+    }
+  }
+  return QLA_OK;
+}
+
+int local_pass_split(const LocalJob& j, int F, const DeviceInfo* d, cudaStream_t stream) {
+  const int64_t units = (int64_t)j.nchains * j.S * F;  // sub-segments
+  const size_t hbytes = (size_t)units * j.K * j.V * sizeof(float);
+  const size_t mbytes = (size_t)units * j.K * j.K * sizeof(float);
+  const bool need_h = j.H != nullptr;
+  float* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), (need_h ? hbytes : 0) + mbytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(local pass sub-segments)");
+  float* Ms = ws;
+  float* Hs = need_h ? ws + (size_t)units * j.K * j.K : nullptr;
+  LocalJob t = j;
+  t.S = j.S * F;
+  t.L = j.L / F;
+  t.H = Hs;
+  t.M = Ms;
+  int st = QLA_OK;
+  e = launch_local_simt(t, stream);
+  if (e != cudaSuccess) st = cuda_fail(e, "kernel launch");
+  if (st == QLA_OK) {
+    // segment s of chain c = group s of F sub-segments: 1a the product of the
+    // M's from the identity, 1b the recurrence over (H, M) from zero
+    SeqJob base{};
+    base.M = Ms;
+    base.m_chain_stride = (int64_t)t.S * j.K * j.K;
+    base.h_chain_stride = (int64_t)t.S * j.K * j.V;
+    base.nchains = j.nchains;
+    base.S = t.S;
+    base.L = F;
+    base.G = j.S;
+    base.K = j.K;
+    base.direction = QLA_FORWARD;
+    SeqJob ja = base;
+    ja.H = nullptr;
+    ja.init_mode = kInitIdentity;
+    ja.fin = j.M;
+    ja.fin_unit_stride = (int64_t)j.K * j.K;
+    ja.V = j.K;
+    ja.layout = QLA_LAYOUT_KV;
+    SeqJob jb = base;
+    jb.H = Hs;
+    jb.init_mode = kInitZero;
+    jb.fin = j.H;
+    jb.fin_unit_stride = (int64_t)j.K * j.V;
+    jb.V = j.V;
+    jb.layout = j.layout;
+    auto run = [&](const SeqJob& jj, cudaStream_t s) {
+      return launch_seq(jj, engine_for(jj, QLA_ENGINE_TC), QLA_RELEASE_MEMBAR, d, s);
+    };
+    if (j.M && j.H)
+      st = fork_join(d, stream, [&](cudaStream_t s) { return run(ja, s); }, [&](cudaStream_t s) { return run(jb, s); });
+    else if (j.M)
+      st = run(ja, stream);
+    else
+      st = run(jb, stream);
+  }
+  e = cudaFreeAsync(ws, stream);
+  if (st == QLA_OK && e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(local pass sub-segments)");
+  return st;
+}
+
 // ---------------------------------------------------------------- allocation-free scan
 //
 // Scratch of qla_cp_correct_scan_static(): a fixed array of this file, one
@@ -698,6 +805,11 @@ int qla_cp_correct_varlen_ex(const float* H, const float* M, const float* h_init
 
 int qla_local_pass(const void* k, const void* v, const float* beta, const float* g, float* H, float* M, int B,
                    int heads, int T, int S, int K, int V, int layout, void* stream) {
+  return qla_local_pass_ex(k, v, beta, g, H, M, B, heads, T, S, K, V, layout, 0, stream);
+}
+
+int qla_local_pass_ex(const void* k, const void* v, const float* beta, const float* g, float* H, float* M, int B,
+                      int heads, int T, int S, int K, int V, int layout, int split, void* stream) {
   t_last_error.clear();
   if (B < 1 || heads < 1 || S < 1 || T < 1 || K < 1 || V < 1)
     return fail(QLA_ERR_INVALID_ARG, "B, heads, T, S, K, V must be >= 1 (got %d, %d, %d, %d, %d, %d)", B, heads, T,
@@ -709,8 +821,12 @@ int qla_local_pass(const void* k, const void* v, const float* beta, const float*
   if (!H && !M) return fail(QLA_ERR_INVALID_ARG, "H and M are both NULL: nothing to compute");
   if (K % 32 || K > 256 || V % 32 || V > 256)
     return fail(QLA_ERR_UNSUPPORTED, "K and V must be multiples of 32 in [32, 256] (got K=%d, V=%d)", K, V);
+  const int L = T / S;
+  if (split < 0 || (split > 0 && L % split))
+    return fail(QLA_ERR_INVALID_ARG, "split must be 0 (automatic) or divide the segment length %d (got %d)", L, split);
   const int64_t chains = (int64_t)B * heads;
-  if (chains * S > 0x7fffffff) return fail(QLA_ERR_UNSUPPORTED, "B*heads*S must be below 2^31");
+  if (chains * S * (split > 0 ? split : 1) > 0x7fffffff)
+    return fail(QLA_ERR_UNSUPPORTED, "B*heads*S*split must be below 2^31");
   if ((double)chains * T * std::max(K, V) >= 4.6e18) return fail(QLA_ERR_INVALID_ARG, "problem too large");
   const void* p16[] = {k, v, H, M};
   const char* n16[] = {"k", "v", "H", "M"};
@@ -733,6 +849,7 @@ int qla_local_pass(const void* k, const void* v, const float* beta, const float*
   DeviceInfo* d = nullptr;
   int st = current_device(&d);
   if (st != QLA_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
   LocalJob j{};
   j.k = static_cast<const uint16_t*>(k);
   j.v = static_cast<const uint16_t*>(v);
@@ -743,14 +860,18 @@ int qla_local_pass(const void* k, const void* v, const float* beta, const float*
   j.nchains = (int)chains;
   j.T = T;
   j.S = S;
-  j.L = T / S;
+  j.L = L;
   j.K = K;
   j.V = V;
   j.layout = layout;
   j.pdl = dependent_launch();
-  const cudaError_t e = launch_local_simt(j, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
-  return QLA_OK;
+  int F = split;
+  if (F == 0 && (st = local_auto_split(j, d, &F)) != QLA_OK) return st;
+  if (F == 1) {
+    const cudaError_t e = launch_local_simt(j, cs);
+    return e == cudaSuccess ? QLA_OK : cuda_fail(e, "kernel launch");
+  }
+  return local_pass_split(j, F, d, cs);
 }
 
 int qla_device_status(int* flags) {

@@ -334,6 +334,26 @@ __global__ void __launch_bounds__(kLocalThreads, 6) local_pass_kernel(const Loca
 }
 
 template <int R, int G, int NC>
+size_t smem_rg(const LocalJob& j) {
+  // fp32 tile, per-token scalars, raw next tile (bf16 keys and values, fp32 scalars)
+  return sizeof(float) * (size_t)(kTT * (j.K + j.V) + 3 * kTT + 4 + 2 * kTT) +
+         sizeof(uint16_t) * (size_t)kTT * (j.K + j.V);
+}
+
+// CTAs of a launch, and how many fit on one SM at once.
+template <int R, int G, int NC>
+cudaError_t info_rg(const LocalJob& j, int64_t* ctas, int* per_sm) {
+  const int cols = (j.H ? j.V : 0) + (j.M ? j.K : 0);
+  const int per_cta = kLocalWarps * NC * (32 / G);
+  *ctas = (int64_t)j.nchains * j.S * ((cols + per_cta - 1) / per_cta);
+  const size_t smem = smem_rg<R, G, NC>(j);
+  cudaError_t e = cudaFuncSetAttribute(local_pass_kernel<R, G, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, local_pass_kernel<R, G, NC>, kLocalThreads, smem);
+}
+
+template <int R, int G, int NC>
 cudaError_t launch_rg(const LocalJob& j, cudaStream_t stream) {
   LocalParams p{};
   p.j = j;
@@ -349,9 +369,7 @@ cudaError_t launch_rg(const LocalJob& j, cudaStream_t stream) {
     grid.y = 65535u;
     grid.z = (unsigned)((units + 65534) / 65535);
   }
-  // fp32 tile, per-token scalars, raw next tile (bf16 keys and values, fp32 scalars)
-  const size_t smem = sizeof(float) * (size_t)(kTT * (j.K + j.V) + 3 * kTT + 4 + 2 * kTT) +
-                      sizeof(uint16_t) * (size_t)kTT * (j.K + j.V);
+  const size_t smem = smem_rg<R, G, NC>(j);
   cudaError_t e = cudaFuncSetAttribute(local_pass_kernel<R, G, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
@@ -364,6 +382,20 @@ cudaError_t launch_rg(const LocalJob& j, cudaStream_t stream) {
 // dimension K (a multiple of 32 up to 256): four columns of 32 or fewer rows
 // up to K = 128 (each key value read feeds four FMAs per use), two columns of
 // at most 64 rows above.
+cudaError_t local_grid_info(const LocalJob& j, int64_t* ctas, int* per_sm) {
+  switch (j.K) {
+    case 32: return info_rg<32, 1, 4>(j, ctas, per_sm);
+    case 64: return info_rg<32, 2, 4>(j, ctas, per_sm);
+    case 96: return info_rg<24, 4, 4>(j, ctas, per_sm);
+    case 128: return info_rg<32, 4, 4>(j, ctas, per_sm);
+    case 160: return info_rg<40, 4, 2>(j, ctas, per_sm);
+    case 192: return info_rg<48, 4, 2>(j, ctas, per_sm);
+    case 224: return info_rg<56, 4, 2>(j, ctas, per_sm);
+    case 256: return info_rg<64, 4, 2>(j, ctas, per_sm);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t launch_local_simt(const LocalJob& j, cudaStream_t stream) {
   switch (j.K) {
     case 32: return launch_rg<32, 1, 4>(j, stream);

@@ -234,3 +234,25 @@ def test_local_pass_argument_checks(L, kw, status):
 def test_local_pass_valid_call_without_gpu(L):
     assert call_local(L) == -5
     assert call_local(L, H=None) == -5 and call_local(L, M=None) == -5
+
+
+def call_local_ex(L, split, T=64, S=4, **kw):
+    vp = ctypes.c_void_p
+    a = dict(k=FAKE, v=FAKE + (1 << 32), beta=FAKE + (2 << 32), g=FAKE + (3 << 32), H=FAKE + (4 << 32),
+             M=FAKE + (5 << 32))
+    a.update(kw)
+    return L.qla_local_pass_ex(vp(a["k"]), vp(a["v"]), vp(a["beta"]), vp(a["g"]), vp(a["H"]), vp(a["M"]), 1, 2, T,
+                               S, 64, 64, 0, split, None)
+
+
+@pytest.mark.parametrize("split", [-1, 3, 32])
+def test_local_pass_split_checks(L, split):
+    # segment length T / S = 16: the split must be 0 or divide it
+    assert call_local_ex(L, split) == -1
+    assert "split" in L.qla_last_error().decode()
+
+
+@no_gpu_only
+def test_local_pass_valid_splits_without_gpu(L):
+    for split in (0, 1, 2, 16):
+        assert call_local_ex(L, split) == -5

@@ -188,3 +188,40 @@ def test_local_pass_chained_into_the_correction(graph):
     finally:
         qla.set_dependent_launch(False)
     assert qla.device_status() == 0
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+@pytest.mark.parametrize("layout", ["kv", "vk"])
+def test_sub_segment_split(split, layout):
+    """Each segment run as `split` sub-segments whose maps the correction
+    kernels compose (M_i = product of the sub-segment M's, H_i = their
+    recurrence from zero): the same H and M as the oracle, for both parts, H
+    alone and M alone."""
+    import torch
+    import linear_attention_context_gb300 as qla
+    c = qi.LocalCase(B=1, heads=3, T=1024, S=2, K=128, V=64, seed=35)
+    k, v, b, g = qi.make_local_inputs(c)
+    Hr, Mr = oracle.local_pass(k, v, b, g, c.S, layout)
+    dk, dv, db, dg = (to_dev(a) for a in (k, v, b, g))
+    for want_H, want_M in ((True, True), (True, False), (False, True)):
+        H, M = qla.local_pass(dk, dv, db, dg, c.S, layout=layout, want_H=want_H, want_M=want_M, split=split)
+        torch.cuda.synchronize()
+        if want_H:
+            assert_parity(H.cpu().numpy().astype(np.float64), Hr, what=f"split {split} H {layout}")
+        if want_M:
+            assert_parity(M.cpu().numpy().astype(np.float64), Mr, what=f"split {split} M {layout}")
+
+
+@pytest.mark.parametrize("K,V", [(64, 32), (256, 64), (96, 160)])
+def test_sub_segment_split_other_widths(K, V):
+    """The composition runs on the 3xTF32 engine (K = 128, 256) or the FFMA
+    engine (other K)."""
+    import torch
+    import linear_attention_context_gb300 as qla
+    c = qi.LocalCase(B=1, heads=2, T=512, S=2, K=K, V=V, seed=36)
+    k, v, b, g = qi.make_local_inputs(c)
+    Hr, Mr = oracle.local_pass(k, v, b, g, c.S)
+    H, M = qla.local_pass(*(to_dev(a) for a in (k, v, b, g)), c.S, split=4)
+    torch.cuda.synchronize()
+    assert_parity(H.cpu().numpy().astype(np.float64), Hr, what=f"split K={K} V={V} H")
+    assert_parity(M.cpu().numpy().astype(np.float64), Mr, what=f"split K={K} V={V} M")
