@@ -19,7 +19,8 @@
 // one segment for the whole segment: a lane holds R rows x NC columns in
 // registers and G = K / R lanes share a column group (the dot product k^T Y is
 // a partial sum per lane, then a shuffle reduction over those G lanes).  Per
-// token and lane: NC R FMAs for the dot products and NC R for the update;
+// token and lane: NC R FMAs for the dot products and NC R for the update, as
+// packed two-row FMAs (fma.rn.f32x2: each half rounds as a scalar FMA would);
 // every key value read from shared memory (a broadcast) feeds NC FMAs.  No
 // synchronisation between tokens.
 //
@@ -114,44 +115,69 @@ __device__ __forceinline__ void reduce_parts(float (&d)[NC]) {
 
 // One pass over the registers: optionally Yhat += k_i c^T (token i's update),
 // then optionally d = k_n^T Yhat (the next token's dot products, partial over
-// this lane's rows); each key value read feeds NC FMAs per use.
+// this lane's rows); each key value read feeds NC FMAs per use.  The state is
+// held as pairs of rows and every FMA is a packed fma.rn.f32x2 (two rows per
+// instruction, each rounded as a scalar FMA): the pass issues half the
+// instructions of scalar FMAs.
 template <int R, int NC, bool UPD, bool DOT>
-__device__ __forceinline__ void token_pass(float (&y)[NC][R], const float* kc, const float (&cc)[NC],
+__device__ __forceinline__ void token_pass(float2 (&y)[NC][R / 2], const float* kc, const float (&cc)[NC],
                                            const float* kn, float (&d)[NC]) {
-  float a[NC][2];
+  float2 a[NC][2];
+  float2 cp[NC];
 #pragma unroll
-  for (int c = 0; c < NC; ++c) a[c][0] = a[c][1] = 0.f;
+  for (int c = 0; c < NC; ++c) {
+    a[c][0] = a[c][1] = make_float2(0.f, 0.f);
+    cp[c] = make_float2(cc[c], cc[c]);
+  }
 #pragma unroll
   for (int r = 0; r < R; r += 4) {
     if constexpr (UPD) {
       const float4 kk = *reinterpret_cast<const float4*>(kc + r);
+      const float2 k01 = make_float2(kk.x, kk.y), k23 = make_float2(kk.z, kk.w);
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        y[c][r] = fmaf(kk.x, cc[c], y[c][r]);
-        y[c][r + 1] = fmaf(kk.y, cc[c], y[c][r + 1]);
-        y[c][r + 2] = fmaf(kk.z, cc[c], y[c][r + 2]);
-        y[c][r + 3] = fmaf(kk.w, cc[c], y[c][r + 3]);
+        y[c][r / 2] = __ffma2_rn(k01, cp[c], y[c][r / 2]);
+        y[c][r / 2 + 1] = __ffma2_rn(k23, cp[c], y[c][r / 2 + 1]);
       }
     }
     if constexpr (DOT) {
       const float4 kq = *reinterpret_cast<const float4*>(kn + r);
+      const float2 q01 = make_float2(kq.x, kq.y), q23 = make_float2(kq.z, kq.w);
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        a[c][0] = fmaf(kq.x, y[c][r], a[c][0]);
-        a[c][1] = fmaf(kq.y, y[c][r + 1], a[c][1]);
-        a[c][0] = fmaf(kq.z, y[c][r + 2], a[c][0]);
-        a[c][1] = fmaf(kq.w, y[c][r + 3], a[c][1]);
+        a[c][0] = __ffma2_rn(q01, y[c][r / 2], a[c][0]);
+        a[c][1] = __ffma2_rn(q23, y[c][r / 2 + 1], a[c][1]);
       }
     }
   }
   if constexpr (DOT) {
 #pragma unroll
-    for (int c = 0; c < NC; ++c) d[c] = a[c][0] + a[c][1];
+    for (int c = 0; c < NC; ++c) d[c] = (a[c][0].x + a[c][1].x) + (a[c][0].y + a[c][1].y);
   }
 }
 
+// Element r of a lane's column c held as row pairs.
+template <int R, int NC>
+__device__ __forceinline__ float yat(const float2 (&y)[NC][R / 2], int c, int r) {
+  return (r & 1) ? y[c][r >> 1].y : y[c][r >> 1].x;
+}
+
+// y *= f, two rows per packed multiply.
+template <int R, int NC>
+__device__ __forceinline__ void scale_state(float2 (&y)[NC][R / 2], float f) {
+  const float2 ff = make_float2(f, f);
+#pragma unroll
+  for (int c = 0; c < NC; ++c)
+#pragma unroll
+    for (int m = 0; m < R / 2; ++m) y[c][m] = __fmul2_rn(y[c][m], ff);
+}
+
+// Four CTAs per SM: the staging (keys and values of 32 tokens, fp32 and raw)
+// takes ~49 KB of shared memory per CTA at K = V = 128, which is the limit;
+// the register budget follows from it (up to ~200 per thread without spills
+// for the packed state).
 template <int R, int G, int NC>
-__global__ void __launch_bounds__(kLocalThreads, 6) local_pass_kernel(const LocalParams p) {
+__global__ void __launch_bounds__(kLocalThreads, 4) local_pass_kernel(const LocalParams p) {
   constexpr int CW = 32 / G;  // column groups (of NC columns) per warp
   const LocalJob& j = p.j;
   const int K = j.K, V = j.V, L = j.L;
@@ -183,11 +209,13 @@ __global__ void __launch_bounds__(kLocalThreads, 6) local_pass_kernel(const Loca
   const int mc = gc - V;             // its first column of M when !is_h
   const bool need_v = cta_c0 < V;    // the CTA holds a column of H
 
-  float y[NC][R];
+  float2 y[NC][R / 2];
 #pragma unroll
   for (int c = 0; c < NC; ++c)
 #pragma unroll
-    for (int r = 0; r < R; ++r) y[c][r] = (!is_h && row0 + r == mc + c) ? 1.0f : 0.0f;
+    for (int m = 0; m < R / 2; ++m)
+      y[c][m] = make_float2((!is_h && row0 + 2 * m == mc + c) ? 1.0f : 0.0f,
+                            (!is_h && row0 + 2 * m + 1 == mc + c) ? 1.0f : 0.0f);
 
   // Let a dependent kernel (the correction) launch now; it reads H and M only
   // after its griddepcontrol.wait, i.e. after this grid has completed.
@@ -253,12 +281,7 @@ __global__ void __launch_bounds__(kLocalThreads, 6) local_pass_kernel(const Loca
     float cz[NC] = {};
     {
       const float fac = fac_s[0];
-      if (fac != 1.0f) {  // same for every thread of the CTA
-#pragma unroll
-        for (int c = 0; c < NC; ++c)
-#pragma unroll
-          for (int r = 0; r < R; ++r) y[c][r] *= fac;
-      }
+      if (fac != 1.0f) scale_state<R, NC>(y, fac);  // same for every thread of the CTA
       token_pass<R, NC, false, true>(y, nullptr, cz, ks + row0, d);
       reduce_parts<CW, NC>(d);
     }
@@ -285,12 +308,9 @@ __global__ void __launch_bounds__(kLocalThreads, 6) local_pass_kernel(const Loca
         reduce_parts<CW, NC>(d);
         const float fac = fac_s[i + 1];
         if (fac != 1.0f) {  // rescale before token i + 1: its dot products scale alike
+          scale_state<R, NC>(y, fac);
 #pragma unroll
-          for (int c = 0; c < NC; ++c) {
-#pragma unroll
-            for (int r = 0; r < R; ++r) y[c][r] *= fac;
-            d[c] *= fac;
-          }
+          for (int c = 0; c < NC; ++c) d[c] *= fac;
         }
       } else {
         token_pass<R, NC, true, false>(y, kc, cc, nullptr, d);
@@ -306,9 +326,10 @@ __global__ void __launch_bounds__(kLocalThreads, 6) local_pass_kernel(const Loca
       for (int r = 0; r < R; ++r) {
         float* dst = h + (int64_t)(row0 + r) * V + gc;
         if constexpr (NC == 4)
-          *reinterpret_cast<float4*>(dst) = make_float4(y[0][r] * s, y[1][r] * s, y[2][r] * s, y[3][r] * s);
+          *reinterpret_cast<float4*>(dst) = make_float4(yat<R, NC>(y, 0, r) * s, yat<R, NC>(y, 1, r) * s,
+                                                        yat<R, NC>(y, 2, r) * s, yat<R, NC>(y, 3, r) * s);
         else
-          *reinterpret_cast<float2*>(dst) = make_float2(y[0][r] * s, y[1][r] * s);
+          *reinterpret_cast<float2*>(dst) = make_float2(yat<R, NC>(y, 0, r) * s, yat<R, NC>(y, 1, r) * s);
       }
     } else {  // vk: H[v][k], R consecutive rows per column
 #pragma unroll
@@ -316,8 +337,8 @@ __global__ void __launch_bounds__(kLocalThreads, 6) local_pass_kernel(const Loca
         float* dst = h + (int64_t)(gc + c) * K + row0;
 #pragma unroll
         for (int r = 0; r < R; r += 4)
-          *reinterpret_cast<float4*>(dst + r) =
-              make_float4(y[c][r] * s, y[c][r + 1] * s, y[c][r + 2] * s, y[c][r + 3] * s);
+          *reinterpret_cast<float4*>(dst + r) = make_float4(y[c][r / 2].x * s, y[c][r / 2].y * s,
+                                                            y[c][r / 2 + 1].x * s, y[c][r / 2 + 1].y * s);
       }
     }
   } else {
@@ -326,9 +347,10 @@ __global__ void __launch_bounds__(kLocalThreads, 6) local_pass_kernel(const Loca
     for (int r = 0; r < R; ++r) {
       float* dst = m + (int64_t)(row0 + r) * K + mc;
       if constexpr (NC == 4)
-        *reinterpret_cast<float4*>(dst) = make_float4(y[0][r] * s, y[1][r] * s, y[2][r] * s, y[3][r] * s);
+        *reinterpret_cast<float4*>(dst) = make_float4(yat<R, NC>(y, 0, r) * s, yat<R, NC>(y, 1, r) * s,
+                                                      yat<R, NC>(y, 2, r) * s, yat<R, NC>(y, 3, r) * s);
       else
-        *reinterpret_cast<float2*>(dst) = make_float2(y[0][r] * s, y[1][r] * s);
+        *reinterpret_cast<float2*>(dst) = make_float2(yat<R, NC>(y, 0, r) * s, yat<R, NC>(y, 1, r) * s);
     }
   }
 }
