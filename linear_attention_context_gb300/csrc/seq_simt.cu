@@ -240,11 +240,11 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
     for (int q = 0; q < R; ++q)
       *reinterpret_cast<float4*>(Xs + (k0 + q) * kXsLd + cg * 4) = make_float4(x[q][0], x[q][1], x[q][2], x[q][3]);
 
-    float acc[R][4];
+    // acc[q][p] holds columns 2p, 2p + 1 of row q: packed fma.rn.f32x2, each
+    // half rounded as a scalar FMA
+    float2 acc[R][2];
 #pragma unroll
-    for (int q = 0; q < R; ++q)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[q][e] = 0.f;
+    for (int q = 0; q < R; ++q) acc[q][0] = acc[q][1] = make_float2(0.f, 0.f);
 
     for (int kb = 0; kb < CH; ++kb) {
       const int c = jj * CH + kb;
@@ -258,21 +258,24 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
 #pragma unroll 8
       for (int kk = 0; kk < 32; ++kk) {
         const float4 xv = *reinterpret_cast<const float4*>(Xs + (kc + kk) * kXsLd + cg * 4);
+        const float2 x01 = make_float2(xv.x, xv.y), x23 = make_float2(xv.z, xv.w);
         float a[R];
         load_run<R>(A + kk * SL, a);  // A[k0 .. k0 + R - 1][kc + kk]
 #pragma unroll
         for (int q = 0; q < R; ++q) {
-          acc[q][0] = fmaf(a[q], xv.x, acc[q][0]);
-          acc[q][1] = fmaf(a[q], xv.y, acc[q][1]);
-          acc[q][2] = fmaf(a[q], xv.z, acc[q][2]);
-          acc[q][3] = fmaf(a[q], xv.w, acc[q][3]);
+          const float2 aq = make_float2(a[q], a[q]);
+          acc[q][0] = __ffma2_rn(aq, x01, acc[q][0]);
+          acc[q][1] = __ffma2_rn(aq, x23, acc[q][1]);
         }
       }
     }
 #pragma unroll
-    for (int q = 0; q < R; ++q)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) x[q][e] = acc[q][e] + h[q][e];
+    for (int q = 0; q < R; ++q) {
+      x[q][0] = acc[q][0].x + h[q][0];
+      x[q][1] = acc[q][0].y + h[q][1];
+      x[q][2] = acc[q][1].x + h[q][2];
+      x[q][3] = acc[q][1].y + h[q][3];
+    }
   }
   cp_async_wait<0>();  // no copy may land after the CTA is gone
   griddep_launch_dependents();
@@ -433,11 +436,13 @@ __global__ void __launch_bounds__(2 * K) seq_simt_ksplit_kernel(const SeqJob j) 
     __syncthreads();     // everyone's, and the state tile is written; step jj-1 is done with copy (jj+1)&1
     if (jj + 1 < nsteps) issue_a(jj + 1);
 
-    float acc[8][8];
+    // acc[r][p] holds columns 2p, 2p + 1 of row r: packed fma.rn.f32x2, each
+    // half rounded as a scalar FMA, half the FMA instructions
+    float2 acc[8][4];
 #pragma unroll
     for (int r = 0; r < 8; ++r)
 #pragma unroll
-      for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+      for (int c = 0; c < 4; ++c) acc[r][c] = make_float2(0.f, 0.f);
     const float* A = As0 + (jj & 1) * K * AL + kg * KR * AL + rb * 8;
     const float* X = Xs + kg * KR * kPld + cb * 8;
 #pragma unroll 4
@@ -447,19 +452,23 @@ __global__ void __launch_bounds__(2 * K) seq_simt_ksplit_kernel(const SeqJob j) 
       const float4 x0 = *reinterpret_cast<const float4*>(X + k * kPld);
       const float4 x1 = *reinterpret_cast<const float4*>(X + k * kPld + 4);
       const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const float2 xp[4] = {make_float2(x0.x, x0.y), make_float2(x0.z, x0.w), make_float2(x1.x, x1.y),
+                            make_float2(x1.z, x1.w)};
 #pragma unroll
-      for (int r = 0; r < 8; ++r)
+      for (int r = 0; r < 8; ++r) {
+        const float2 ar = make_float2(av[r], av[r]);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av[r], xv[c], acc[r][c]);
+        for (int c = 0; c < 4; ++c) acc[r][c] = __ffma2_rn(ar, xp[c], acc[r][c]);
+      }
     }
     // partial blocks -> shared memory; the owners add them (k-groups in order) and H
     float* P = Ps + kg * K * kPld;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-      *reinterpret_cast<float4*>(P + pidx(rb * 8 + r, cb * 8)) = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+      *reinterpret_cast<float4*>(P + pidx(rb * 8 + r, cb * 8)) =
+          make_float4(acc[r][0].x, acc[r][0].y, acc[r][1].x, acc[r][1].y);
       *reinterpret_cast<float4*>(P + pidx(rb * 8 + r, cb * 8 + 4)) =
-          make_float4(acc[r][4], acc[r][5], acc[r][6], acc[r][7]);
+          make_float4(acc[r][2].x, acc[r][2].y, acc[r][3].x, acc[r][3].y);
     }
     __syncthreads();
 #pragma unroll
