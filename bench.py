@@ -50,12 +50,12 @@ def algorithmic_bytes(chains, S_, K_, V_, with_init=True):
     return 4 * chains * ((S_ - 1) * K_ * V_ + (S_ - 1) * K_ * K_ + S_ * K_ * V_ + (K_ * V_ if with_init else 0))
 
 
-def scan_groups(S_):
-    """The scan's automatic group count for S segments (G ~ sqrt(2 S), as the
-    library chooses it)."""
-    G = max(1, round(math.sqrt(2.0 * S_)))
-    L = (S_ + G - 1) // G
-    return (S_ + L - 1) // L
+def scan_groups(heads, S_, K_, V_):
+    """The scan's automatic group count on the current device, read back from
+    the library's scratch size (chains x groups x (K^2 + 2 K V) floats)."""
+    import linear_attention_context_gb300 as qla
+    per_group = heads * (K_ * K_ + 2 * K_ * V_) * 4
+    return qla.scan_workspace_bytes(1, heads, S_, K_, V_) // per_group
 
 
 def algorithmic_flops(chains, S_, K_, V_):
@@ -588,7 +588,7 @@ def run_sweep(args):
             # products of M, S steps of K^3; group recurrences (S steps),
             # carries (G) and re-runs (S - G), K^2 V each
             Kk = Vv = 128
-            G = scan_groups(S_)
+            G = scan_groups(heads, S_, Kk, Vv)
             flops = 3 * 2 * heads * (S_ * Kk ** 3 + 2 * S_ * Kk * Kk * Vv)
             rate = flops / (times["scan"] * 1e-6) / 1e12
             lines.append({"sweep": {"heads": heads, "S": S_, "layout": layout, "direction": direction},

@@ -132,7 +132,13 @@ QLA_API int qla_cp_correct(const float* H, const float* M, const float* h_init, 
  *   variant      QLA_VARIANT_*;  engine QLA_ENGINE_*;  release QLA_RELEASE_*
  *                (ignored by engines without a TMA producer).
  *   scan_group   number of scan groups G (QLA_VARIANT_SCAN), 0 = automatic;
- *                each group covers ceil(S / G) consecutive segments.
+ *                each group covers ceil(S / G) consecutive segments.  The
+ *                automatic G is at most round(sqrt(2 S)) and fewer where the
+ *                phases' CTAs (one per chain, group and 32-column tile) would
+ *                run in several waves on the device's SMs.
+ * QLA_VARIANT_AUTO takes the scan where a cost model of both variants (fitted
+ * to GB300 timings at K = V = 128; qla_resolve reports the choice) rates it
+ * below 0.95 of the sequential kernel: long chains with few heads.
  * The scan variant needs qla_scan_workspace_bytes() of device scratch, which
  * it takes from the stream-ordered allocator (cudaMallocAsync on `stream`) and
  * returns on the same stream.
@@ -181,8 +187,8 @@ QLA_API int qla_cp_correct_varlen(const float* H, const float* M, const float* h
  * are empty (their aggregates are the identity and zero).  A sequence longer
  * than max_segments is treated like invalid offsets: bit 1 of the device
  * status word is set and that chain's outputs are left unspecified.
- * variant QLA_VARIANT_AUTO picks the scan when max_segments >= 24 and
- * N * heads * ceil(V / 32) <= 16 (as qla_resolve for fixed lengths).  The scan
+ * variant QLA_VARIANT_AUTO decides as for fixed lengths with S = max_segments
+ * and N * heads chains (qla_resolve).  The scan
  * allocates its workspace with cudaMallocAsync on `stream`
  * (N * heads * G * (K*K + 2*K*V) * 4 bytes) and frees it the same way.
  */
@@ -192,7 +198,8 @@ QLA_API int qla_cp_correct_varlen_ex(const float* H, const float* M, const float
                           int max_segments, int scan_group, void* stream);
 
 /* Bytes of device scratch the scan variant uses for this shape and group
- * size (0 = automatic); 0 when the scan does not apply. */
+ * size (0 = automatic, for the current device; without a usable device, for
+ * G = round(sqrt(2 S)), which is never less); 0 when the scan does not apply. */
 QLA_API size_t qla_scan_workspace_bytes(int B, int heads, int S, int K, int V, int scan_group);
 
 /* Process-wide override of the automatic variant choice: QLA_VARIANT_SEQ or

@@ -193,12 +193,56 @@ int check_varlen_args(const float* H, const float* M, const float* h_init, const
   return QLA_OK;
 }
 
-// Scan group count for S segments: the critical path is about 2L + G steps
-// with G*L >= S, smallest near G = sqrt(2S).
-int auto_groups(int S) {
-  int G = std::max(1, (int)std::lround(std::sqrt(2.0 * S)));
+// Cost models of the two variants on one-CTA-per-SM launches (each unit and
+// 32-column tile is one CTA of the tensor-core kernel).  A phase that has more
+// CTAs than SMs runs in waves, each costing its steps again.  The scan's model,
+// in us, for G groups of L segments:
+//     4.74 + 1.96 L w1 + 2.01 G w2 + 1.24 L w3,
+// w = waves of phase 1 (products and offsets together, G (K + V) / 32 CTAs per
+// chain), phase 2 (V / 32 per chain) and phase 3 (G V / 32 per chain).  The
+// sequential kernel's is
+//     4.7 + 1.62 (S - 1) w.
+// Both are least-squares fits to calls timed on GB300 at K = V = 128: the scan
+// at 1, 2 and 4 heads, S = 32 .. 128 and every G from 4 to 32; the sequential
+// kernel over S = 2 .. 128.  Within 10 % of the measured time at 1 to 32 heads.
+double waves_of(int64_t ctas, int sms) { return (double)((ctas + sms - 1) / sms); }
+
+double scan_model_us(int S, int G, int64_t chains, int K, int V, int sms) {
   const int L = (S + G - 1) / G;
-  return (S + L - 1) / L;
+  const int Gr = (S + L - 1) / L;
+  return 4.74 + 1.96 * L * waves_of(chains * Gr * ((K + V) / 32), sms) + 2.01 * Gr * waves_of(chains * (V / 32), sms) +
+         1.24 * L * waves_of(chains * Gr * (V / 32), sms);
+}
+
+double seq_model_us(int S, int64_t chains, int V, int sms) {
+  return 4.7 + 1.62 * (S - 1) * waves_of(chains * ((V + 31) / 32), sms);
+}
+
+// Scan group count for S segments of `chains` chains.  The critical path is
+// about 2L + G steps with G*L >= S, smallest near G = sqrt(2S); with more
+// chains the phases with G units per chain run in several waves, so fewer
+// groups can be faster.  Among the group counts up to sqrt(2S) (never more
+// scratch than that choice), the one the scan's model rates fastest; it picks
+// the fastest measured G at each of the points it was fitted on.  Without the
+// SM count (sms <= 0), the step-count balance alone.
+int auto_groups(int S, int64_t chains, int K, int V, int sms) {
+  const int G0 = std::max(1, (int)std::lround(std::sqrt(2.0 * S)));
+  if (sms <= 0 || chains <= 0) {
+    const int L = (S + G0 - 1) / G0;
+    return (S + L - 1) / L;
+  }
+  int best = 1;
+  double best_cost = 0.0;
+  for (int G = 1; G <= std::min(G0, S); ++G) {
+    const int L = (S + G - 1) / G;
+    if ((S + L - 1) / L != G) continue;  // the same (L, Gr) as a smaller G
+    const double cost = scan_model_us(S, G, chains, K, V, sms);
+    if (G == 1 || cost < best_cost) {
+      best = G;
+      best_cost = cost;
+    }
+  }
+  return best;
 }
 
 bool known_engine(int engine) {
@@ -276,13 +320,18 @@ SeqJob dependent(SeqJob j) {
   return j;
 }
 
+// Automatic variant: the scan where its model (with its automatic group
+// count) is below 0.95 of the sequential kernel's, else the sequential kernel.
+// The margin covers the scan's extra launches where the two are close.
 int resolve_variant(const Shape& s, int variant, const DeviceInfo* d) {
-  (void)d;
   if (variant != QLA_VARIANT_AUTO) return variant;
   const int forced = variant_override();
   if (forced != QLA_VARIANT_AUTO) return forced;
-  const int64_t tiles = s.chains() * ((s.V + 31) / 32);
-  return (s.S >= 24 && tiles <= 16) ? QLA_VARIANT_SCAN : QLA_VARIANT_SEQ;
+  if (s.S < 2 || d->sm_count < 1) return QLA_VARIANT_SEQ;
+  const int64_t chains = s.chains();
+  const int G = auto_groups(s.S, chains, s.K, s.V, d->sm_count);
+  const double scan = scan_model_us(s.S, G, chains, s.K, s.V, d->sm_count);
+  return scan < 0.95 * seq_model_us(s.S, chains, s.V, d->sm_count) ? QLA_VARIANT_SCAN : QLA_VARIANT_SEQ;
 }
 
 int launch_seq(const SeqJob& job, int engine, int release, const DeviceInfo* d, cudaStream_t stream) {
@@ -435,10 +484,11 @@ int scan_phases(const SeqJob& base, const Shape& s, int L, int Gr, float* ws, in
   return QLA_OK;
 }
 
-// Group length L and the number of groups actually formed for S segments and
-// a requested group count (0: automatic).
-void scan_groups_for(int S, int group, int* L, int* Gr) {
-  const int G = group > 0 ? std::min(group, S) : auto_groups(S);
+// Group length L and the number of groups actually formed for S segments of
+// `chains` chains and a requested group count (0: automatic, for a device
+// with `sms` SMs).
+void scan_groups_for(int S, int group, int64_t chains, int K, int V, int sms, int* L, int* Gr) {
+  const int G = group > 0 ? std::min(group, S) : auto_groups(S, chains, K, V, sms);
   *L = (S + G - 1) / G;
   *Gr = (S + *L - 1) / *L;
 }
@@ -447,7 +497,7 @@ void scan_groups_for(int S, int group, int* L, int* Gr) {
 int run_scan_alloc(const SeqJob& base, const Shape& s, int engine, int release, int group, const DeviceInfo* d,
                    cudaStream_t stream) {
   int L, Gr;
-  scan_groups_for(s.S, group, &L, &Gr);
+  scan_groups_for(s.S, group, base.nchains, s.K, s.V, d->sm_count, &L, &Gr);
   const size_t bytes = (size_t)base.nchains * Gr * ((size_t)s.K * s.K + 2 * (size_t)s.state()) * sizeof(float);
   float* ws = nullptr;
   cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), bytes, stream);
@@ -602,7 +652,7 @@ int scan_static_pointer(float** out) {
 int run_scan_in(const float* H, const float* M, const float* h_init, float* out, float* fin, const Shape& s,
                 int engine, int release, int group, float* ws, const DeviceInfo* d, cudaStream_t stream) {
   int L, Gr;
-  scan_groups_for(s.S, group, &L, &Gr);
+  scan_groups_for(s.S, group, (int64_t)s.B * s.heads, s.K, s.V, d->sm_count, &L, &Gr);
   return scan_phases(plain_job(H, M, h_init, out, fin, s), s, L, Gr, ws, engine, release, d, stream);
 }
 
@@ -651,16 +701,16 @@ int qla_cp_correct_scan_static(const float* H, const float* M, const float* h_in
   if (release < QLA_RELEASE_MEMBAR || release > QLA_RELEASE_NONE)
     return fail(QLA_ERR_INVALID_ARG, "unknown release mode %d", release);
   if (scan_group < 0) return fail(QLA_ERR_INVALID_ARG, "scan_group must be >= 0");
+  DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != QLA_OK) return st;
   int L, Gr;
-  scan_groups_for(S, scan_group, &L, &Gr);
+  scan_groups_for(S, scan_group, (int64_t)B * heads, K, V, d->sm_count, &L, &Gr);
   const size_t need = scan_bytes(s, Gr);
   if (need > QLA_SCAN_STATIC_BYTES)
     return fail(QLA_ERR_UNSUPPORTED,
                 "this shape needs %zu bytes of scan scratch; the allocation-free scan holds %u bytes "
                 "(use qla_cp_correct_ex with QLA_VARIANT_SCAN instead)",
                 need, (unsigned)QLA_SCAN_STATIC_BYTES);
-  DeviceInfo* d = nullptr;
-  if ((st = current_device(&d)) != QLA_OK) return st;
   float* ws = nullptr;
   if ((st = scan_static_pointer(&ws)) != QLA_OK) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -688,8 +738,15 @@ const char* qla_last_error(void) { return t_last_error.c_str(); }
 size_t qla_scan_workspace_bytes(int B, int heads, int S, int K, int V, int scan_group) {
   if (B < 1 || heads < 1 || S < 1 || K < 1 || V < 1) return 0;
   Shape s{B, heads, S, K, V, 0, 0};
+  // the automatic group count depends on the current device's SM count;
+  // without a usable device, the step-count rule (never fewer groups, so
+  // never less scratch)
+  int sms = 0;
+  DeviceInfo* d = nullptr;
+  if (current_device(&d) == QLA_OK) sms = d->sm_count;
+  t_last_error.clear();
   int L, Gr;
-  scan_groups_for(S, scan_group, &L, &Gr);
+  scan_groups_for(S, scan_group, (int64_t)B * heads, K, V, sms, &L, &Gr);
   return scan_bytes(s, Gr);
 }
 
@@ -797,7 +854,7 @@ int qla_cp_correct_varlen_ex(const float* H, const float* M, const float* h_init
   j.nstates = (int64_t)heads * T;
   if (var == QLA_VARIANT_SEQ || Smax < 2) return launch_seq(dependent(j), eng, QLA_RELEASE_MEMBAR, d, cs);
   int L, Gr;
-  scan_groups_for(s.S, scan_group, &L, &Gr);
+  scan_groups_for(s.S, scan_group, (int64_t)N * heads, K, V, d->sm_count, &L, &Gr);
   if ((int64_t)N * heads * Gr * (V / 32) > 0x7fffffff)
     return fail(QLA_ERR_UNSUPPORTED, "N*heads*G*(V/32) must be below 2^31 for the scan variant");
   return run_scan_varlen(j, s, eng, scan_group, d, cs);
