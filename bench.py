@@ -276,6 +276,8 @@ def run_ours(args):
         bufs.append(row)
     stream = torch.cuda.Stream(dev)
     kw = dict(engine=args.engine, variant=args.variant, release=args.release)
+    if args.dependent_launch:
+        qla.set_dependent_launch(True)
 
     def call(b, s=None):
         qla.cp_correct(b["H"], b["M"], b["h0"], b["out"], layout=b["layout"], direction=b["direction"],
@@ -438,6 +440,7 @@ def run_ours(args):
                        "l2_defeat": f"inputs larger than L2: {reps} rotating replicas x {len(CALLS)} calls "
                                     f"({reps * len(CALLS) * per_call / 1e6:.0f} MB) vs L2 {l2 / 1e6:.0f} MB",
                        "graph": f"CUDA graphs of {G} steps ({G * len(CALLS)} calls) replayed back to back",
+                       "dependent_launch": bool(args.dependent_launch),
                        "parallelism": f"replicas x{world} (no collective)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4),
@@ -937,6 +940,8 @@ def main():
     ap.add_argument("--configs", action="store_true", help="time configs 0-2 one at a time")
     ap.add_argument("--local", action="store_true", help="time the per-segment local pass and its chain into the correction")
     ap.add_argument("--accuracy", action="store_true", help="worst per-state error against the oracle, per config")
+    ap.add_argument("--dependent-launch", action="store_true",
+                    help="launch every correction call as a programmatic dependent of the previous one")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
