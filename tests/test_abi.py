@@ -256,3 +256,16 @@ def test_local_pass_split_checks(L, split):
 def test_local_pass_valid_splits_without_gpu(L):
     for split in (0, 1, 2, 16):
         assert call_local_ex(L, split) == -5
+
+
+@no_gpu_only
+def test_automatic_scan_groups_without_a_device_take_the_step_count_rule(L):
+    """Without a usable device the automatic group count is round(sqrt(2 S)),
+    as many groups as the SM-aware rule ever takes (so the scratch size is an
+    upper bound)."""
+    import math
+    for S in (2, 10, 32, 64, 128, 200):
+        G = max(1, round(math.sqrt(2 * S)))
+        Ls = -(-S // G)
+        Gr = -(-S // Ls)
+        assert L.qla_scan_workspace_bytes(1, 4, S, 128, 128, 0) == 4 * Gr * (128 * 128 + 2 * 128 * 128) * 4

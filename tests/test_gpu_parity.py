@@ -391,3 +391,33 @@ def test_automatic_choice_keeps_the_bar_on_long_undecayed_chains(K, S):
             got, fin = run(H, M, h0, "kv", direction, engine="auto", variant=variant, final=True)
             assert_parity(got, ref, what=f"auto engine K={K} S={S} {direction} {variant}")
             assert_parity(fin, rfin, what=f"auto engine final K={K} S={S} {direction} {variant}")
+
+
+def _scan_model(S, G, chains, K, V, sms):
+    # the documented cost models of the two variants (us); waves of one-CTA-per-SM phases
+    w = lambda n: -(-n // sms)  # noqa: E731
+    Ls = -(-S // G)
+    Gr = -(-S // Ls)
+    return (4.74 + 1.96 * Ls * w(chains * Gr * ((K + V) // 32)) + 2.01 * Gr * w(chains * (V // 32))
+            + 1.24 * Ls * w(chains * Gr * (V // 32)))
+
+
+@pytest.mark.parametrize("heads,S", [(1, 32), (1, 128), (2, 128), (4, 32), (4, 128), (8, 64), (8, 128),
+                                     (16, 128), (32, 8), (32, 128), (4, 16), (1, 3)])
+def test_automatic_scan_groups_and_variant_follow_the_cost_models(heads, S):
+    """The automatic group count (read back from the scratch size) is the cost
+    model's fastest G up to round(sqrt(2 S)), and the automatic variant is the
+    scan exactly where that model is below 0.95 of the sequential kernel's."""
+    import math
+    import torch
+    import linear_attention_context_gb300 as qla
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    K = V = 128
+    G0 = max(1, round(math.sqrt(2 * S)))
+    cands = [G for G in range(1, min(G0, S) + 1) if -(-S // -(-S // G)) == G]
+    best = min(cands, key=lambda G: (_scan_model(S, G, heads, K, V, sms), G))
+    per_group = heads * (K * K + 2 * K * V) * 4
+    assert qla.scan_workspace_bytes(1, heads, S, K, V) == best * per_group
+    seq = 4.7 + 1.62 * (S - 1) * -(-(heads * (V // 32)) // sms)
+    want = "scan" if S >= 2 and _scan_model(S, best, heads, K, V, sms) < 0.95 * seq else "seq"
+    assert qla.resolve(1, heads, S, K, V)[0] == want
