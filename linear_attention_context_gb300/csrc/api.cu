@@ -537,12 +537,10 @@ int local_auto_split(const LocalJob& j, const DeviceInfo* d, int* F) {
     LocalJob t = j;
     t.S = j.S * f;
     t.L = j.L / f;
-    // the split always computes the sub-segments' M (H only if H is wanted);
-    // the pointer only sets the column count of the query
-    if (f > 1 && !t.M) t.M = reinterpret_cast<float*>(16);
+    // the split always computes the sub-segments' M (H only if H is wanted)
     int64_t ctas = 0;
     int per_sm = 0;
-    const cudaError_t e = local_grid_info(t, &ctas, &per_sm);
+    const cudaError_t e = local_grid_info(t, t.H != nullptr, f > 1 || t.M != nullptr, &ctas, &per_sm);
     if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
     if (per_sm < 1) per_sm = 1;
     const int64_t slots = (int64_t)per_sm * d->sm_count;

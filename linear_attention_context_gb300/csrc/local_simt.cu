@@ -366,8 +366,8 @@ size_t smem_rg(const LocalJob& j) {
 
 // CTAs of a launch, and how many fit on one SM at once.
 template <int R, int G, int NC>
-cudaError_t info_rg(const LocalJob& j, int64_t* ctas, int* per_sm) {
-  const int cols = (j.H ? j.V : 0) + (j.M ? j.K : 0);
+cudaError_t info_rg(const LocalJob& j, bool with_h, bool with_m, int64_t* ctas, int* per_sm) {
+  const int cols = (with_h ? j.V : 0) + (with_m ? j.K : 0);
   const int per_cta = kLocalWarps * NC * (32 / G);
   *ctas = (int64_t)j.nchains * j.S * ((cols + per_cta - 1) / per_cta);
   const size_t smem = smem_rg<R, G, NC>(j);
@@ -406,16 +406,16 @@ cudaError_t launch_rg(const LocalJob& j, cudaStream_t stream) {
 // dimension K (a multiple of 32 up to 256): four columns of 32 or fewer rows
 // up to K = 128 (each key value read feeds four FMAs per use), two columns of
 // at most 64 rows above.
-cudaError_t local_grid_info(const LocalJob& j, int64_t* ctas, int* per_sm) {
+cudaError_t local_grid_info(const LocalJob& j, bool with_h, bool with_m, int64_t* ctas, int* per_sm) {
   switch (j.K) {
-    case 32: return info_rg<32, 1, 4>(j, ctas, per_sm);
-    case 64: return info_rg<32, 2, 4>(j, ctas, per_sm);
-    case 96: return info_rg<24, 4, 4>(j, ctas, per_sm);
-    case 128: return info_rg<32, 4, 4>(j, ctas, per_sm);
-    case 160: return info_rg<40, 4, 2>(j, ctas, per_sm);
-    case 192: return info_rg<48, 4, 2>(j, ctas, per_sm);
-    case 224: return info_rg<56, 4, 2>(j, ctas, per_sm);
-    case 256: return info_rg<64, 4, 2>(j, ctas, per_sm);
+    case 32: return info_rg<32, 1, 4>(j, with_h, with_m, ctas, per_sm);
+    case 64: return info_rg<32, 2, 4>(j, with_h, with_m, ctas, per_sm);
+    case 96: return info_rg<24, 4, 4>(j, with_h, with_m, ctas, per_sm);
+    case 128: return info_rg<32, 4, 4>(j, with_h, with_m, ctas, per_sm);
+    case 160: return info_rg<40, 4, 2>(j, with_h, with_m, ctas, per_sm);
+    case 192: return info_rg<48, 4, 2>(j, with_h, with_m, ctas, per_sm);
+    case 224: return info_rg<56, 4, 2>(j, with_h, with_m, ctas, per_sm);
+    case 256: return info_rg<64, 4, 2>(j, with_h, with_m, ctas, per_sm);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -152,8 +152,9 @@ struct LocalJob {
   int pdl;            // launch as a programmatic dependent of the stream's previous kernel
 };
 cudaError_t launch_local_simt(const LocalJob& job, cudaStream_t stream);
-// The launch's CTA count and how many of its CTAs fit on one SM at once.
-cudaError_t local_grid_info(const LocalJob& job, int64_t* ctas, int* per_sm);
+// The CTA count of a launch computing the H columns (with_h) and/or the M
+// columns (with_m) of `job`'s units, and how many of its CTAs fit on one SM.
+cudaError_t local_grid_info(const LocalJob& job, bool with_h, bool with_m, int64_t* ctas, int* per_sm);
 
 // Bound on every device-side wait of the pipelined engines.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
