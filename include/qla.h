@@ -360,8 +360,10 @@ QLA_API int qla_local_pass(const void* k, const void* v, const float* beta, cons
  * B*heads*S*F*(K*K + K*V)*4 bytes of device scratch from the stream-ordered
  * allocator (cudaMallocAsync on `stream`, returned the same way).
  *   split  0: automatic (the F in {1, 2, 4, 8, 16} that minimises the
- *          estimated time, from the launch's occupancy on this device);
- *          otherwise F, which must divide L = T / S.
+ *          estimated time, from the launch's occupancy on this device;
+ *          when its scratch cannot be allocated, the pass runs unsplit);
+ *          otherwise F, which must divide L = T / S (an allocation failure
+ *          is then returned as QLA_ERR_CUDA, with nothing launched).
  * qla_local_pass is split = 0.
  */
 QLA_API int qla_local_pass_ex(const void* k, const void* v, const float* beta, const float* g, float* H, float* M,

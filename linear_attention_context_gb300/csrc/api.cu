@@ -533,7 +533,7 @@ int local_auto_split(const LocalJob& j, const DeviceInfo* d, int* F) {
   if (d->sm_count < 1) return QLA_OK;
   double best = 0.0;
   for (int f = 1; f <= 16; f *= 2) {
-    if (j.L % f || j.L / f < 64) break;
+    if (j.L % f || j.L / f < 64 || (int64_t)j.nchains * j.S * f > 0x7fffffff) break;
     LocalJob t = j;
     t.S = j.S * f;
     t.L = j.L / f;
@@ -558,14 +558,19 @@ int local_auto_split(const LocalJob& j, const DeviceInfo* d, int* F) {
   return QLA_OK;
 }
 
-int local_pass_split(const LocalJob& j, int F, const DeviceInfo* d, cudaStream_t stream) {
+// `no_scratch` (optional) is set when the sub-segments' scratch could not be
+// allocated; nothing was launched then.
+int local_pass_split(const LocalJob& j, int F, const DeviceInfo* d, cudaStream_t stream, bool* no_scratch) {
   const int64_t units = (int64_t)j.nchains * j.S * F;  // sub-segments
   const size_t hbytes = (size_t)units * j.K * j.V * sizeof(float);
   const size_t mbytes = (size_t)units * j.K * j.K * sizeof(float);
   const bool need_h = j.H != nullptr;
   float* ws = nullptr;
   cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), (need_h ? hbytes : 0) + mbytes, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(local pass sub-segments)");
+  if (e != cudaSuccess) {
+    if (no_scratch) *no_scratch = true;
+    return cuda_fail(e, "cudaMallocAsync(local pass sub-segments)");
+  }
   float* Ms = ws;
   float* Hs = need_h ? ws + (size_t)units * j.K * j.K : nullptr;
   LocalJob t = j;
@@ -922,11 +927,16 @@ int qla_local_pass_ex(const void* k, const void* v, const float* beta, const flo
   j.pdl = dependent_launch();
   int F = split;
   if (F == 0 && (st = local_auto_split(j, d, &F)) != QLA_OK) return st;
-  if (F == 1) {
-    const cudaError_t e = launch_local_simt(j, cs);
-    return e == cudaSuccess ? QLA_OK : cuda_fail(e, "kernel launch");
+  if (F > 1) {
+    bool no_scratch = false;
+    st = local_pass_split(j, F, d, cs, &no_scratch);
+    // an automatic split that finds no memory for its scratch runs unsplit
+    if (!(split == 0 && no_scratch)) return st;
+    cudaGetLastError();
+    t_last_error.clear();
   }
-  return local_pass_split(j, F, d, cs);
+  const cudaError_t e = launch_local_simt(j, cs);
+  return e == cudaSuccess ? QLA_OK : cuda_fail(e, "kernel launch");
 }
 
 int qla_device_status(int* flags) {
