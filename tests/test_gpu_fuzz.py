@@ -3,10 +3,12 @@
 The state correction: shapes (K, V in 32 .. 256, S in 1 .. 40, B and heads),
 M families, both layouts and directions, every engine that takes the shape,
 both variants with random scan group counts, in place or not, a null h_init,
-and the final state.  The local pass: widths, segment counts and lengths,
-decay and write-strength ranges, layouts, H or M alone, and sub-segment
-splits.  Each case comes from a fixed seed, so a failure names a
-reproducible configuration; the bar is the parity bar of the other tests.
+and the final state; long chains across the tensor-core engine's length
+limit under the automatic choice; variable-length batches.  The local pass:
+widths, segment counts and lengths, decay and write-strength ranges,
+layouts, H or M alone, and sub-segment splits.  Each case comes from a fixed
+seed, so a failure names a reproducible configuration; the bar is the parity
+bar of the other tests.
 """
 import numpy as np
 import pytest
@@ -99,3 +101,56 @@ def test_local_pass_random_configuration(i):
         assert_parity(M.cpu().numpy().astype(np.float64), Mr, what=what + " M")
     else:
         assert M is None
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_long_chain_random_configuration(i):
+    """Chains of 40 to 200 segments (K <= 128) or 20 to 70 (K = 256) with the
+    automatic engine, across the tensor-core engine's length limit, in either
+    variant: the automatic choice must keep the bar."""
+    r = np.random.default_rng(11000 + i)
+    K = int(r.choice([64, 96, 128, 128, 256]))
+    V = int(r.choice([32, 64, 128]))
+    S = int(r.integers(40, 201)) if K <= 128 else int(r.integers(20, 71))
+    heads = int(r.integers(1, 5))
+    layout = str(r.choice(["kv", "vk"]))
+    direction = str(r.choice(["fwd", "rev"]))
+    variant = str(r.choice(["auto", "seq", "scan"]))
+    c = qi.Case(B=1, heads=heads, S=S, K=K, V=V, seed=600 + i, m_kind=str(r.choice(["householder", "orthogonal"])),
+                h_scale=0.3, init_scale=0.3)
+    H, M, h0 = qi.make_inputs(c, layout)
+    ref, rfin = oracle.cp_correct(H, M, h0, layout, direction, want_final=True)
+    out, fin = run(H, M, h0, layout, direction, variant=variant, final=True)
+    what = f"long case {i}: heads={heads} S={S} K={K} V={V} {c.m_kind} {layout}/{direction} {variant}"
+    assert_parity(out, ref, what=what)
+    assert_parity(fin, rfin, what=what + " final")
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_varlen_random_configuration(i):
+    """Variable-length batches: up to 8 sequences of 0 to 39 segments, every
+    engine that takes the shape, both variants, with and without initial
+    states."""
+    from test_gpu_varlen import _run as run_varlen
+    r = np.random.default_rng(12000 + i)
+    K = int(r.choice([64, 128, 256]))
+    V = int(r.choice([32, 64, 128]))
+    lengths = [int(x) for x in r.integers(0, 40, size=int(r.integers(1, 9)))]
+    if sum(lengths) == 0:
+        lengths[0] = 1
+    heads = int(r.integers(1, 4))
+    layout = str(r.choice(["kv", "vk"]))
+    direction = str(r.choice(["fwd", "rev"]))
+    engine = str(r.choice(["auto", "simt"] + (["tc"] if engine_supports("tc", K, V) else [])))
+    variant = str(r.choice(["auto", "seq", "scan"]))
+    with_init = bool(r.integers(0, 2))
+    H, M, h0, cu = qi.make_varlen_inputs(lengths, heads, K, V, seed=800 + i, layout=layout, m_kind="orthogonal",
+                                         h_scale=0.2, init_scale=0.2, with_init=with_init)
+    ref, rfin = oracle.cp_correct_varlen(H, M, h0, cu, layout, direction)
+    kw = {"variant": variant}
+    if variant != "seq":
+        kw["max_segments"] = max(lengths)
+    got, fin = run_varlen(H, M, h0, cu, layout, direction, engine, **kw)
+    what = f"varlen case {i}: {lengths} heads={heads} K={K} V={V} {layout}/{direction} {engine} {variant}"
+    assert_parity(got, ref, what=what)
+    assert_parity(fin, rfin, what=what + " final")
