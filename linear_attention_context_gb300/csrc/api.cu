@@ -348,7 +348,7 @@ int launch_seq(const SeqJob& job, int engine, int release, const DeviceInfo* d, 
       e = launch_seq_tc(j, release, d->status_word, kWaitLimitNs, 0, stream);
       break;
     default:
-      return fail(QLA_ERR_UNSUPPORTED, "engine %d is not available in this build", engine);
+      return fail(QLA_ERR_UNSUPPORTED, "engine %d is not compiled into this library", engine);
   }
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return QLA_OK;
