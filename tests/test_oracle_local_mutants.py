@@ -1,8 +1,10 @@
 """Plants mistakes in a copy of the local-pass oracle (on the CPU) and checks
-that the pins of test_oracle_local.py catch each one: the decay applied to the
-write term or left off the propagation matrix, a write strength dropped from
-the removal term, the tokens visited backwards, the propagation matrix started
-from zero, tokens shifted by one, the vk layout left untransposed.
+that the pins of test_oracle_local.py catch each one, and that the
+chunked-form pin of test_oracle_local_chunked.py catches each one on its own:
+the decay applied to the write term or left off the propagation matrix, a
+write strength dropped from the removal term, the tokens visited backwards,
+the propagation matrix started from zero, tokens shifted by one, the vk
+layout left untransposed.
 """
 import os
 import subprocess
@@ -84,3 +86,30 @@ def test_unmutated_local_oracle_passes_battery():
 def test_pins_catch_local_mutant(name):
     variant = build_mutant(name)
     assert not pins_pass(variant), f"mutant {name} slipped through the pins"
+
+
+def chunked_pin_passes(variant):
+    """The chunked-form pin alone (test_oracle_local_chunked.py): the oracle
+    against a triangular solve per chunk, both layouts."""
+    from test_oracle_local_chunked import chunked_local_pass
+    rng = np.random.default_rng(11)
+    for layout in ("kv", "vk"):
+        k, v, b, g = rand_tokens(rng, 12, 4, 3)
+        H, M = oracle.local_pass(k, v, b, g, 2, layout, variant=variant)
+        Hc, Mc = chunked_local_pass(qi.bf16_to_f32(k).astype(np.float64), qi.bf16_to_f32(v).astype(np.float64),
+                                    b, g, 2, 4)
+        if layout == "vk":
+            Hc = np.swapaxes(Hc, -1, -2)
+        if not (np.allclose(H, Hc, rtol=1e-10, atol=1e-12) and np.allclose(M, Mc, rtol=1e-10, atol=1e-12)):
+            return False
+    return True
+
+
+def test_unmutated_local_oracle_passes_chunked_pin():
+    assert chunked_pin_passes("")
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_chunked_pin_catches_local_mutant(name):
+    variant = build_mutant(name)
+    assert not chunked_pin_passes(variant), f"mutant {name} slipped through the chunked-form pin"
