@@ -51,3 +51,21 @@ def run(H, M, h0, layout, direction, engine="auto", variant="auto", in_place=Fal
     o = None if out is None else out.cpu().numpy().astype(np.float64)
     f = None if fin is None else fin.cpu().numpy().astype(np.float64)
     return o, f
+
+
+def run_varlen(H, M, h0, cu, layout, direction, engine, in_place=False, **kw):
+    """Runs the variable-length form on numpy inputs (offsets `cu`, N + 1
+    int32); returns (out, final) as numpy, after checking the device status
+    word."""
+    import torch
+    import linear_attention_context_gb300 as qla
+    Hd, Md, h0d = to_dev(H), to_dev(M), to_dev(h0)
+    cud = to_dev(cu.astype(np.int32))
+    N, heads = len(cu) - 1, H.shape[0]
+    fin = torch.empty((N, heads) + H.shape[2:], device=dev())
+    out = Hd if in_place else None
+    out = qla.cp_correct_varlen(Hd, Md, cud, h0d, out, layout=layout, direction=direction, final_state=fin,
+                                engine=engine, **kw)
+    torch.cuda.synchronize()
+    assert qla.device_status() == 0
+    return out.cpu().numpy(), fin.cpu().numpy()

@@ -15,7 +15,7 @@ import pytest
 
 import oracle
 import qla_inputs as qi
-from gpu_util import engine_supports, run, to_dev
+from gpu_util import engine_supports, run, run_varlen, to_dev
 from qla_check import assert_parity
 
 pytestmark = pytest.mark.gpu
@@ -131,7 +131,6 @@ def test_varlen_random_configuration(i):
     """Variable-length batches: up to 8 sequences of 0 to 39 segments, every
     engine that takes the shape, both variants, with and without initial
     states."""
-    from test_gpu_varlen import _run as run_varlen
     r = np.random.default_rng(12000 + i)
     K = int(r.choice([64, 128, 256]))
     V = int(r.choice([32, 64, 128]))

@@ -12,32 +12,13 @@ import pytest
 import oracle
 import qla_inputs as qi
 from gpu_util import engine_supports, engines_under_test
+from gpu_util import run_varlen as _run
+from gpu_util import to_dev as _dev
 from qla_check import assert_parity
 
 pytestmark = pytest.mark.gpu
 
 LENGTHS = [3, 0, 1, 8, 2, 0, 5, 13]
-
-
-def _dev(a):
-    import torch
-    return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to("cuda:0")
-
-
-def _run(H, M, h0, cu, layout, direction, engine, in_place=False, **kw):
-    import torch
-
-    import linear_attention_context_gb300 as qla
-    Hd, Md, h0d = _dev(H), _dev(M), _dev(h0)
-    cud = _dev(cu.astype(np.int32))
-    N, heads = len(cu) - 1, H.shape[0]
-    fin = torch.empty((N, heads) + H.shape[2:], device="cuda:0")
-    out = Hd if in_place else None
-    out = qla.cp_correct_varlen(Hd, Md, cud, h0d, out, layout=layout, direction=direction, final_state=fin,
-                                engine=engine, **kw)
-    torch.cuda.synchronize()
-    assert qla.device_status() == 0
-    return out.cpu().numpy(), fin.cpu().numpy()
 
 
 @pytest.mark.parametrize("engine", engines_under_test())
