@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(2 * K) seq_simt_ksplit_kernel(const SeqJob j) 
       for (int c = 0; c < 4; ++c) acc[r][c] = make_float2(0.f, 0.f);
     const float* A = As0 + (jj & 1) * K * AL + kg * KR * AL + rb * 8;
     const float* X = Xs + kg * KR * kPld + cb * 8;
-#pragma unroll 4
+#pragma unroll
     for (int k = 0; k < KR; ++k) {
       const float4 a0 = *reinterpret_cast<const float4*>(A + k * AL);
       const float4 a1 = *reinterpret_cast<const float4*>(A + k * AL + 4);
