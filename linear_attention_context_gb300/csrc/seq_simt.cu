@@ -305,6 +305,14 @@ __device__ __forceinline__ int pidx(int row, int col) {
   return row * kPld + ((((col >> 2) ^ (row >> 3)) & 1) | ((col >> 2) & 6)) * 4 + (col & 3);
 }
 
+// Forward A (= M) is kept m-major, A[m][k] in row m, with the 16-byte chunks of
+// odd 8-row blocks swapped in pairs: the two row blocks a quarter-warp reads
+// then fall in different banks (rows a multiple of 16 bytes apart would not).
+template <int AL>
+__device__ __forceinline__ int amx(int m, int k) {
+  return m * AL + ((((k >> 2) ^ (m >> 3)) & 1) | ((k >> 2) & ~1)) * 4 + (k & 3);
+}
+
 template <int K>
 __host__ __device__ constexpr int ks_threads() {
   return 2 * K;
@@ -395,17 +403,16 @@ __global__ void __launch_bounds__(2 * K) seq_simt_ksplit_kernel(const SeqJob j) 
   }
   const int nsteps = n - 1 + (j.fin ? 1 : 0);
   auto seg_of = [&](int jj) { return fwd ? s_lo + jj : s_lo + n - 1 - jj; };
-  // A of step jj into copy jj & 1 as [k][m]: reverse A = M^T, so As[k][m] =
-  // M[k][m] (16-byte copies of M's rows); forward A = M, As[k][m] = M[m][k],
-  // transposed on the way in with 4-byte copies (a warp takes 8 k x 4 m, so
-  // it reads 32-byte runs of M's rows and its shared writes spread over banks).
+  // A of step jj into copy jj & 1, with 16-byte copies of M's rows either
+  // way: reverse A = M^T is kept k-major, As[k][m] = M[k][m]; forward A = M is
+  // kept m-major, As[m][k] = M[m][k] (amx).
   auto issue_a = [&](int jj) {
     const float* Ms = Mc + (int64_t)seg_of(jj) * K * K;
     float* dst = As0 + (jj & 1) * K * AL;
     if (fwd) {
-      for (int e = t; e < K * K; e += NT) {
-        const int k = (e & 7) + 8 * ((e >> 5) % (K / 8)), m = ((e >> 3) & 3) + 4 * (e / (4 * K));
-        cp_async4(dst + k * AL + m, Ms + (int64_t)m * K + k);
+      for (int e = t; e < K * K / 4; e += NT) {
+        const int m = e / (K / 4), k4 = 4 * (e - m * (K / 4));
+        cp_async16(dst + amx<AL>(m, k4), Ms + (int64_t)m * K + k4);
       }
     } else {
       for (int e = t; e < K * K / 4; e += NT) {
@@ -443,8 +450,31 @@ __global__ void __launch_bounds__(2 * K) seq_simt_ksplit_kernel(const SeqJob j) 
     for (int r = 0; r < 8; ++r)
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[r][c] = make_float2(0.f, 0.f);
-    const float* A = As0 + (jj & 1) * K * AL + kg * KR * AL + rb * 8;
     const float* X = Xs + kg * KR * kPld + cb * 8;
+    if (fwd) {  // A m-major: 8 rows x 4 k per step of four k
+      const float* Am = As0 + (jj & 1) * K * AL;
+#pragma unroll
+      for (int k4 = 0; k4 < KR; k4 += 4) {
+        float4 ar[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) ar[r] = *reinterpret_cast<const float4*>(Am + amx<AL>(rb * 8 + r, kg * KR + k4));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const float4 x0 = *reinterpret_cast<const float4*>(X + (k4 + kk) * kPld);
+          const float4 x1 = *reinterpret_cast<const float4*>(X + (k4 + kk) * kPld + 4);
+          const float2 xp[4] = {make_float2(x0.x, x0.y), make_float2(x0.z, x0.w), make_float2(x1.x, x1.y),
+                                make_float2(x1.z, x1.w)};
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const float a = kk == 0 ? ar[r].x : kk == 1 ? ar[r].y : kk == 2 ? ar[r].z : ar[r].w;
+            const float2 ap = make_float2(a, a);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[r][c] = __ffma2_rn(ap, xp[c], acc[r][c]);
+          }
+        }
+      }
+    } else {  // A k-major: 8 rows of one k per step
+    const float* A = As0 + (jj & 1) * K * AL + kg * KR * AL + rb * 8;
 #pragma unroll
     for (int k = 0; k < KR; ++k) {
       const float4 a0 = *reinterpret_cast<const float4*>(A + k * AL);
@@ -460,6 +490,7 @@ __global__ void __launch_bounds__(2 * K) seq_simt_ksplit_kernel(const SeqJob j) 
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[r][c] = __ffma2_rn(ar, xp[c], acc[r][c]);
       }
+    }
     }
     // partial blocks -> shared memory; the owners add them (k-groups in order) and H
     float* P = Ps + kg * K * kPld;
