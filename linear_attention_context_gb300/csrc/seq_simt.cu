@@ -51,18 +51,21 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// One chunk stage holds A[m][kc + kk] k-major, as [32 rows kk][K + 4]: the
-// forward copy transposes M's rows on the way in (element-wise cp.async), the
-// reverse one keeps M's rows.  A thread's R consecutive rows m of one kk are
-// then adjacent, so the compute reads them with vector loads; the 4-float pad
-// keeps those loads 16-byte aligned.
+// A reverse chunk stage holds A[m][kc + kk] = M[kc + kk][m] k-major, as
+// [32 rows kk][K + 4]: a thread's R consecutive rows m of one kk are adjacent,
+// so the compute reads them with vector loads; the 4-float pad keeps those
+// loads 16-byte aligned.
 template <int K>
 __host__ __device__ constexpr int stage_ld() {
   return K + 4;
 }
+// A forward stage holds A[m][kc + kk] = M[m][kc + kk] m-major instead: K rows
+// of the chunk's 32 k, padded to 36 (both copies are 16-byte copies of M's
+// rows, no transposition on the way in).
+constexpr int kStageMLd = 36;
 template <int K>
 __host__ __device__ constexpr int stage_floats() {
-  return 32 * stage_ld<K>();
+  return 32 * stage_ld<K>() > K * kStageMLd ? 32 * stage_ld<K>() : K * kStageMLd;
 }
 
 // R consecutive floats from / to p (aligned to 4 R bytes): float4 pieces when
@@ -107,7 +110,7 @@ __host__ __device__ constexpr int ring_stages() {
 }
 
 template <int R, int LAYOUT>
-__global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
+__global__ void __launch_bounds__(kThreads, 1) seq_simt_kernel(const SeqJob j) {
   constexpr int K = R * 32;
   constexpr int CH = K / 32;  // chunks per step
   constexpr int SL = stage_ld<K>();
@@ -193,23 +196,24 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
   const int nsteps = n - 1 + (j.fin ? 1 : 0);
   const int total = nsteps > 0 ? nsteps * CH : 0;  // chunks over all steps
   auto seg_of = [&](int jj) { return fwd ? s_lo + jj : s_lo + n - 1 - jj; };
-  // Chunk c (step c / CH, k block c % CH) -> stage c % NST as [kk][m], one
-  // 4-byte cp.async per element.  Reverse: A[m][kc + kk] = M[kc + kk][m], and
-  // consecutive threads take consecutive m.  Forward: A[m][kc + kk] =
-  // M[m][kc + kk], transposed on the way in; a warp takes 8 kk x 4 m, so it
-  // reads four 32-byte runs of M's rows and its shared writes, (K + 4) floats
-  // apart per kk, fall in 32 different banks.
+  // Chunk c (step c / CH, k block c % CH) -> stage c % NST, with 16-byte
+  // cp.async copies of M's rows either way.  Reverse: A[m][kc + kk] =
+  // M[kc + kk][m], kept k-major as [kk][m].  Forward: A[m][kc + kk] =
+  // M[m][kc + kk], kept m-major as [m][kk] (rows of kStageMLd); the compute
+  // then reads R rows x 4 k per step of four k.
   auto issue_chunk = [&](int c) {
     const float* Ms = Mc + (int64_t)seg_of(c / CH) * K * K;
     const int kc = (c % CH) * 32;
     float* dst = As + (c % NST) * SF;
-    for (int e = t; e < 32 * K; e += kThreads) {
-      if (fwd) {
-        const int kk = (e & 7) + 8 * ((e >> 5) & 3), m = ((e >> 3) & 3) + 4 * (e >> 7);
-        cp_async4(dst + kk * SL + m, Ms + (int64_t)m * K + kc + kk);
-      } else {
-        const int kk = e / K, m = e - kk * K;
-        cp_async4(dst + kk * SL + m, Ms + (int64_t)(kc + kk) * K + m);
+    if (fwd) {  // m-major: row m holds A[m][kc .. kc + 32), 16-byte copies of M's rows
+      for (int e = t; e < 8 * K; e += kThreads) {
+        const int m = e >> 3, p4 = 4 * (e & 7);
+        cp_async16(dst + m * kStageMLd + p4, Ms + (int64_t)m * K + kc + p4);
+      }
+    } else {  // k-major: row kk holds M[kc + kk][0 .. K), 16-byte copies
+      for (int e = t; e < 8 * K; e += kThreads) {
+        const int kk = e / (K / 4), m4 = 4 * (e - kk * (K / 4));
+        cp_async16(dst + kk * SL + m4, Ms + (int64_t)(kc + kk) * K + m4);
       }
     }
   };
@@ -253,8 +257,30 @@ __global__ void __launch_bounds__(kThreads) seq_simt_kernel(const SeqJob j) {
       cp_async_commit();
       cp_async_wait<D>();  // this thread's copies of chunk c have landed
       __syncthreads();     // everyone's have
-      const float* A = As + (c % NST) * SF + k0;
       const int kc = kb * 32;
+      if (fwd) {  // m-major stage: R rows x 4 k per step of four k
+        const float* Am = As + (c % NST) * SF + k0 * kStageMLd;
+#pragma unroll 2
+        for (int kk4 = 0; kk4 < 32; kk4 += 4) {
+          float4 a4[R];
+#pragma unroll
+          for (int q = 0; q < R; ++q) a4[q] = *reinterpret_cast<const float4*>(Am + q * kStageMLd + kk4);
+#pragma unroll
+          for (int j4 = 0; j4 < 4; ++j4) {
+            const float4 xv = *reinterpret_cast<const float4*>(Xs + (kc + kk4 + j4) * kXsLd + cg * 4);
+            const float2 x01 = make_float2(xv.x, xv.y), x23 = make_float2(xv.z, xv.w);
+#pragma unroll
+            for (int q = 0; q < R; ++q) {
+              const float a = j4 == 0 ? a4[q].x : j4 == 1 ? a4[q].y : j4 == 2 ? a4[q].z : a4[q].w;
+              const float2 aq = make_float2(a, a);
+              acc[q][0] = __ffma2_rn(aq, x01, acc[q][0]);
+              acc[q][1] = __ffma2_rn(aq, x23, acc[q][1]);
+            }
+          }
+        }
+        continue;
+      }
+      const float* A = As + (c % NST) * SF + k0;
 #pragma unroll 8
       for (int kk = 0; kk < 32; ++kk) {
         const float4 xv = *reinterpret_cast<const float4*>(Xs + (kc + kk) * kXsLd + cg * 4);
