@@ -449,14 +449,26 @@ __global__ void __launch_bounds__(2 * K) seq_simt_ksplit_kernel(const SeqJob j) 
     cp_async_commit();
   };
   if (nsteps > 0) issue_a(0);
+  // vk: H of the next step is read one step ahead (its owners' reads are
+  // K-strided, so their latency is long), under the current step's FMAs.  In
+  // place (out == H): each thread reads its H_seg elements before it writes
+  // out[seg] over the same addresses; no other thread touches them.
+  float hn[16];
+  if (LAYOUT == 1 && nsteps > 0 && Hc) {
+    load_own(Hc + seg_of(0) * st, hn);
+  } else {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) hn[c] = 0.f;
+  }
 
   for (int jj = 0; jj < n; ++jj) {
     const int seg = seg_of(jj);
     const bool do_step = jj < nsteps;
-    // In place (out == H): each thread reads its H_seg elements before it
-    // writes out[seg] over the same addresses; no other thread touches them.
     float h[16];
-    if (do_step && Hc) {
+    if (LAYOUT == 1) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) h[c] = hn[c];
+    } else if (do_step && Hc) {
       load_own(Hc + seg * st, h);
     } else {
 #pragma unroll
@@ -464,6 +476,7 @@ __global__ void __launch_bounds__(2 * K) seq_simt_ksplit_kernel(const SeqJob j) 
     }
     if (Oc) store_own(Oc + seg * st, x);
     if (!do_step) break;
+    if (LAYOUT == 1 && jj + 1 < nsteps && Hc) load_own(Hc + seg_of(jj + 1) * st, hn);
     put_state(x);
     cp_async_wait<0>();  // this thread's copies of step jj's A have landed
     __syncthreads();     // everyone's, and the state tile is written; step jj-1 is done with copy (jj+1)&1
