@@ -514,9 +514,13 @@ def run_reference(args):
     t0 = time.perf_counter()
     _, _, threads = oracle.cp_correct(p["H"][:, :1], p["M"][:, :1], p["h0"][:, :1], p["layout"], p["direction"],
                                       return_threads=True)
-    one = time.perf_counter() - t0
+    one = time.perf_counter() - t0  # one head on one thread
+    # Each step runs a multiple of the thread count in heads (the oracle's
+    # threads take one head each), as many rounds as the per-step budget allows.
     budget = 150.0 / max(1, args.steps + args.warmup)
-    heads = max(1, min(HEADS, threads, int(budget / max(one, 1e-9))))
+    rounds = max(1, int(budget / max(one, 1e-9)))
+    heads = max(1, min(HEADS, threads * rounds))
+    cores = min(threads, heads)
     times = []
     for s in range(args.warmup + args.steps):
         q = probs[s % len(probs)]
@@ -532,7 +536,7 @@ def run_reference(args):
             "data": "synthetic (seeded; same inputs as the GPU arm)",
             "config": {"workload": WORKLOAD, "B": 1, "heads": HEADS, "K": K, "V": V, "S": S,
                        "calls_per_step": 1, "parallelism": "host threads"},
-            "cpu_baseline": {"value": round(us_per_call, 1), "unit": "us", "cores": threads, "kind": "oracle",
+            "cpu_baseline": {"value": round(us_per_call, 1), "unit": "us", "cores": cores, "kind": "oracle",
                              "sample": f"each step: {heads} of {HEADS} heads of one call (rotating over the "
                                        f"4 calls), scaled to a full call"},
             "e2e": {"value": round(us_per_call, 1), "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
