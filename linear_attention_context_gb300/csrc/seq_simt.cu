@@ -479,7 +479,11 @@ __global__ void __launch_bounds__(2 * K) seq_simt_ksplit_kernel(const SeqJob j) 
     if (LAYOUT == 1 && jj + 1 < nsteps && Hc) load_own(Hc + seg_of(jj + 1) * st, hn);
     put_state(x);
     cp_async_wait<0>();  // this thread's copies of step jj's A have landed
-    __syncthreads();     // everyone's, and the state tile is written; step jj-1 is done with copy (jj+1)&1
+    // Everyone's have, and the state tile is written.  Every thread is also past
+    // step jj-1: done with copy (jj+1)&1 (refilled next) and with its reads of
+    // the partial blocks (rewritten after this step's FMAs), so one barrier
+    // covers both hand-overs.
+    __syncthreads();
     if (jj + 1 < nsteps) issue_a(jj + 1);
 
     // acc[r][p] holds columns 2p, 2p + 1 of row r: packed fma.rn.f32x2, each
@@ -555,7 +559,6 @@ __global__ void __launch_bounds__(2 * K) seq_simt_ksplit_kernel(const SeqJob j) 
       x[4 * q + 2] = sum.z + h[4 * q + 2];
       x[4 * q + 3] = sum.w + h[4 * q + 3];
     }
-    __syncthreads();  // every owner has read the partials before the next step writes them
   }
   cp_async_wait<0>();  // no copy may land after the CTA is gone
   griddep_launch_dependents();
