@@ -103,10 +103,11 @@ __device__ __forceinline__ void store_run(float* p, const float (&a)[R]) {
   }
 }
 
-// Ring stages for K (75 KB of shared memory at most, with the state tile).
+// Ring stages: three, so two chunks are in flight while one is in use (at
+// K = 256, 108 KB of ring plus the 36 KB state tile; one CTA per SM).
 template <int K>
 __host__ __device__ constexpr int ring_stages() {
-  return K <= 64 ? 8 : 2;
+  return 3;
 }
 
 template <int R, int LAYOUT>
@@ -252,11 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1) seq_simt_kernel(const SeqJob j) {
 
     for (int kb = 0; kb < CH; ++kb) {
       const int c = jj * CH + kb;
-      __syncthreads();  // every thread is done with chunk c - 1, whose stage chunk c + D reuses; Xs written
+      // D + c groups are committed, chunk c's is the (c + 1)-th: with D - 1
+      // pending, this thread's copies of chunk c have landed.
+      cp_async_wait<D - 1>();
+      // Everyone's have, Xs is written, and every thread is done with chunk
+      // c - 1, whose stage chunk c + D reuses.
+      __syncthreads();
       if (c + D < total) issue_chunk(c + D);
       cp_async_commit();
-      cp_async_wait<D>();  // this thread's copies of chunk c have landed
-      __syncthreads();     // everyone's have
       const int kc = kb * 32;
       if (fwd) {  // m-major stage: R rows x 4 k per step of four k
         const float* Am = As + (c % NST) * SF + k0 * kStageMLd;
