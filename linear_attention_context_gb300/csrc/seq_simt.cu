@@ -15,14 +15,14 @@
 // each of its 256 threads accumulates R x 4 outputs (R = K / 32 consecutive
 // rows, 4 adjacent columns) in registers; the chunk is stored k-major, so per
 // k a thread reads its R values of A and its 4 of the state with vector loads.
-// The chunks go through a ring of NST stages filled with cp.async NST - 1
-// chunks ahead, across step boundaries
-// too (M does not depend on the state), so a chunk's global latency overlaps
-// the arithmetic of the chunks before it.  NST is 8 for K <= 64, where a step
-// has only one or two chunks and their latency dominates (config of 1 head,
-// K = V = 64, S = 4: 8.92 -> 8.56 us per call), and 2 above: at K = 128 with
-// 32 heads five stages measured up to 9 % slower (the larger shared-memory
-// carve-out leaves less L1 to the 4-byte cp.async copies and the H loads).
+// The chunks go through a ring of three stages filled with cp.async two
+// chunks ahead, across step boundaries too (M does not depend on the state),
+// so a chunk's global latency overlaps the arithmetic of the two chunks before
+// it; one barrier per chunk hands a landed chunk to every thread and frees the
+// stage of the chunk before.  This form serves K > 128; K <= 128 runs the
+// k-split form below.  At K = V = 256 (32 heads, S = 8) three stages with one
+// barrier per chunk measured 252.5 / 211.4 us forward / reverse against
+// 262.8 / 221.7 for two stages with two barriers per chunk.
 //
 // In-place (out == H): a thread reads its H_seg elements before it writes
 // out[seg] over the same addresses, and no other thread touches them.
