@@ -13,8 +13,10 @@
 // propagation matrix through shared memory in 32-wide k chunks of A (A = M
 // going forward, M^T in reverse), keeps the state tile in shared memory, and
 // each of its 256 threads accumulates R x 4 outputs (R = K / 32 consecutive
-// rows, 4 adjacent columns) in registers; the chunk is stored k-major, so per
-// k a thread reads its R values of A and its 4 of the state with vector loads.
+// rows, 4 adjacent columns) in registers.  A reverse chunk is stored k-major,
+// so per k a thread reads its R values of A and its 4 of the state with vector
+// loads; a forward chunk is stored m-major (16-byte copies of M's rows either
+// way), read as R rows x 4 k per step of four k.
 // The chunks go through a ring of three stages filled with cp.async two
 // chunks ahead, across step boundaries too (M does not depend on the state),
 // so a chunk's global latency overlaps the arithmetic of the two chunks before
